@@ -1,0 +1,120 @@
+"""BatchNorm2d training forward / apply / backward in float64 (oracle).
+
+Test infrastructure only; see ``oracle/__init__.py``.
+
+Sources
+-------
+Aether-ML PR #18, "perf(batchnorm): device-sized grid, one-pass statistics,
+finalize kernels":
+
+* section "One-pass statistics": the forward finalize writes per channel
+  (mean, var, inv_std, gamma * inv_std) and updates running_mean and
+  running_var in place; the apply is ``out = (x - mean) * scale + beta`` and
+  is shared by training and inference.
+* section "Backward finalize": grads = (dgamma, dbeta, k1, k2) with
+  ``k1 = -scale * inv_std^2 * sum(dy * (x - mean)) / N``,
+  ``k2 = -scale * dbeta / N`` and ``dx = dy * scale + (x - mean) * k1 + k2``.
+
+The one-pass shifted sums and the partials are how the GPU reaches these
+numbers; the quantities themselves have plain definitions, so this file
+writes the definitions out (two-pass variance, float64, no shift).
+
+Readings where the pages are silent
+-----------------------------------
+* ``N`` in k1/k2 is the per-channel element count ``M = B * H * W``.
+* The batch variance is biased (divides by M), as in the page's test that
+  compares it with "the float64 variance of the same data".
+* running_var takes the unbiased ``var * M / (M - 1)``; momentum follows
+  ``new = (1 - m) * old + m * batch`` (the PyTorch BatchNorm2d convention).
+"""
+
+import numpy as np
+
+
+def _bcs(x):
+    """View an NC... array as float64 [B, C, S] with S = product of the rest."""
+    x = np.asarray(x, dtype=np.float64)
+    if x.ndim < 2:
+        raise ValueError("batch norm input needs at least 2 dims (N, C, ...)")
+    return x.reshape(x.shape[0], x.shape[1], -1)
+
+
+def _channel(v):
+    """Broadcast a per-channel vector [C] against [B, C, S]."""
+    return np.asarray(v, dtype=np.float64)[None, :, None]
+
+
+def batch_norm_forward_train(x, gamma, beta, running_mean, running_var,
+                             momentum, eps):
+    """Training-mode forward.  Returns a dict of float64 arrays.
+
+    x: [B, C, ...]; gamma, beta, running_mean, running_var: [C].
+    Keys: y (shape of x), mean, var, inv_std, scale, running_mean,
+    running_var (all [C]).
+    """
+    x3 = _bcs(x)
+    B, C, S = x3.shape
+    M = B * S
+    gamma = np.asarray(gamma, dtype=np.float64)
+    beta = np.asarray(beta, dtype=np.float64)
+
+    mean = x3.sum(axis=(0, 2)) / M
+    centred = x3 - _channel(mean)
+    var = (centred * centred).sum(axis=(0, 2)) / M
+    inv_std = 1.0 / np.sqrt(var + eps)
+    scale = gamma * inv_std
+    y = centred * _channel(scale) + _channel(beta)
+
+    m = float(momentum)
+    new_rm = (1.0 - m) * np.asarray(running_mean, np.float64) + m * mean
+    new_rv = (1.0 - m) * np.asarray(running_var, np.float64) \
+        + m * var * (M / (M - 1.0))
+    return {
+        "y": y.reshape(np.shape(x)),
+        "mean": mean,
+        "var": var,
+        "inv_std": inv_std,
+        "scale": scale,
+        "running_mean": new_rm,
+        "running_var": new_rv,
+    }
+
+
+def batch_norm_apply(x, mean, scale, beta):
+    """Centred apply ``(x - mean) * scale + beta`` (inference form)."""
+    x3 = _bcs(x)
+    y = (x3 - _channel(mean)) * _channel(scale) + _channel(beta)
+    return y.reshape(np.shape(x))
+
+
+def batch_norm_backward(x, dy, gamma, eps):
+    """Training-mode backward given the forward's input.
+
+    mean and inv_std are recomputed from x in float64.  Returns a dict:
+    dx (shape of x), dgamma, dbeta, k1, k2 (all [C]).
+    """
+    x3 = _bcs(x)
+    dy3 = _bcs(dy)
+    B, C, S = x3.shape
+    M = B * S
+    gamma = np.asarray(gamma, dtype=np.float64)
+
+    mean = x3.sum(axis=(0, 2)) / M
+    centred = x3 - _channel(mean)
+    var = (centred * centred).sum(axis=(0, 2)) / M
+    inv_std = 1.0 / np.sqrt(var + eps)
+    scale = gamma * inv_std
+
+    dbeta = dy3.sum(axis=(0, 2))
+    sum_dy_xc = (dy3 * centred).sum(axis=(0, 2))
+    dgamma = sum_dy_xc * inv_std
+    k1 = -scale * inv_std * inv_std * sum_dy_xc / M
+    k2 = -scale * dbeta / M
+    dx = dy3 * _channel(scale) + centred * _channel(k1) + _channel(k2)
+    return {
+        "dx": dx.reshape(np.shape(x)),
+        "dgamma": dgamma,
+        "dbeta": dbeta,
+        "k1": k1,
+        "k2": k2,
+    }

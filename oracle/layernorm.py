@@ -1,0 +1,111 @@
+"""LayerNorm backward, plain and fused with bias+dropout+add (oracle).
+
+Test infrastructure only; see ``oracle/__init__.py``.
+
+Source: nvFuser issue #1473, "Why is LayerNorm Backward Segmenting?".
+
+* "A repro of the 3-Kernel layer_norm backward fusion" (nvfuser_fusion_id14)
+  is the plain LayerNorm backward.
+* "A repro of the 1-Kernel bias+dropout+add+layer_norm backward fusion"
+  (nvfuser_fusion_id9) is the same backward followed by the gradient of a
+  bias+dropout+add that produced the LayerNorm input.
+
+Decoding of the fusion definitions, per row of length H with saved mean mu
+and saved rstd rho (T5/T7 in the repros):
+
+    xhat  = (z - mu) * rho                      (T15)
+    g     = dy * gamma                          (T20)
+    dvar  = -1/2 * sum_j g * (z - mu) * rho^3   (T43)
+    dmean = -sum_j g * rho                      (T33/T44)
+    dz    = g*rho + 2*dvar*(z - mu)/H + dmean/H (T76)
+    dz   += dz_extra                            (T77; the extra fp32 gradient T2)
+    dgamma = sum_rows dy * xhat                 (T22)
+    dbeta  = sum_rows dy                        (T18)
+
+and, for the fused form where z = residual + dropout(input + bias):
+
+    dresidual = dz                              (T77)
+    dinput    = dz * scale * mask               (T78/T79)
+    dbias     = sum_rows dinput                 (T81)
+
+Readings where the pages are silent (the fusion definitions show the
+backward only): the forward is ``z = residual + mask * scale * (input +
+bias)``, the post-attention bias-dropout-add; ``dz_extra`` is optional.
+"""
+
+import numpy as np
+
+
+def _f64(a):
+    return None if a is None else np.asarray(a, dtype=np.float64)
+
+
+def dropout_add(inp, residual, bias, mask, scale):
+    """z = residual + mask * scale * (inp + bias), in float64.
+
+    bias may be None (no bias); mask may be None (everything kept).
+    """
+    inp = _f64(inp)
+    t = inp if bias is None else inp + _f64(bias)[None, :]
+    if mask is not None:
+        t = t * np.asarray(mask, dtype=np.float64)
+    return _f64(residual) + float(scale) * t
+
+
+def layer_norm_saved_stats(z, eps):
+    """Setup helper: per-row mean and rstd = 1/sqrt(biased var + eps)."""
+    z = _f64(z)
+    mu = z.mean(axis=1)
+    c = z - mu[:, None]
+    var = (c * c).mean(axis=1)
+    return mu, 1.0 / np.sqrt(var + eps)
+
+
+def _ln_core(dy, z, mean, rstd, gamma, dz_extra):
+    dy = _f64(dy)
+    z = _f64(z)
+    mu = _f64(mean)[:, None]
+    rho = _f64(rstd)[:, None]
+    gamma = _f64(gamma)[None, :]
+    H = z.shape[1]
+
+    centred = z - mu
+    xhat = centred * rho
+    g = dy * gamma
+    dvar = -0.5 * (g * centred).sum(axis=1, keepdims=True) * rho * rho * rho
+    dmean = -(g * rho).sum(axis=1, keepdims=True)
+    dz = g * rho + 2.0 * dvar * centred / H + dmean / H
+    if dz_extra is not None:
+        dz = dz + _f64(dz_extra)
+    dgamma = (dy * xhat).sum(axis=0)
+    dbeta = dy.sum(axis=0)
+    return dz, dgamma, dbeta
+
+
+def layer_norm_backward(dy, x, mean, rstd, gamma, dz_extra=None):
+    """Plain LayerNorm backward (nvfuser_fusion_id14).
+
+    Returns dict dx [R, H] (includes dz_extra when given), dgamma, dbeta [H].
+    """
+    dz, dgamma, dbeta = _ln_core(dy, x, mean, rstd, gamma, dz_extra)
+    return {"dx": dz, "dgamma": dgamma, "dbeta": dbeta}
+
+
+def fused_bias_dropout_add_layer_norm_backward(dy, inp, residual, bias, mask,
+                                               scale, mean, rstd, gamma,
+                                               dz_extra=None):
+    """Backward of LayerNorm(residual + dropout(inp + bias)) (fusion_id9).
+
+    The LayerNorm input z is recomputed from (inp, residual, bias, mask,
+    scale).  Returns dict dx (gradient of inp), dresidual, dbias, dgamma,
+    dbeta.  bias may be None (then dbias is returned as None); mask may be
+    None (everything kept).
+    """
+    z = dropout_add(inp, residual, bias, mask, scale)
+    dz, dgamma, dbeta = _ln_core(dy, z, mean, rstd, gamma, dz_extra)
+    dresidual = dz
+    keep = 1.0 if mask is None else np.asarray(mask, dtype=np.float64)
+    dx = dresidual * float(scale) * keep
+    dbias = None if bias is None else dx.sum(axis=0)
+    return {"dx": dx, "dresidual": dresidual, "dbias": dbias,
+            "dgamma": dgamma, "dbeta": dbeta}

@@ -1,0 +1,593 @@
+"""Benchmark of the normalization hot path on GB300 (one JSON line on rank 0).
+
+One step = one pass of every hot-path operation over its workload:
+
+  bn_f32_fwd   BatchNorm2d training forward  fp32 [256,32,32,32], |mean| <= 1000
+  bn_f32_bwd   BatchNorm2d training backward fp32 [256,32,32,32]
+  rms_bf16_bwd RMSNorm backward bf16 [2048, 8192]
+  rms_f32_bwd  RMSNorm backward fp32 [2048, 8192]
+  ln_bf16_bwd  bias+dropout+add+LayerNorm backward bf16 [16*512, 1600]
+  bn_bf16_fwd  BatchNorm2d training forward  bf16 [128,256,56,56]
+  bn_bf16_bwd  BatchNorm2d training backward bf16 [128,256,56,56]
+
+Every call goes through the C ABI (ctypes binding).  Each operation is timed
+with CUDA events on the stream it runs on, after a 256 MB write that flushes
+L2 (outside the events); BatchNorm phases (stats | finalize+apply, grad_sums
+| finalize+dx) are timed separately.  value = unique bytes of every input and
+output tensor of the step / summed device time (the effective-bandwidth
+convention), in GB/s, over all ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--ops a,b,...] [--no-e2e] [--no-cpu-baseline]
+
+Under torchrun each rank runs the same workload on its own GPU (replicas; the
+path needs no cross-GPU exchange); value sums the ranks' bytes over the
+slowest rank's time.  ``--impl reference`` times the float64 CPU oracle on a
+bounded sample of the same workload on the host cores (rank 0 only).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "norm fwd+bwd effective HBM GB/s and % of GB300 peak; µs per call"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+OPS_ALL = ["bn_f32_fwd", "bn_f32_bwd", "rms_bf16_bwd", "rms_f32_bwd", "ln_bf16_bwd",
+           "bn_bf16_fwd", "bn_bf16_bwd"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def aggregate(local_seconds, local_bytes, world):
+    """Whole-job numbers: max time over ranks, sum of bytes over ranks."""
+    if world == 1:
+        return local_seconds, local_bytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_seconds], dtype=torch.float64)
+    b = torch.tensor([local_bytes], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t, b = t.cuda(), b.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(b.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        # under load = samples above half the max clock (idle samples are low)
+        loaded = [v for v in sm if mx is None or v > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads
+
+class Op:
+    """One hot-path operation on its workload.
+
+    phases: list of (kernel-name, fn) run in order; each fn launches one
+    kernel-pair call of the C ABI on the current stream.
+    unique_bytes: bytes of every input and output tensor (algorithmic).
+    phase_bytes: algorithmic bytes per phase launch (for the roofline).
+    """
+
+    def __init__(self, name, desc, phases, unique_bytes, phase_bytes, launches,
+                 h2d, d2h, host_call):
+        self.name = name
+        self.desc = desc
+        self.phases = phases
+        self.unique_bytes = unique_bytes
+        self.phase_bytes = phase_bytes
+        self.launches = launches
+        self.h2d = h2d          # list of (pinned host tensor, device tensor)
+        self.d2h = d2h          # list of (device tensor, pinned host tensor)
+        self.host_call = host_call
+
+
+def _nbytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def _pin(t):
+    return t.contiguous().pin_memory()
+
+
+def build_ops(names, dev):
+    import torch
+    from bwd_bn_pass_gb300 import gbnorm as G, synth
+
+    ops = []
+    for name in names:
+        if name.startswith("bn_"):
+            case = synth.CASES["bn_offset_f32" if "f32" in name else "bn_offset_bf16"]
+            inp = synth.bn_inputs(case)
+            hx, hdy = _pin(inp["x"]), _pin(inp["dy"])
+            x, dy = hx.to(dev), hdy.to(dev)
+            g, b = inp["gamma"].to(dev), inp["beta"].to(dev)
+            rm, rv = inp["running_mean"].to(dev), inp["running_var"].to(dev)
+            C = x.shape[1]
+            y = torch.empty_like(x)
+            stats = G.bn_stats_tensor(C, dev)
+            ws = G.bn_workspace(x)
+            # a forward once so the backward has valid stats
+            G.bn_forward_train(x, g, b, rm, rv, case.momentum, case.eps, y=y, stats=stats,
+                               ws=ws)
+            T = _nbytes(x)
+            small = _nbytes(g, b, rm, rv) + 4 * C * 4
+            shape = "x".join(map(str, case.shape))
+            if name.endswith("fwd"):
+                phases = [
+                    ("bn_stats", lambda x=x, ws=ws: G.bn_stats(x, ws)),
+                    ("bn_finalize_apply",
+                     lambda x=x, g=g, b=b, rm=rm, rv=rv, y=y, stats=stats, ws=ws, c=case:
+                     G.bn_finalize_apply(x, g, b, rm, rv, c.momentum, c.eps, y, stats, ws)),
+                ]
+                hy = torch.empty_like(hx).pin_memory()
+                ops.append(Op(name, f"BatchNorm2d fwd {case.dtype} [{shape}]", phases,
+                              2 * T + small, {"bn_stats": T, "bn_finalize_apply": 2 * T}, 2,
+                              [(hx, x)], [(y, hy)], None))
+            else:
+                dx = torch.empty_like(x)
+                grads = torch.empty(4 * C, dtype=torch.float32, device=dev)
+                phases = [
+                    ("bn_grad_sums", lambda x=x, dy=dy, s=stats, ws=ws:
+                     G.bn_grad_sums(x, dy, s, ws)),
+                    ("bn_finalize_dx", lambda x=x, dy=dy, s=stats, dx=dx, gr=grads, ws=ws:
+                     G.bn_finalize_dx(x, dy, s, dx, gr, ws)),
+                ]
+                hdx = torch.empty_like(hx).pin_memory()
+                ops.append(Op(name, f"BatchNorm2d bwd {case.dtype} [{shape}]", phases,
+                              3 * T + 8 * C * 4 + 4 * C * 4,
+                              {"bn_grad_sums": 2 * T, "bn_finalize_dx": 3 * T}, 2,
+                              [(hx, x), (hdy, dy)], [(dx, hdx)], None))
+        elif name.startswith("rms_"):
+            case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]
+            inp = synth.rms_inputs(case)
+            hx, hdy, hw = _pin(inp["x"]), _pin(inp["dy"]), _pin(inp["w"])
+            x, dy, w = hx.to(dev), hdy.to(dev), hw.to(dev)
+            rstd = torch.rsqrt(x.double().pow(2).mean(dim=1) + case.eps).float()
+            hr = _pin(rstd.cpu())
+            dx = torch.empty_like(x)
+            dw = torch.empty_like(w)
+            ws = G.rowwise_workspace(case.rows, case.hidden, G.GBN_ROW_RMS, x.dtype, dev)
+            phases = [("rms_bwd", lambda dy=dy, x=x, w=w, rstd=rstd, dx=dx, dw=dw, ws=ws:
+                        G.rmsnorm_backward(dy, x, w, rstd, dx=dx, dw=dw, ws=ws))]
+            ub = _nbytes(x, dy, dx, w, dw, rstd)
+            hdx, hdw = torch.empty_like(hx).pin_memory(), torch.empty_like(hw).pin_memory()
+            ops.append(Op(name, f"RMSNorm bwd {case.dtype} [{case.rows}x{case.hidden}]",
+                          phases, ub, {"rms_bwd": ub}, 2, [(hx, x), (hdy, dy), (hw, w), (hr, rstd)],
+                          [(dx, hdx), (dw, hdw)], None))
+        elif name.startswith("ln_"):
+            case = synth.CASES["ln_fused_bf16"]
+            inp = synth.ln_inputs(case)
+            host = {k: _pin(v) for k, v in inp.items() if torch.is_tensor(v)}
+            d = {k: v.to(dev) for k, v in host.items()}
+            s = inp["dropout_scale"]
+            z = (d["residual"].float() + d["mask"].float() * s
+                 * (d["inp"].float() + d["bias"].float()))
+            mean = z.mean(dim=1)
+            rstd = torch.rsqrt(z.var(dim=1, unbiased=False) + case.eps)
+            del z
+            host["mean"], host["rstd"] = _pin(mean.cpu()), _pin(rstd.cpu())
+            d["mean"], d["rstd"] = mean, rstd
+            dx, dres = torch.empty_like(d["inp"]), torch.empty_like(d["inp"])
+            dg, db, dbias = (torch.empty_like(d["gamma"]) for _ in range(3))
+            ws = G.rowwise_workspace(case.rows, case.hidden, G.GBN_ROW_LN_FUSED,
+                                     d["inp"].dtype, dev)
+            phases = [("ln_bwd", lambda d=d, s=s, dx=dx, dres=dres, dg=dg, db=db, dbias=dbias,
+                        ws=ws: G.layernorm_backward(
+                            d["dy"], d["inp"], d["mean"], d["rstd"], d["gamma"],
+                            residual=d["residual"], bias=d["bias"], mask=d["mask"],
+                            dropout_scale=s, dx=dx, dresidual=dres, dgamma=dg, dbeta=db,
+                            dbias=dbias, ws=ws))]
+            ub = _nbytes(d["dy"], d["inp"], d["residual"], d["mask"], d["mean"], d["rstd"],
+                         d["gamma"], d["bias"], dx, dres, dg, db, dbias)
+            order = ["dy", "inp", "residual", "mask", "mean", "rstd", "gamma", "bias"]
+            outs = [(t, torch.empty_like(t, device="cpu").pin_memory())
+                    for t in (dx, dres, dg, db, dbias)]
+            ops.append(Op(name, f"bias+dropout+add+LayerNorm bwd bf16 "
+                          f"[{case.rows}x{case.hidden}]", phases, ub, {"ln_bwd": ub}, 2,
+                          [(host[k], d[k]) for k in order], outs, None))
+        else:
+            raise ValueError(f"unknown op {name}")
+    return ops
+
+
+# ------------------------------------------------------------- our arm
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bwd_bn_pass_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as fh:
+            h.update(fn.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was captured from the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    v = d.get("per_launch_dram_bytes", {}).get(kernel)
+    return None if v is None else float(v)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from bwd_bn_pass_gb300 import build, gbnorm
+
+    if not os.path.exists(gbnorm.library_path()):
+        build.build_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    gbnorm.init(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    names = args.ops.split(",") if args.ops else OPS_ALL
+    ops = build_ops(names, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def one_step(record):
+        for op in ops:
+            flush.zero_()
+            evs = [torch.cuda.Event(enable_timing=True)]
+            evs[0].record(stream)
+            for _, fn in op.phases:
+                fn()
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                evs.append(e)
+            record.append((op, evs))
+
+    for _ in range(args.warmup):
+        one_step([])
+    barrier()
+    rec = []
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            one_step(rec)
+        barrier()
+        wall = time.perf_counter() - t0
+    clocks = clk.summary()
+
+    per_op = {op.name: [] for op in ops}
+    per_phase = {}
+    for op, evs in rec:
+        per_op[op.name].append(evs[0].elapsed_time(evs[-1]) * 1e-3)
+        for i, (pname, _) in enumerate(op.phases):
+            per_phase.setdefault((op.name, pname), []).append(
+                evs[i].elapsed_time(evs[i + 1]) * 1e-3)
+    step_s = sum(statistics.mean(v) for v in per_op.values())
+    step_bytes = sum(op.unique_bytes for op in ops)
+    job_s, job_bytes = aggregate(step_s, step_bytes, world)
+    value = job_bytes / job_s / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # dominant kernel: the phase with the largest share of the step
+    (dop, dphase), dtimes = max(per_phase.items(), key=lambda kv: statistics.mean(kv[1]))
+    dmean = statistics.mean(dtimes)
+    dbytes = next(op.phase_bytes[dphase] for op in ops if op.name == dop)
+    achieved = dbytes / dmean / 1e9
+    roofline = {"bound": "hbm", "kernel": f"{dphase} ({dop})", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_kind == "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": dbytes,
+                "traffic": recorded_traffic(f"{dop}:{dphase}")}
+
+    ops_out = {}
+    for op in ops:
+        t = statistics.mean(per_op[op.name])
+        ops_out[op.name] = {
+            "desc": op.desc, "us": round(t * 1e6, 2),
+            "us_min": round(min(per_op[op.name]) * 1e6, 2),
+            "unique_bytes": op.unique_bytes,
+            "eff_gbs": round(op.unique_bytes / t / 1e9, 1),
+            "frac_of_measured_peak": round(op.unique_bytes / t / 1e9 / peak, 4),
+            "phases_us": {p: round(statistics.mean(per_phase[(op.name, p)]) * 1e6, 2)
+                          for p, _ in op.phases},
+        }
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(ops, stream, dev, args.steps, world)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(job_s * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, the pages' value laws)",
+        "config": {
+            "workload": "; ".join(op.desc for op in ops),
+            "ops": names,
+            "l2": "256 MB write before every operation (outside the timed events)",
+            "timing": "CUDA events per operation on the launching stream; sum over ops",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "pct_of_measured_peak": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "ops": ops_out,
+        "roofline": roofline,
+        "gpu_launches": sum(op.launches for op in ops) * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return line
+
+
+def run_e2e(ops, stream, dev, steps, world):
+    """Same metric through the C ABI with host buffers: per step every op
+    copies its inputs from pinned host memory, runs, and copies its outputs
+    back, all inside the timed region."""
+    import torch
+    h2d = sum(_nbytes(h) for op in ops for h, _ in op.h2d)
+    d2h = sum(_nbytes(h) for op in ops for _, h in op.d2h)
+    times = []
+    for it in range(steps + 1):
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for op in ops:
+            for h, d in op.h2d:
+                d.copy_(h, non_blocking=True)
+            for _, fn in op.phases:
+                fn()
+            for d, h in op.d2h:
+                h.copy_(d, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if it > 0:
+            times.append(a.elapsed_time(b) * 1e-3)
+    t = statistics.mean(times)
+    step_bytes = sum(op.unique_bytes for op in ops)
+    job_s, job_bytes = aggregate(t, step_bytes, world)
+    return {"value": round(job_bytes / job_s / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(job_s * 1e3, 3)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """A bounded sample of every op's workload, prepared once as float64
+    arrays for the oracle: BatchNorm on the first `bn_channels` channels (all
+    batches and pixels), RMSNorm / LayerNorm on the first rows.  `time_pass`
+    runs the oracle once over all ops and returns (unique storage bytes of
+    the sample, seconds of oracle time)."""
+
+    def __init__(self, bn_f32_channels, bn_bf16_channels, rms_rows, ln_rows):
+        import numpy as np
+        import oracle
+        from bwd_bn_pass_gb300 import synth
+
+        self.items = []
+        self.desc = {}
+        for name in OPS_ALL:
+            if name.startswith("bn_"):
+                case = synth.CASES["bn_offset_f32" if "f32" in name else "bn_offset_bf16"]
+                k = bn_f32_channels if "f32" in name else bn_bf16_channels
+                inp = synth.bn_inputs(case)
+                x = inp["x"][:, :k].double().numpy()
+                dy = inp["dy"][:, :k].double().numpy()
+                g = inp["gamma"][:k].double().numpy()
+                b = inp["beta"][:k].double().numpy()
+                esz = inp["x"].element_size()
+                if name.endswith("fwd"):
+                    fn = (lambda x=x, g=g, b=b, k=k, c=case: oracle.batch_norm_forward_train(
+                        x, g, b, np.zeros(k), np.ones(k), c.momentum, c.eps))
+                    nb = 2 * x.size * esz
+                else:
+                    fn = lambda x=x, dy=dy, g=g, c=case: oracle.batch_norm_backward(x, dy, g, c.eps)
+                    nb = 3 * x.size * esz
+                self.desc[name] = f"{k}/{case.shape[1]} channels"
+            elif name.startswith("rms_"):
+                case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]
+                inp = synth.rms_inputs(case)
+                x = inp["x"][:rms_rows].double().numpy()
+                dy = inp["dy"][:rms_rows].double().numpy()
+                w = inp["w"].double().numpy()
+                rstd = oracle.rms_norm_rstd(x, case.eps)
+                fn = lambda x=x, dy=dy, w=w, r=rstd: oracle.rms_norm_backward(x, dy, w, r)
+                nb = 3 * x.size * inp["x"].element_size()
+                self.desc[name] = f"{rms_rows}/{case.rows} rows"
+            else:
+                case = synth.CASES["ln_fused_bf16"]
+                inp = synth.ln_inputs(case)
+                f = {n: inp[n][:ln_rows].double().numpy()
+                     for n in ("inp", "residual", "dy", "mask")}
+                bias = inp["bias"].double().numpy()
+                gamma = inp["gamma"].double().numpy()
+                s = inp["dropout_scale"]
+                z = oracle.dropout_add(f["inp"], f["residual"], bias, f["mask"], s)
+                mu, rs = oracle.layer_norm_saved_stats(z, case.eps)
+                fn = (lambda f=f, bias=bias, gamma=gamma, s=s, mu=mu, rs=rs:
+                      oracle.fused_bias_dropout_add_layer_norm_backward(
+                          f["dy"], f["inp"], f["residual"], bias, f["mask"], s, mu, rs, gamma))
+                nb = ln_rows * case.hidden * (5 * 2 + 1)
+                self.desc[name] = f"{ln_rows}/{case.rows} rows"
+            self.items.append((name, fn, nb))
+
+    def time_pass(self):
+        nb, secs = 0, 0.0
+        for _, fn, b in self.items:
+            t0 = time.perf_counter()
+            fn()
+            secs += time.perf_counter() - t0
+            nb += b
+        return nb, secs
+
+    def describe(self):
+        return ", ".join(f"{k} {v}" for k, v in self.desc.items())
+
+
+def cpu_baseline(budget_s):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    step (about `budget_s` seconds of oracle time)."""
+    sample = OracleSample(bn_f32_channels=32, bn_bf16_channels=32, rms_rows=2048,
+                          ln_rows=8192)
+    nb, secs, passes = 0, 0.0, 0
+    while secs < budget_s and passes < 8:
+        b, s = sample.time_pass()
+        nb += b
+        secs += s
+        passes += 1
+    return {"value": round(nb / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "float64 numpy oracle, one thread; per op: " + sample.describe()
+            + f"; {passes} pass(es)", "seconds": round(secs, 2)}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is one bounded sample."""
+    if rank != 0:
+        return None
+    sample = OracleSample(bn_f32_channels=8, bn_bf16_channels=8, rms_rows=256, ln_rows=1024)
+    for _ in range(args.warmup):
+        sample.time_pass()
+    nb, secs = 0, 0.0
+    for _ in range(args.steps):
+        b, s = sample.time_pass()
+        nb += b
+        secs += s
+    value = nb / secs / 1e9
+    desc = "float64 numpy oracle, one thread; per step: " + sample.describe()
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, the pages' value laws)",
+        "config": {"workload": "bounded sample of: " + "; ".join(OPS_ALL), "ops": OPS_ALL},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ops", default="")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,562 @@
+// BatchNorm2d training forward / backward kernels (NCHW).
+//
+// Method: Aether-ML PR #18 "perf(batchnorm): device-sized grid, one-pass
+// statistics, finalize kernels".
+//   * "Reduction grid": a grid of (C, grid_y) 256-thread blocks that fills
+//     every resident block slot once; block (c, j) owns a contiguous slice of
+//     channel c's M = B*HW elements.
+//   * "One-pass statistics": each block sums d = x - x[0,c,0] and d*d and
+//     writes its pair to partials[2, grid_y, C] -- no atomics, no zero-init.
+//     The finalize reduces the partials into stats (mean, var, inv_std,
+//     gamma*inv_std) and updates the running statistics; the apply is the
+//     centred form (x - mean)*scale + beta.
+//   * "Backward finalize": grad_sums partials (sum dy, sum dy*(x - mean)),
+//     finalize to grads (dgamma, dbeta, k1, k2), dx = dy*scale + (x-mean)*k1
+//     + k2.
+//
+// GB300 design (differs from the page's three launches per direction):
+//   * Two launches per direction.  The finalize is the prologue of the
+//     consuming kernel: every block of channel c reduces that channel's
+//     partials in the same fixed order (so all blocks hold bit-identical
+//     values), and block j = 0 writes stats/grads and the running update.
+//     The consumer is launched with programmatic dependent launch: it loads
+//     its first vectors of x (and dy) before griddepcontrol.wait.
+//   * Partials are fp64.  Per thread, sums are double-fp32 (TwoSum); the
+//     backward also keeps each product's FMA residual and, for fp32 inputs,
+//     the rounding error of x - shift, so sum dy*(x - mean) is accurate even
+//     when it nearly cancels.  The backward forms S = sum dy*(x - shift) -
+//     (mean - shift)*sum dy in fp64 from the forward's fp64 (mean - shift).
+//   * The consumer walks its slice in reverse, so the tail that the producer
+//     read last (still in L2) is read first.
+#include "gbn_common.cuh"
+#include "gbn_internal.h"
+
+namespace gbn {
+
+namespace {
+
+// Geometry of one launch.  Vector offsets are in units of VEC elements from
+// the tensor base; I is uint32_t unless the tensor has >= 2^32 vectors.
+struct BnGeom {
+  uint64_t step;   // offset change for +blockDim vectors of a channel, no wrap
+  uint64_t wrap;   // extra change when the in-plane index wraps: C*Pv - Pv
+  int64_t P;       // plane size in elements (x[0, c, 0] is element c*P)
+  double M;        // per-channel count
+  int32_t C;
+  int32_t Pv;      // vectors per plane
+  int32_t Mv;      // vectors per channel
+  int32_t grid_y;
+  int32_t tmod;    // blockDim % Pv
+};
+
+template <typename I>
+struct Cursor {
+  I vo;       // vector offset from the tensor base
+  int32_t p;  // vector index inside the (b, c) plane
+};
+
+template <typename I>
+__device__ __forceinline__ Cursor<I> cursor_at(const BnGeom& g, int c, int32_t v) {
+  const int32_t b = v / g.Pv;
+  Cursor<I> q;
+  q.p = v - b * g.Pv;
+  q.vo = ((I)b * (I)g.C + (I)c) * (I)g.Pv + (I)q.p;
+  return q;
+}
+template <typename I>
+__device__ __forceinline__ void cursor_fwd(Cursor<I>& q, const BnGeom& g) {
+  q.p += g.tmod;
+  q.vo += (I)g.step;
+  if (q.p >= g.Pv) { q.p -= g.Pv; q.vo += (I)g.wrap; }
+}
+template <typename I>
+__device__ __forceinline__ void cursor_back(Cursor<I>& q, const BnGeom& g) {
+  q.p -= g.tmod;
+  q.vo -= (I)g.step;
+  if (q.p < 0) { q.p += g.Pv; q.vo -= (I)g.wrap; }
+}
+
+// Block j's slice [v0, v1) of the channel's vectors and this thread's count
+// of vectors in it (stride blockDim).
+__device__ __forceinline__ void slice(const BnGeom& g, int j, int32_t& v0, int32_t& cnt) {
+  v0 = (int32_t)((int64_t)g.Mv * j / g.grid_y);
+  const int32_t v1 = (int32_t)((int64_t)g.Mv * (j + 1) / g.grid_y);
+  const int32_t n = v1 - v0 - (int32_t)threadIdx.x;
+  cnt = n > 0 ? (n + kBnThreads - 1) / kBnThreads : 0;
+}
+
+// Channel c's partials summed over j in a fixed order by warp 0 (all lanes
+// end with the same values: xor-shuffle trees are symmetric).
+__device__ __forceinline__ void reduce_partials(const double* part, const BnGeom& g, int c,
+                                                double& s0, double& s1) {
+  const int lane = threadIdx.x & 31;
+  double a = 0.0, b = 0.0;
+  for (int jj = lane; jj < g.grid_y; jj += 32) {
+    a += part[(int64_t)jj * g.C + c];
+    b += part[((int64_t)g.grid_y + jj) * g.C + c];
+  }
+  s0 = warp_sum(a);
+  s1 = warp_sum(b);
+}
+
+template <typename T>
+__device__ __forceinline__ void x_minus_shift(float e, float shift, float& d, float& d_lo) {
+  d = e - shift;
+  if constexpr (sizeof(T) == 4) {
+    // rounding error of the subtraction (TwoSum); zero when exact
+    const float bb = d - e;
+    d_lo = (e - (d - bb)) + (-shift - bb);
+  } else {
+    d_lo = 0.f;  // bf16 operands: the fp32 difference is exact
+  }
+}
+
+// ------------------------------------------------------------- stats --
+
+// Blocks of 256 threads sized for 8 resident blocks per SM (<= 32
+// registers/thread): vectors stay raw until used.  Vectors in flight per
+// thread: stats 4, apply 2, grad_sums 2 of each input, dx 1 of each input
+// (the most the 32-register budget holds without spilling).
+constexpr int kUStats = 4;
+constexpr int kUApply = 2;
+constexpr int kUSums = 2;
+constexpr int kUDx = 1;
+
+template <typename T, int VEC, typename I>
+__global__ void __launch_bounds__(kBnThreads, 8)
+    bn_stats_kernel(const T* __restrict__ x, BnGeom g, double* __restrict__ part) {
+  using V = Vec<T, VEC>;
+  __shared__ double red[64];
+  pdl_launch_dependents();
+  const int c = blockIdx.x, j = blockIdx.y;
+  int32_t v0, cnt;
+  slice(g, j, v0, cnt);
+  const float shift = to_f32(x[(int64_t)c * g.P]);
+
+  DF s1 = {0.f, 0.f}, s2 = {0.f, 0.f};
+  Cursor<I> q = cursor_at<I>(g, c, v0 + (int32_t)threadIdx.x);
+  for (int32_t i = 0; i < cnt; i += kUStats) {
+    typename V::raw r[kUStats];
+#pragma unroll
+    for (int u = 0; u < kUStats; ++u) {
+      if (i + u < cnt) r[u] = V::ld(x + (size_t)q.vo * VEC);
+      cursor_fwd(q, g);
+    }
+#pragma unroll
+    for (int u = 0; u < kUStats; ++u) {
+      if (i + u < cnt) {
+        float e[VEC];
+        V::cvt(r[u], e);
+        float a1 = 0.f, a2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+          const float d = e[k] - shift;
+          a1 += d;
+          a2 = fmaf(d, d, a2);
+        }
+        df_add(s1, a1);
+        df_add(s2, a2);
+      }
+    }
+  }
+  double t1 = df_value(s1), t2 = df_value(s2);
+  block_sum2(t1, t2, red);
+  if (threadIdx.x == 0) {
+    part[(int64_t)j * g.C + c] = t1;
+    part[((int64_t)g.grid_y + j) * g.C + c] = t2;
+  }
+}
+
+// ------------------------------------------------- finalize + apply --
+
+struct ApplyArgs {
+  int mode;
+  const double* part;
+  const float* gamma;
+  const float* beta;
+  float* stats;
+  float* running_mean;
+  float* running_var;
+  float momentum;
+  float eps;
+  const float* mean;
+  const float* scale;
+};
+
+// Warp 0 computes (shift, mean - shift, scale, beta) for channel c; in
+// training mode this is the forward finalize, and block j = 0 also writes
+// the stats rows and the running-statistics update.
+__device__ __noinline__ void apply_prologue(const BnGeom& g, const ApplyArgs& a, int c, int j,
+                                               float shift_x, float* fin) {
+  float shift, mean_d, scale;
+  const float beta = a.beta ? a.beta[c] : 0.f;
+  if (a.mode == kApplyTrain) {
+    double s1, s2;
+    reduce_partials(a.part, g, c, s1, s2);
+    const double md = s1 / g.M;
+    double var = s2 / g.M - md * md;
+    if (var < 0.0) var = 0.0;
+    const double inv_std = 1.0 / sqrt(var + (double)a.eps);
+    const double sc = (a.gamma ? (double)a.gamma[c] : 1.0) * inv_std;
+    shift = shift_x;
+    mean_d = (float)md;
+    scale = (float)sc;
+    if (j == 0 && threadIdx.x == 0) {
+      const int64_t C = g.C;
+      const double mean = (double)shift + md;
+      a.stats[c] = (float)mean;
+      a.stats[C + c] = (float)var;
+      a.stats[2 * C + c] = (float)inv_std;
+      a.stats[3 * C + c] = scale;
+      a.stats[4 * C + c] = shift;
+      a.stats[5 * C + c] = mean_d;
+      reinterpret_cast<double*>(a.stats + 6 * C)[c] = md;
+      const double m = (double)a.momentum;
+      if (a.running_mean) a.running_mean[c] = (float)((1.0 - m) * a.running_mean[c] + m * mean);
+      if (a.running_var)
+        a.running_var[c] = (float)((1.0 - m) * a.running_var[c] + m * var * (g.M / (g.M - 1.0)));
+    }
+  } else if (a.mode == kApplyStats) {
+    const int64_t C = g.C;
+    shift = a.stats[4 * C + c];
+    mean_d = a.stats[5 * C + c];
+    scale = a.stats[3 * C + c];
+  } else {
+    shift = a.mean[c];
+    mean_d = 0.f;
+    scale = a.scale[c];
+  }
+  if (threadIdx.x == 0) { fin[0] = shift; fin[1] = mean_d; fin[2] = scale; fin[3] = beta; }
+}
+
+template <typename T, int VEC, typename I>
+__global__ void __launch_bounds__(kBnThreads, 8)
+    bn_apply_kernel(const T* __restrict__ x, T* y, BnGeom g, ApplyArgs a) {
+  using V = Vec<T, VEC>;
+  __shared__ float fin[4];  // shift, mean_d, scale, beta
+  const int c = blockIdx.x, j = blockIdx.y;
+  int32_t v0, cnt;
+  slice(g, j, v0, cnt);
+
+  // Walk this thread's vectors backwards (the stats pass read the slice
+  // tails last, so they are the likeliest to be in L2); load the first batch
+  // before waiting on the stats grid (x is never written by it).
+  const int32_t vlast = v0 + (int32_t)threadIdx.x + (cnt > 0 ? cnt - 1 : 0) * kBnThreads;
+  Cursor<I> q = cursor_at<I>(g, c, vlast);
+  typename V::raw r[kUApply];
+  I off[kUApply];
+#pragma unroll
+  for (int u = 0; u < kUApply; ++u) {
+    off[u] = q.vo;
+    if (u < cnt) r[u] = V::ld(x + (size_t)q.vo * VEC);
+    cursor_back(q, g);
+  }
+
+  if (a.mode == kApplyTrain) pdl_wait();
+  if (threadIdx.x < 32) apply_prologue(g, a, c, j, to_f32(x[(int64_t)c * g.P]), fin);
+  __syncthreads();
+  const float shift = fin[0], mean_d = fin[1], scale = fin[2], beta = fin[3];
+
+  for (int32_t i = 0; i < cnt; i += kUApply) {
+#pragma unroll
+    for (int u = 0; u < kUApply; ++u) {
+      if (i + u < cnt) {
+        float e[VEC];
+        V::cvt(r[u], e);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) e[k] = fmaf((e[k] - shift) - mean_d, scale, beta);
+        V::store(y + (size_t)off[u] * VEC, e);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUApply; ++u) {
+      off[u] = q.vo;
+      if (i + kUApply + u < cnt) r[u] = V::ld(x + (size_t)q.vo * VEC);
+      cursor_back(q, g);
+    }
+  }
+}
+
+// --------------------------------------------------------- grad_sums --
+
+template <typename T, int VEC, typename I>
+__global__ void __launch_bounds__(kBnThreads, 8)
+    bn_grad_sums_kernel(const T* __restrict__ x, const T* __restrict__ dy, BnGeom g,
+                        const float* __restrict__ stats, double* __restrict__ part) {
+  using V = Vec<T, VEC>;
+  __shared__ double red[64];
+  pdl_launch_dependents();
+  const int c = blockIdx.x, j = blockIdx.y;
+  int32_t v0, cnt;
+  slice(g, j, v0, cnt);
+  const float shift = stats[4 * (int64_t)g.C + c];
+
+  DF s0 = {0.f, 0.f}, s1 = {0.f, 0.f};
+  Cursor<I> q = cursor_at<I>(g, c, v0 + (int32_t)threadIdx.x);
+  for (int32_t i = 0; i < cnt; i += kUSums) {
+    typename V::raw rx[kUSums], rd[kUSums];
+#pragma unroll
+    for (int u = 0; u < kUSums; ++u) {
+      if (i + u < cnt) {
+        rx[u] = V::ld(x + (size_t)q.vo * VEC);
+        rd[u] = V::ld(dy + (size_t)q.vo * VEC);
+      }
+      cursor_fwd(q, g);
+    }
+#pragma unroll
+    for (int u = 0; u < kUSums; ++u) {
+      if (i + u < cnt) {
+        float ex[VEC], ed[VEC];
+        V::cvt(rx[u], ex);
+        V::cvt(rd[u], ed);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+          float d, d_lo;
+          x_minus_shift<T>(ex[k], shift, d, d_lo);
+          df_add(s0, ed[k]);
+          df_add_prod(s1, ed[k], d);
+          if constexpr (sizeof(T) == 4) s1.lo = fmaf(ed[k], d_lo, s1.lo);
+        }
+      }
+    }
+  }
+  double t0 = df_value(s0), t1 = df_value(s1);
+  block_sum2(t0, t1, red);
+  if (threadIdx.x == 0) {
+    part[(int64_t)j * g.C + c] = t0;
+    part[((int64_t)g.grid_y + j) * g.C + c] = t1;
+  }
+}
+
+// ---------------------------------------------------- finalize + dx --
+
+// Warp 0: the backward finalize for channel c (block j = 0 writes grads).
+__device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
+                                            const double* part, float* grads, int c, int j,
+                                            float* fin) {
+  double p0, p1;
+  reduce_partials(part, g, c, p0, p1);
+  const int64_t C = g.C;
+  const double inv_std = stats[2 * C + c];
+  const double scale = stats[3 * C + c];
+  const double md = reinterpret_cast<const double*>(stats + 6 * C)[c];
+  const double S = p1 - md * p0;  // sum dy*(x - mean)
+  const double k1 = -scale * inv_std * inv_std * S / g.M;
+  const double k2 = -scale * p0 / g.M;
+  if (j == 0 && threadIdx.x == 0) {
+    grads[c] = (float)(S * inv_std);
+    grads[C + c] = (float)p0;
+    grads[2 * C + c] = (float)k1;
+    grads[3 * C + c] = (float)k2;
+  }
+  if (threadIdx.x == 0) {
+    fin[0] = stats[4 * C + c];
+    fin[1] = stats[5 * C + c];
+    fin[2] = (float)scale;
+    fin[3] = (float)k1;
+    fin[4] = (float)k2;
+  }
+}
+
+template <typename T, int VEC, typename I>
+__global__ void __launch_bounds__(kBnThreads, 8)
+    bn_dx_kernel(const T* __restrict__ x, const T* dy, T* dx, BnGeom g,
+                 const float* __restrict__ stats, const double* __restrict__ part,
+                 float* __restrict__ grads) {
+  using V = Vec<T, VEC>;
+  __shared__ float fin[5];  // shift, mean_d, scale, k1, k2
+  const int c = blockIdx.x, j = blockIdx.y;
+  int32_t v0, cnt;
+  slice(g, j, v0, cnt);
+
+  const int32_t vlast = v0 + (int32_t)threadIdx.x + (cnt > 0 ? cnt - 1 : 0) * kBnThreads;
+  Cursor<I> q = cursor_at<I>(g, c, vlast);
+  typename V::raw rx[kUDx], rd[kUDx];
+  I off[kUDx];
+#pragma unroll
+  for (int u = 0; u < kUDx; ++u) {
+    off[u] = q.vo;
+    if (u < cnt) {
+      rx[u] = V::ld(x + (size_t)q.vo * VEC);
+      rd[u] = V::ld(dy + (size_t)q.vo * VEC);
+    }
+    cursor_back(q, g);
+  }
+
+  pdl_wait();
+  if (threadIdx.x < 32) dx_prologue(g, stats, part, grads, c, j, fin);
+  __syncthreads();
+  const float shift = fin[0], mean_d = fin[1], scale = fin[2], k1 = fin[3], k2 = fin[4];
+
+  for (int32_t i = 0; i < cnt; i += kUDx) {
+#pragma unroll
+    for (int u = 0; u < kUDx; ++u) {
+      if (i + u < cnt) {
+        float ex[VEC], ed[VEC];
+        V::cvt(rx[u], ex);
+        V::cvt(rd[u], ed);
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+          const float xc = (ex[k] - shift) - mean_d;
+          ex[k] = fmaf(ed[k], scale, fmaf(xc, k1, k2));
+        }
+        V::store(dx + (size_t)off[u] * VEC, ex);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUDx; ++u) {
+      off[u] = q.vo;
+      if (i + kUDx + u < cnt) {
+        rx[u] = V::ld(x + (size_t)q.vo * VEC);
+        rd[u] = V::ld(dy + (size_t)q.vo * VEC);
+      }
+      cursor_back(q, g);
+    }
+  }
+}
+
+BnGeom make_geom(const BnPlan& p) {
+  BnGeom g;
+  const int64_t Pv = p.P / p.vec;
+  g.P = p.P;
+  g.C = (int32_t)p.C;
+  g.Pv = (int32_t)Pv;
+  g.Mv = (int32_t)(p.B * Pv);
+  g.grid_y = p.grid_y;
+  g.tmod = (int32_t)(kBnThreads % Pv);
+  g.step = (uint64_t)(kBnThreads / Pv) * (uint64_t)p.C * (uint64_t)Pv + (uint64_t)g.tmod;
+  g.wrap = (uint64_t)p.C * (uint64_t)Pv - (uint64_t)Pv;
+  g.M = (double)p.M;
+  return g;
+}
+
+dim3 bn_grid(const BnPlan& p) { return dim3((unsigned)p.C, (unsigned)p.grid_y, 1); }
+
+// Dispatch on (dtype, vec, offset width) to a template instance.
+template <template <typename, int, typename> class F, typename I, typename... A>
+cudaError_t dispatch_t(int dtype, int vec, A&&... args) {
+  if (dtype == GBN_F32) {
+    switch (vec) {
+      case 4: return F<float, 4, I>::run(args...);
+      case 2: return F<float, 2, I>::run(args...);
+      default: return F<float, 1, I>::run(args...);
+    }
+  }
+  switch (vec) {
+    case 8: return F<bf16, 8, I>::run(args...);
+    case 4: return F<bf16, 4, I>::run(args...);
+    case 2: return F<bf16, 2, I>::run(args...);
+    default: return F<bf16, 1, I>::run(args...);
+  }
+}
+
+template <template <typename, int, typename> class F, typename... A>
+cudaError_t dispatch(const BnPlan& p, int dtype, A&&... args) {
+  const uint64_t vectors = (uint64_t)p.B * (uint64_t)p.C * (uint64_t)(p.P / p.vec);
+  if (vectors < (1ull << 32)) return dispatch_t<F, uint32_t>(dtype, p.vec, args...);
+  return dispatch_t<F, uint64_t>(dtype, p.vec, args...);
+}
+
+template <typename T, int VEC, typename I> struct StatsL {
+  static cudaError_t run(const void* x, const BnPlan& p, double* part, cudaStream_t st) {
+    return launch(bn_stats_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, false,
+                  static_cast<const T*>(x), make_geom(p), part);
+  }
+};
+template <typename T, int VEC, typename I> struct ApplyL {
+  static cudaError_t run(const void* x, void* y, const BnPlan& p, const ApplyArgs& a,
+                         cudaStream_t st, bool pdl) {
+    return launch(bn_apply_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, pdl,
+                  static_cast<const T*>(x), static_cast<T*>(y), make_geom(p), a);
+  }
+};
+template <typename T, int VEC, typename I> struct GradSumsL {
+  static cudaError_t run(const void* x, const void* dy, const BnPlan& p, const float* stats,
+                         double* part, cudaStream_t st) {
+    return launch(bn_grad_sums_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, false,
+                  static_cast<const T*>(x), static_cast<const T*>(dy), make_geom(p), stats, part);
+  }
+};
+template <typename T, int VEC, typename I> struct DxL {
+  static cudaError_t run(const void* x, const void* dy, void* dx, const BnPlan& p,
+                         const float* stats, const double* part, float* grads, cudaStream_t st,
+                         bool pdl) {
+    return launch(bn_dx_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, pdl,
+                  static_cast<const T*>(x), static_cast<const T*>(dy), static_cast<T*>(dx),
+                  make_geom(p), stats, part, grads);
+  }
+};
+
+}  // namespace
+
+bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan) {
+  if (B < 0 || C < 0 || HW < 0) return false;
+  plan->B = B;
+  plan->C = C;
+  plan->P = HW;
+  plan->M = B * HW;
+  // Fill every resident 256-thread block slot once ("Reduction grid"), but
+  // give each block at least kBnMinElemsPerBlock elements.
+  const int64_t slots = (int64_t)dev.sms * (dev.max_threads_sm / kBnThreads);
+  int64_t gy = C > 0 ? slots / C : 1;
+  const int64_t by_work = (plan->M + kBnMinElemsPerBlock - 1) / kBnMinElemsPerBlock;
+  if (by_work < gy) gy = by_work;
+  if (gy < 1) gy = 1;
+  if (gy > 65535) gy = 65535;
+  plan->grid_y = (int)gy;
+  const size_t bytes = (size_t)2 * (size_t)gy * (size_t)(C > 0 ? C : 1) * sizeof(double);
+  plan->ws_bytes = (bytes + 255) & ~(size_t)255;
+  return true;
+}
+
+int bn_vec_width(int dtype, int64_t P, const void* const* ptrs, int nptrs) {
+  const int esize = dtype == GBN_F32 ? 4 : 2;
+  int vec = 16 / esize;
+  while (vec > 1) {
+    bool ok = (P % vec) == 0;
+    for (int i = 0; i < nptrs && ok; ++i)
+      if (ptrs[i] != nullptr && (reinterpret_cast<uintptr_t>(ptrs[i]) % (uintptr_t)(vec * esize)) != 0)
+        ok = false;
+    if (ok) break;
+    vec >>= 1;
+  }
+  return vec;
+}
+
+cudaError_t bn_launch_stats(const void* x, int dtype, const BnPlan& p, double* part,
+                            cudaStream_t st) {
+  return dispatch<StatsL>(p, dtype, x, p, part, st);
+}
+
+cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, int mode,
+                            const double* part, const float* gamma, const float* beta,
+                            float* stats, float* running_mean, float* running_var,
+                            float momentum, float eps, const float* mean, const float* scale,
+                            cudaStream_t st, bool pdl) {
+  ApplyArgs a;
+  a.mode = mode;
+  a.part = part;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.stats = stats;
+  a.running_mean = running_mean;
+  a.running_var = running_var;
+  a.momentum = momentum;
+  a.eps = eps;
+  a.mean = mean;
+  a.scale = scale;
+  return dispatch<ApplyL>(p, dtype, x, y, p, a, st, pdl);
+}
+
+cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const BnPlan& p,
+                                const float* stats, double* part, cudaStream_t st) {
+  return dispatch<GradSumsL>(p, dtype, x, dy, p, stats, part, st);
+}
+
+cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
+                         const float* stats, const double* part, float* grads, cudaStream_t st,
+                         bool pdl) {
+  return dispatch<DxL>(p, dtype, x, dy, dx, p, stats, part, grads, st, pdl);
+}
+
+}  // namespace gbn

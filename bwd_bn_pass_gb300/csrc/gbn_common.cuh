@@ -1,0 +1,287 @@
+// Device-side building blocks shared by the normalization kernels.
+//
+// - storage <-> fp32 conversion and 2..16-byte vector loads/stores;
+// - double-fp32 ("DF") accumulation: Knuth's TwoSum keeps the exact rounding
+//   error of every addition, and an FMA recovers the exact error of a
+//   product, so fp32 outputs that are sums of 10^5..10^6 terms stay within a
+//   few fp32 ulps of the exact sum even when the sum nearly cancels;
+// - warp / block reductions with a fixed shuffle tree (deterministic);
+// - programmatic dependent launch (griddepcontrol), mbarrier and 1-D bulk
+//   copy (cp.async.bulk, the non-tensor TMA form) wrappers, with waits that
+//   give up after about a second instead of spinning forever.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbn {
+
+using bf16 = __nv_bfloat16;
+
+// ------------------------------------------------------------ conversion --
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round-to-nearest-even
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// VEC elements of T moved as one raw word group (VEC*sizeof(T) bytes, a
+// power of two <= 16) and converted to fp32 only when used, so a thread can
+// keep several vectors in flight in few registers.  bf16 element 0 sits in
+// the low half of a 32-bit word.
+template <typename T, int VEC> struct Vec;
+
+template <> struct Vec<float, 1> {
+  using raw = uint32_t;
+  __device__ static raw ld(const float* p) { return __float_as_uint(*p); }
+  __device__ static void cvt(raw r, float (&v)[1]) { v[0] = __uint_as_float(r); }
+  __device__ static void store(float* p, const float (&v)[1]) { *p = v[0]; }
+};
+template <> struct Vec<float, 2> {
+  using raw = uint2;
+  __device__ static raw ld(const float* p) { return *reinterpret_cast<const uint2*>(p); }
+  __device__ static void cvt(raw r, float (&v)[2]) {
+    v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+  }
+  __device__ static void store(float* p, const float (&v)[2]) {
+    *reinterpret_cast<float2*>(p) = make_float2(v[0], v[1]);
+  }
+};
+template <> struct Vec<float, 4> {
+  using raw = uint4;
+  __device__ static raw ld(const float* p) { return *reinterpret_cast<const uint4*>(p); }
+  __device__ static void cvt(raw r, float (&v)[4]) {
+    v[0] = __uint_as_float(r.x); v[1] = __uint_as_float(r.y);
+    v[2] = __uint_as_float(r.z); v[3] = __uint_as_float(r.w);
+  }
+  __device__ static void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <> struct Vec<bf16, 1> {
+  using raw = uint32_t;
+  __device__ static raw ld(const bf16* p) { return *reinterpret_cast<const uint16_t*>(p); }
+  __device__ static void cvt(raw r, float (&v)[1]) { v[0] = bf16_lo(r); }
+  __device__ static void store(bf16* p, const float (&v)[1]) { *p = __float2bfloat16_rn(v[0]); }
+};
+template <> struct Vec<bf16, 2> {
+  using raw = uint32_t;
+  __device__ static raw ld(const bf16* p) { return *reinterpret_cast<const uint32_t*>(p); }
+  __device__ static void cvt(raw r, float (&v)[2]) { v[0] = bf16_lo(r); v[1] = bf16_hi(r); }
+  __device__ static void store(bf16* p, const float (&v)[2]) {
+    *reinterpret_cast<uint32_t*>(p) = pack_bf16x2(v[0], v[1]);
+  }
+};
+template <> struct Vec<bf16, 4> {
+  using raw = uint2;
+  __device__ static raw ld(const bf16* p) { return *reinterpret_cast<const uint2*>(p); }
+  __device__ static void cvt(raw r, float (&v)[4]) {
+    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+  }
+  __device__ static void store(bf16* p, const float (&v)[4]) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+  }
+};
+template <> struct Vec<bf16, 8> {
+  using raw = uint4;
+  __device__ static raw ld(const bf16* p) { return *reinterpret_cast<const uint4*>(p); }
+  __device__ static void cvt(raw r, float (&v)[8]) {
+    v[0] = bf16_lo(r.x); v[1] = bf16_hi(r.x); v[2] = bf16_lo(r.y); v[3] = bf16_hi(r.y);
+    v[4] = bf16_lo(r.z); v[5] = bf16_hi(r.z); v[6] = bf16_lo(r.w); v[7] = bf16_hi(r.w);
+  }
+  __device__ static void store(bf16* p, const float (&v)[8]) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                              pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+  }
+};
+
+// 16-byte shared-memory vector of T (VE = 16 / sizeof(T) elements).
+template <typename T> struct Vec16 {
+  static constexpr int VE = 16 / sizeof(T);
+  __device__ static void load(const void* p, float (&v)[VE]) {
+    Vec<T, VE>::cvt(Vec<T, VE>::ld(reinterpret_cast<const T*>(p)), v);
+  }
+  __device__ static void store(void* p, const float (&v)[VE]) {
+    Vec<T, VE>::store(reinterpret_cast<T*>(p), v);
+  }
+};
+
+// ------------------------------------------------- double-fp32 arithmetic --
+
+struct DF {
+  float hi, lo;
+};
+
+// a += v with the rounding error of the addition kept in a.lo (TwoSum).
+__device__ __forceinline__ void df_add(DF& a, float v) {
+  const float s = a.hi + v;
+  const float bb = s - a.hi;
+  const float err = (a.hi - (s - bb)) + (v - bb);
+  a.hi = s;
+  a.lo += err;
+}
+
+// a += p*q with the product's rounding error kept (FMA residual).
+__device__ __forceinline__ void df_add_prod(DF& a, float p, float q) {
+  const float m = p * q;
+  const float e = fmaf(p, q, -m);
+  df_add(a, m);
+  a.lo += e;
+}
+
+__device__ __forceinline__ double df_value(const DF& a) { return (double)a.hi + (double)a.lo; }
+
+// Error-free building blocks: exact a + b and a * b as (hi, lo) pairs.
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return DF{s, (a - (s - bb)) + (b - bb)};
+}
+__device__ __forceinline__ DF two_prod(float a, float b) {
+  const float p = a * b;
+  return DF{p, fmaf(a, b, -p)};
+}
+// (hi, lo) * b, keeping the exact error of hi*b (lo*b is rounded; it is
+// already ~2^-24 of the result).
+__device__ __forceinline__ DF df_mul(DF a, float b) {
+  DF p = two_prod(a.hi, b);
+  p.lo = fmaf(a.lo, b, p.lo);
+  return p;
+}
+// (hi, lo) + b
+__device__ __forceinline__ DF df_plus(DF a, float b) {
+  DF s = two_sum(a.hi, b);
+  s.lo += a.lo;
+  return s;
+}
+// acc += t for a (hi, lo) term
+__device__ __forceinline__ void df_acc(DF& acc, DF t) {
+  df_add(acc, t.hi);
+  acc.lo += t.lo;
+}
+__device__ __forceinline__ float df_round(DF a) { return a.hi + a.lo; }
+
+// --------------------------------------------------------------- reduce --
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum two doubles over the block; every thread gets the result.  `red` must
+// hold 2*32 doubles.  Contains __syncthreads (all threads must call it).
+__device__ __forceinline__ void block_sum2(double& a, double& b, double* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  a = warp_sum(a);
+  b = warp_sum(b);
+  if (lane == 0) { red[warp] = a; red[32 + warp] = b; }
+  __syncthreads();
+  double x = lane < nwarps ? red[lane] : 0.0;
+  double y = lane < nwarps ? red[32 + lane] : 0.0;
+  a = warp_sum(x);
+  b = warp_sum(y);
+}
+
+// ------------------------------------------- programmatic dependent launch --
+
+// Let the next kernel on the stream (launched with the programmatic stream
+// serialization attribute) be scheduled; it must still wait before reading
+// anything this grid writes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid has completed and its writes are visible.
+// A no-op when the kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// --------------------------------------------------- mbarrier / bulk copy --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_mbarrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same buffer.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// Wait for phase `parity` of `bar` to complete; false if it has not after
+// about `limit_ns` nanoseconds (the caller records an error and stops).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void report_status(int* status, int bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+}  // namespace gbn

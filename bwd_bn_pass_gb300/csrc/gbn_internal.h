@@ -1,0 +1,142 @@
+// Host-side declarations shared by the C ABI (abi.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "gbnorm.h"
+
+namespace gbn {
+
+// Cached per-device facts.  Filled once per device by device_info().
+struct DevInfo {
+  int sms = 0;               // multiprocessor count (152 on GB300)
+  int max_threads_sm = 0;    // resident threads per SM (2048)
+  int smem_optin = 0;        // max dynamic shared memory per block (bytes)
+  int* status = nullptr;     // device address of the library status word
+  bool ok = false;
+};
+
+// Returns nullptr (and leaves a CUDA error pending) if the device cannot be
+// queried.  device < 0 means the current device.
+const DevInfo* device_info(int device);
+
+// Launch `kern` with the given configuration; `pdl` adds the programmatic
+// stream serialization attribute so the kernel may start while the
+// preceding kernel on the stream drains (it then calls griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                   cudaStream_t stream, bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ------------------------------------------------------------- BatchNorm --
+
+constexpr int kBnThreads = 256;
+constexpr int64_t kBnMinElemsPerBlock = 4096;
+
+// Shape facts derived once per call on the host.
+struct BnPlan {
+  int64_t B = 0, C = 0, P = 0;  // batch, channels, plane size (HW)
+  int64_t M = 0;                // per-channel count B*P
+  int grid_y = 0;               // blocks per channel
+  int vec = 1;                  // elements per vector access
+  size_t ws_bytes = 0;          // partials bytes (2 * grid_y * C doubles, rounded)
+};
+
+// Fills grid_y / ws_bytes (device-dependent) for a shape; false on error.
+bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan);
+
+// Largest power-of-two vector width (<= 16 bytes) valid for all pointers.
+int bn_vec_width(int dtype, int64_t P, const void* const* ptrs, int nptrs);
+
+enum BnApplyMode { kApplyTrain = 0, kApplyStats = 1, kApplyInfer = 2 };
+
+cudaError_t bn_launch_stats(const void* x, int dtype, const BnPlan& p, double* part,
+                            cudaStream_t st);
+cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, int mode,
+                            const double* part, const float* gamma, const float* beta,
+                            float* stats, float* running_mean, float* running_var,
+                            float momentum, float eps, const float* mean, const float* scale,
+                            cudaStream_t st, bool pdl);
+cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const BnPlan& p,
+                                const float* stats, double* part, cudaStream_t st);
+cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
+                         const float* stats, const double* part, float* grads, cudaStream_t st,
+                         bool pdl);
+
+// ------------------------------------------------------------ row-wise --
+
+// Column partials: [nout][nplanes][G][H] fp32; nplanes = 2 (hi, lo) when the
+// outputs are fp32 (double-fp32 accumulation), 1 otherwise.
+struct RowPlan {
+  int64_t R = 0, H = 0;
+  int kind = GBN_ROW_RMS;
+  int dtype = GBN_F32;
+  bool fast = false;   // bulk-copy persistent kernel (else the generic kernel)
+  int threads = 0;     // block size
+  int kv = 0;          // 16-byte vectors per thread per row (fast path)
+  int rb = 1;          // rows per pipeline stage (fast path)
+  int nstage = 0;      // pipeline depth (fast path)
+  int G = 0;           // blocks (= rows of column partials)
+  int nout = 1;        // column outputs
+  int nplanes = 1;     // 2 when fp32 outputs use hi/lo partials
+  size_t smem = 0;     // dynamic shared memory per block
+  uint32_t stage_bytes = 0;
+  uint32_t off[5] = {0, 0, 0, 0, 0};  // per-stage offsets: dy, x, residual, mask, dz_extra
+  size_t ws_bytes = 0;
+};
+
+struct LnPtrs {
+  const void* dy = nullptr;
+  const void* x = nullptr;
+  const void* residual = nullptr;
+  const void* bias = nullptr;
+  const uint8_t* mask = nullptr;
+  const float* dz_extra = nullptr;
+  const float* mean = nullptr;
+  const float* rstd = nullptr;
+  const void* gamma = nullptr;
+  float scale = 1.f;
+  void* dx = nullptr;
+  void* dres = nullptr;
+  void* dgamma = nullptr;
+  void* dbeta = nullptr;
+  void* dbias = nullptr;
+};
+
+// Plans the launch.  `fast_ok` says whether pointers/shape allow the
+// bulk-copy path; the workspace query plans with fast_ok=false and true and
+// takes the larger size.
+bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_mask,
+              bool has_dzx, const DevInfo& dev, RowPlan* plan);
+
+cudaError_t rms_launch(const RowPlan& p, const void* dy, const void* x, const void* w,
+                       const float* rstd, void* dx, void* dw, float* part, int* status,
+                       cudaStream_t st);
+cudaError_t ln_launch(const RowPlan& p, const LnPtrs& a, float* part, int* status,
+                      cudaStream_t st);
+
+// Column-partials reduction: out[o][h] = sum_g part[o][*][g][h] in a fixed
+// order; outs[o] may be nullptr (skipped).  Launched with PDL after the row
+// kernel when `pdl` is set.
+cudaError_t colsum_launch(const float* part, int nout, int nplanes, int G, int64_t H, int dtype,
+                          void* const* outs, cudaStream_t st, bool pdl);
+
+// Set the kernels' dynamic shared memory limits (called from device_info).
+cudaError_t row_kernels_configure(int smem_optin);
+
+}  // namespace gbn

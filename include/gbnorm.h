@@ -1,0 +1,245 @@
+/*
+ * gbnorm.h -- C ABI of libgbnorm.so: training-mode normalization forward and
+ * backward on one GB300 (sm_103a) GPU.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers are DEVICE pointers of the current CUDA device (for example
+ *   torch's tensor.data_ptr()), except where a comment says otherwise.  The
+ *   caller owns all memory; the library allocates nothing and keeps no
+ *   per-call state.  It caches only device attributes and the address of its
+ *   device status word (see gbn_get_device_status).
+ * - `stream` is a cudaStream_t passed as void*.  Every call is asynchronous
+ *   on that stream; no call synchronises the host.
+ * - Tensors are dense and contiguous in the layout stated per call.  Sizes
+ *   are int64_t element counts.
+ * - `dtype` selects the storage type of the large tensors: GBN_F32 or
+ *   GBN_BF16.  All accumulation is fp32 on the GPU, with error-free (double
+ *   fp32) summation where a fp32 output needs it; per-channel and per-row
+ *   reductions across blocks are combined in fp64 or double-fp32 in a fixed
+ *   order, so two runs on the same device give bit-identical results.  No
+ *   float atomics are used anywhere.
+ * - Return value: GBN_OK (0) or a negative GBN_E* code.  On an argument
+ *   error nothing is launched and no output is touched.  GBN_ECUDA reports
+ *   a launch error (cudaGetLastError after the launches).  Errors that can
+ *   only be seen on the device (a bounded wait that ran out) are recorded in
+ *   the device status word, read with gbn_get_device_status.
+ * - Alignment: any element-aligned pointer is accepted for the large
+ *   tensors; 16-byte aligned pointers (and rows/planes whose byte length is
+ *   a multiple of 16) take the vectorised / bulk-copy fast paths.  `stats`
+ *   must be 8-byte aligned and workspaces 16-byte aligned (else GBN_EALIGN).
+ *
+ * Source pages (titles; the numbers in brackets are the sections used):
+ *   [P4] Aether-ML PR #18 "perf(batchnorm): device-sized grid, one-pass
+ *        statistics, finalize kernels" -- sections "Reduction grid",
+ *        "One-pass statistics", "Backward finalize", "Behavior changes".
+ *   [P2] nvFuser issue #1473 "Why is LayerNorm Backward Segmenting?" --
+ *        the bias+dropout+add+layer_norm backward repro (fusion_id9) and the
+ *        layer_norm backward repro (fusion_id14), "Perf on A100".
+ *   [P3] nvFuser issue #3629 "Performance gap between manual nvfuser
+ *        definition and thunder.jit for rmsnorm" -- "nvfuser pre-generated
+ *        definition" (rmsnorm_bwd_fusion) and the Thunder definition.
+ *   [P1] Lightning-Thunder PR #182 "Improve batch_norm backward performance
+ *        for automatically generated backward" (BN backward as one pass).
+ */
+#ifndef GBNORM_H
+#define GBNORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GBN_API __attribute__((visibility("default")))
+#else
+#define GBN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define GBN_OK 0
+#define GBN_EINVAL -1     /* null pointer, negative/overflowing size, M < 2 in training, bad combination */
+#define GBN_EDTYPE -2     /* dtype is not GBN_F32 / GBN_BF16 */
+#define GBN_EALIGN -3     /* stats not 8-byte aligned or workspace not 16-byte aligned */
+#define GBN_EWORKSPACE -4 /* ws_bytes smaller than the matching *_workspace_bytes() */
+#define GBN_ECUDA -5      /* CUDA runtime error while querying the device or launching */
+#define GBN_EDEVICE -6    /* a kernel reported an error in the device status word */
+
+/* ---- storage types ----------------------------------------------------- */
+#define GBN_F32 0
+#define GBN_BF16 1
+
+/* ---- device status bits (gbn_get_device_status) ------------------------ */
+#define GBN_DEV_WAIT_TIMEOUT 1 /* a bulk-copy wait in a row kernel ran out (about 1 s) */
+
+/* ---- BatchNorm buffer sizes -------------------------------------------- */
+/* stats: 8*C floats (32*C bytes, 8-byte aligned).  Rows 0..3 are public,
+ * fp32 [4, C] = (mean, var, inv_std, scale = gamma*inv_std) as in [P4]
+ * "One-pass statistics".  Rows 4..7 are private to this library: row 4 the
+ * channel's shift x[0,c,0,0] (fp32), row 5 mean - shift (fp32), rows 6..7 the
+ * same mean - shift as fp64 [C] (used by the backward).                     */
+#define GBN_BN_STATS_FLOATS(C) (8 * (int64_t)(C))
+/* grads: fp32 [4, C] = (dgamma, dbeta, k1, k2), [P4] "Backward finalize".  */
+#define GBN_BN_GRADS_FLOATS(C) (4 * (int64_t)(C))
+
+/* ---- row-wise workspace kinds ------------------------------------------ */
+#define GBN_ROW_RMS 0      /* rmsnorm_backward: dweight partials           */
+#define GBN_ROW_LN 1       /* layernorm_backward, plain: dgamma, dbeta     */
+#define GBN_ROW_LN_FUSED 2 /* layernorm_backward, fused: + dbias           */
+
+/* Version of this ABI (increments on any signature change). */
+GBN_API int gbn_abi_version(void);
+
+/* Static, human-readable text for a status code. */
+GBN_API const char* gbn_status_string(int status);
+
+/* Prepare `device` (-1: current): cache its attributes, resolve the device
+ * status word and raise the kernels' shared-memory limits.  Every entry
+ * point does this on its first call on a device; call it explicitly before
+ * capturing a CUDA graph.  Returns GBN_OK or GBN_ECUDA.                     */
+GBN_API int gbn_init(int device);
+
+/* Read the device status word of `device` (-1: current) into *status, a
+ * HOST pointer (bit set of GBN_DEV_*; 0 = no device-side error), and clear it
+ * when `clear` is nonzero.  Synchronises with the device (it is a copy).     */
+GBN_API int gbn_get_device_status(int device, int* status, int clear);
+
+/* =========================================================================
+ * BatchNorm2d, training mode, NCHW  ([P4]; [P1] for the one-pass backward)
+ *
+ * x, y, dy, dx: [B, C, HW] contiguous (HW = H*W), storage `dtype`.
+ * gamma, beta, running_mean, running_var: fp32 [C].  gamma/beta may be NULL
+ * (treated as 1 and 0); running_mean/running_var may be NULL (not updated).
+ * Per channel, M = B*HW elements are reduced.
+ *
+ * The forward is two launches: a device-sized grid of one-pass shifted-sum
+ * blocks writes per-block fp64 partials (sum d, sum d^2 with d = x - x[0,c])
+ * into `ws` without atomics; a second kernel, launched with programmatic
+ * dependent launch, reduces the partials of its channel in a fixed order
+ * (the "finalize"), writes stats and the running-stat update from the
+ * channel's first block, and applies y = (x - mean)*scale + beta in the
+ * centred form.  The backward mirrors it: grad_sums partials (sum dy,
+ * sum dy*(x - shift)), then finalize + dx = dy*scale + (x-mean)*k1 + k2.
+ * ======================================================================= */
+
+/* Workspace bytes for the BN partials of this shape on `device` (-1:
+ * current): 16 * grid_y * C rounded up to 256, where grid_y is the number of
+ * blocks per channel ([P4] "Reduction grid": fill every resident 256-thread
+ * block slot once).  Returns 0 on a bad shape or a CUDA error.              */
+GBN_API size_t gbn_bn_workspace_bytes(int64_t B, int64_t C, int64_t HW, int device);
+
+/* Full training forward: stats pass + finalize/apply.  Writes y, stats
+ * (8*C floats, see GBN_BN_STATS_FLOATS), and updates the running stats in
+ * place: running_mean = (1-momentum)*running_mean + momentum*mean,
+ * running_var = (1-momentum)*running_var + momentum*var*M/(M-1); var in
+ * stats is biased (divides by M).  Requires M >= 2 (GBN_EINVAL otherwise).
+ * y may alias x.  ws: >= gbn_bn_workspace_bytes(B, C, HW, -1) bytes.       */
+GBN_API int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C,
+                         int64_t HW, const float* gamma, const float* beta,
+                         float* running_mean, float* running_var,
+                         float momentum, float eps, void* y, float* stats,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Phase 1 of the forward alone: writes the stats partials into ws.        */
+GBN_API int gbn_bn_stats(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Phases 2+3 of the forward: finalize the partials left in ws by
+ * gbn_bn_stats (same x, same shape, same device), write stats and the
+ * running update, and apply.  Arguments as gbn_bn_forward_train.           */
+GBN_API int gbn_bn_finalize_apply(const void* x, int dtype, int64_t B, int64_t C,
+                          int64_t HW, const float* gamma, const float* beta,
+                          float* running_mean, float* running_var,
+                          float momentum, float eps, void* y, float* stats,
+                          const void* ws, size_t ws_bytes, void* stream);
+
+/* Centred apply y = (x - mean)*scale + beta, shared by training and
+ * inference ([P4] "One-pass statistics", _bn_apply_ew).  If `stats` is
+ * non-NULL it is a buffer written by a training forward and mean/scale are
+ * ignored; otherwise `mean` and `scale` (fp32 [C], e.g. running_mean and
+ * gamma/sqrt(running_var + eps)) are used.  beta may be NULL (0).           */
+GBN_API int gbn_bn_apply(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                 const float* stats, const float* mean, const float* scale,
+                 const float* beta, void* y, void* stream);
+
+/* Full training backward: grad_sums pass + finalize/dx.  `stats` is the
+ * buffer written by the matching training forward of the same x.  Writes
+ * dx and grads (fp32 [4, C] = dgamma, dbeta, k1, k2; [P4] "Backward
+ * finalize") with k1 = -scale*inv_std^2*sum(dy*(x-mean))/M and
+ * k2 = -scale*dbeta/M.  dx may alias dy.  ws as for the forward.            */
+GBN_API int gbn_bn_backward(const void* x, const void* dy, int dtype, int64_t B,
+                    int64_t C, int64_t HW, const float* stats, void* dx,
+                    float* grads, void* ws, size_t ws_bytes, void* stream);
+
+/* Phase 1 of the backward alone: grad_sums partials into ws.              */
+GBN_API int gbn_bn_grad_sums(const void* x, const void* dy, int dtype, int64_t B,
+                     int64_t C, int64_t HW, const float* stats, void* ws,
+                     size_t ws_bytes, void* stream);
+
+/* Phases 2+3 of the backward: finalize the grad_sums partials in ws and
+ * write grads and dx.                                                       */
+GBN_API int gbn_bn_finalize_dx(const void* x, const void* dy, int dtype, int64_t B,
+                       int64_t C, int64_t HW, const float* stats, void* dx,
+                       float* grads, const void* ws, size_t ws_bytes,
+                       void* stream);
+
+/* =========================================================================
+ * Row-wise backward passes: RMSNorm ([P3]) and LayerNorm ([P2]).
+ *
+ * Tensors are [R, H] row-major in `dtype` unless stated.  One persistent
+ * launch streams rows through shared memory with bulk copies, reduces each
+ * row with warp shuffles while the row is on chip (x and dy are read once),
+ * and accumulates the per-column sums of its rows in registers; a second
+ * small launch (programmatic dependent launch) adds the per-block column
+ * partials in a fixed order.  The column reductions therefore never re-read
+ * the [R, H] inputs.
+ * ======================================================================= */
+
+/* Workspace bytes for a row-wise backward of kind GBN_ROW_* and `dtype` on
+ * `device` (-1: current).  Returns 0 on a bad shape or a CUDA error.        */
+GBN_API size_t gbn_rowwise_workspace_bytes(int64_t R, int64_t H, int kind, int dtype,
+                                   int device);
+
+/* RMSNorm backward ([P3] rmsnorm_bwd_fusion, with the saved statistic taken
+ * as rstd = 1/rms, fp32 [R]):
+ *   S_r   = sum_j w_j*dy_rj*x_rj
+ *   dx_rj = rstd_r*w_j*dy_rj - x_rj*rstd_r^3*S_r/H
+ *   dw_j  = sum_r dy_rj*x_rj*rstd_r        (written in `dtype`)
+ * dy, x, dx: [R, H]; w, dw: [H].                                            */
+GBN_API int gbn_rmsnorm_backward(const void* dy, const void* x, const void* w,
+                         int dtype, const float* rstd, int64_t R, int64_t H,
+                         void* dx, void* dw, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* LayerNorm backward, plain or fused with bias+dropout+add ([P2]).
+ * mean, rstd: fp32 [R] saved by the forward; gamma: [H].
+ *
+ * Plain (residual == NULL; bias, mask, dresidual, dbias must be NULL):
+ *   z = x_or_input (the LayerNorm input), dx = dz (+ dz_extra).
+ * Fused (residual != NULL): the LayerNorm input is recomputed in fp32 as
+ *   z = residual + mask*dropout_scale*(x_or_input + bias)
+ *   dresidual = dz (+ dz_extra), dx = dresidual*dropout_scale*mask,
+ *   dbias = sum_rows dx.
+ * with xhat = (z-mean)*rstd, g = dy*gamma and
+ *   dz = rstd*(g - mean_j(g) - xhat*mean_j(g*xhat)).
+ * Column sums: dgamma = sum_rows dy*xhat, dbeta = sum_rows dy.
+ * mask: uint8 [R, H] (nonzero = kept) or NULL (all kept).  bias: [H] or NULL.
+ * dz_extra: fp32 [R, H] or NULL (an extra gradient arriving at z).
+ * dresidual, dgamma, dbeta, dbias may be NULL (not written).  Outputs are in
+ * `dtype`.                                                                 */
+GBN_API int gbn_layernorm_backward(const void* dy, const void* x_or_input, int dtype,
+                           const float* mean, const float* rstd,
+                           const void* gamma, int64_t R, int64_t H,
+                           const void* residual, const void* bias,
+                           const uint8_t* mask, float dropout_scale,
+                           const float* dz_extra, void* dx, void* dresidual,
+                           void* dgamma, void* dbeta, void* dbias, void* ws,
+                           size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNORM_H */

@@ -1,0 +1,139 @@
+"""The C ABI library on the host: it builds, loads, exports every symbol the
+header declares, and rejects bad arguments before touching CUDA.  No GPU is
+needed: argument validation runs before any CUDA call, and fake (never
+dereferenced) device addresses are enough to exercise it."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from bwd_bn_pass_gb300 import gbnorm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, EINVAL, EDTYPE, EALIGN, EWORKSPACE, ECUDA = 0, -1, -2, -3, -4, -5
+P = ctypes.c_void_p
+A16 = P(0x10000)   # 16-byte aligned fake address
+A4 = P(0x10004)    # 4-byte aligned only
+NULL = None
+
+
+def declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^GBN_API\s+[\w\s\*]+?\b(gbn_\w+)\s*\(", text, re.M)
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ("gbn_bn_forward_train", "gbn_bn_apply", "gbn_bn_backward",
+              "gbn_rmsnorm_backward", "gbn_layernorm_backward"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(gbn):
+    L = gbn.lib()
+    for name in declared_symbols():
+        assert hasattr(L, name), f"{name} not exported"
+        assert name in gbn.exported_symbols(), f"{name} missing from the binding"
+
+
+def test_abi_version_and_status_strings(gbn):
+    L = gbn.lib()
+    assert L.gbn_abi_version() == 1
+    for code in (OK, EINVAL, EDTYPE, EALIGN, EWORKSPACE, ECUDA, -6, 12345):
+        assert isinstance(L.gbn_status_string(code), bytes)
+    assert L.gbn_status_string(EWORKSPACE) == b"workspace too small"
+
+
+def _fwd(L, x=A16, dtype=0, B=4, C=3, HW=5, gamma=NULL, beta=NULL, rm=NULL, rv=NULL,
+         mom=0.1, eps=1e-5, y=A16, stats=A16, ws=A16, nbytes=1 << 20):
+    return L.gbn_bn_forward_train(x, dtype, B, C, HW, gamma, beta, rm, rv, mom, eps, y, stats,
+                                  ws, nbytes, NULL)
+
+
+def test_bn_forward_argument_errors(gbn):
+    L = gbn.lib()
+    assert _fwd(L, dtype=7) == EDTYPE
+    assert _fwd(L, B=-1) == EINVAL
+    assert _fwd(L, HW=-3) == EINVAL
+    assert _fwd(L, B=1, HW=1) == EINVAL          # M = 1: no unbiased running var
+    assert _fwd(L, B=0) == EINVAL                # M = 0 in training
+    assert _fwd(L, x=NULL) == EINVAL
+    assert _fwd(L, y=NULL) == EINVAL
+    assert _fwd(L, stats=NULL) == EINVAL
+    assert _fwd(L, ws=NULL) == EINVAL
+    assert _fwd(L, stats=A4) == EALIGN
+    assert _fwd(L, ws=A4) == EALIGN
+    assert _fwd(L, eps=float("nan")) == EINVAL
+    assert _fwd(L, eps=-1.0) == EINVAL
+    assert _fwd(L, mom=float("nan")) == EINVAL
+    assert _fwd(L, B=1 << 40, C=1 << 40) == EINVAL   # element count overflow
+    assert _fwd(L, B=1 << 20, HW=1 << 12) == EINVAL  # per-channel count >= 2^31
+    assert _fwd(L, C=0) == OK                    # nothing to do, nothing launched
+
+
+def test_bn_other_entry_points_argument_errors(gbn):
+    L = gbn.lib()
+    assert L.gbn_bn_stats(A16, 3, 2, 2, 2, A16, 4096, NULL) == EDTYPE
+    assert L.gbn_bn_stats(NULL, 0, 2, 2, 2, A16, 4096, NULL) == EINVAL
+    assert L.gbn_bn_apply(A16, 0, 2, 2, 2, NULL, NULL, NULL, NULL, A16, NULL) == EINVAL
+    assert L.gbn_bn_apply(A16, 0, 2, 2, 2, A4, NULL, NULL, NULL, A16, NULL) == EALIGN
+    assert L.gbn_bn_apply(A16, 0, 0, 2, 2, NULL, NULL, NULL, NULL, A16, NULL) == OK
+    assert L.gbn_bn_backward(A16, NULL, 0, 2, 2, 2, A16, A16, A16, A16, 4096, NULL) == EINVAL
+    assert L.gbn_bn_backward(A16, A16, 0, 2, 2, 2, A16, NULL, A16, A16, 4096, NULL) == EINVAL
+    assert L.gbn_bn_backward(A16, A16, 0, 2, 2, 2, A4, A16, A16, A16, 4096, NULL) == EALIGN
+    assert L.gbn_bn_backward(A16, A16, 1, 1, 2, 1, A16, A16, A16, A16, 4096, NULL) == EINVAL
+    assert L.gbn_bn_grad_sums(A16, A16, 0, 2, 2, 2, NULL, A16, 4096, NULL) == EINVAL
+    assert L.gbn_bn_finalize_dx(A16, A16, 0, 2, 2, 2, A16, A16, NULL, A16, 4096, NULL) == EINVAL
+    assert L.gbn_bn_workspace_bytes(-1, 2, 2, -1) == 0
+
+
+def _rms(L, dtype=1, R=4, H=64, dy=A16, x=A16, w=A16, rstd=A16, dx=A16, dw=A16, ws=A16):
+    return L.gbn_rmsnorm_backward(dy, x, w, dtype, rstd, R, H, dx, dw, ws, 1 << 20, NULL)
+
+
+def test_rmsnorm_argument_errors(gbn):
+    L = gbn.lib()
+    assert _rms(L, dtype=5) == EDTYPE
+    assert _rms(L, R=-1) == EINVAL
+    assert _rms(L, w=NULL) == EINVAL
+    assert _rms(L, dw=NULL) == EINVAL
+    assert _rms(L, rstd=NULL) == EINVAL
+    assert _rms(L, ws=A4) == EALIGN
+    assert _rms(L, H=0) == OK
+    assert L.gbn_rowwise_workspace_bytes(4, 64, 9, 0, -1) == 0
+
+
+def _ln(L, dtype=1, R=4, H=64, residual=NULL, bias=NULL, mask=NULL, scale=1.0,
+        dres=NULL, dbias=NULL, gamma=A16, ws=A16, mean=A16):
+    return L.gbn_layernorm_backward(A16, A16, dtype, mean, A16, gamma, R, H, residual, bias,
+                                    mask, scale, NULL, A16, dres, A16, A16, dbias, ws, 1 << 20,
+                                    NULL)
+
+
+def test_layernorm_argument_errors(gbn):
+    L = gbn.lib()
+    assert _ln(L, dtype=2) == EDTYPE
+    assert _ln(L, H=-1) == EINVAL
+    assert _ln(L, bias=A16) == EINVAL            # bias without residual
+    assert _ln(L, mask=A16) == EINVAL            # mask without residual
+    assert _ln(L, dres=A16) == EINVAL            # dresidual without residual
+    assert _ln(L, dbias=A16) == EINVAL
+    assert _ln(L, gamma=NULL) == EINVAL
+    assert _ln(L, mean=NULL) == EINVAL
+    assert _ln(L, residual=A16, scale=float("nan")) == EINVAL
+    assert _ln(L, ws=A4) == EALIGN
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host without GPU only")
+def test_valid_call_without_gpu_reports_cuda_error(gbn):
+    L = gbn.lib()
+    assert _fwd(L) == ECUDA
+    assert _rms(L) == ECUDA
+    assert L.gbn_init(-1) == ECUDA

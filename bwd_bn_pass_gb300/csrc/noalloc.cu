@@ -1,0 +1,61 @@
+// BatchNorm2d training forward for callers that cannot allocate device
+// memory.
+//
+// Some callers have no way to provide the workspace that gbn_bn_forward_train
+// needs: code running inside a CUDA-graph capture or a real-time loop where a
+// cudaMalloc would synchronise or is forbidden, plugins whose host framework
+// owns every device allocation, or C callers without an allocator at all.
+// This file gives them one entry point whose scratch (the per-block
+// statistics partials) lives in a fixed, file-scope device array that every
+// GPU loading the library holds until the process exits.
+//
+// The entry point allocates nothing: it resolves the array's device address
+// once per device (the host-side symbol is only a stand-in, never a device
+// address) and then runs the ordinary forward with that address as the
+// workspace.
+#include <mutex>
+
+#include "gbn_internal.h"
+
+namespace {
+
+// 64 KiB: the stats partials take 16 * grid_y * C bytes, and grid_y * C is at
+// most one resident block slot per SM (1216 on GB300) whenever C <= 1216, so
+// every shape with C <= 4096 channels fits on GB300.
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device; nullptr if the
+// CUDA runtime refuses.  Done once per device, with that device current.
+void* scratch_on_current_device() {
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[device] = p;
+  }
+  return g_noalloc_ptr[device];
+}
+
+}  // namespace
+
+extern "C" int gbn_bn_forward_train_noalloc(const void* x, int dtype, int64_t B, int64_t C,
+                                            int64_t HW, const float* gamma, const float* beta,
+                                            float* running_mean, float* running_var,
+                                            float momentum, float eps, void* y, float* stats,
+                                            void* stream) {
+  void* scratch = scratch_on_current_device();
+  if (scratch == nullptr) return GBN_ECUDA;
+  const size_t need = gbn_bn_workspace_bytes(B, C, HW, -1);
+  if (need > kNoAllocScratchBytes) return GBN_EWORKSPACE;
+  return gbn_bn_forward_train(x, dtype, B, C, HW, gamma, beta, running_mean, running_var,
+                              momentum, eps, y, stats, scratch, kNoAllocScratchBytes, stream);
+}

@@ -56,6 +56,8 @@ _SIGNATURES = {
     "gbn_bn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "gbn_bn_forward_train": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                     _P, _P, _P, _SZ, _P]),
+    "gbn_bn_forward_train_noalloc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F,
+                                            _F, _P, _P, _P]),
     "gbn_bn_stats": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _SZ, _P]),
     "gbn_bn_finalize_apply": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                      _P, _P, _P, _SZ, _P]),
@@ -204,6 +206,26 @@ def bn_forward_train(x, gamma=None, beta=None, running_mean=None, running_var=No
             _ptr(running_var), float(momentum), float(eps), _ptr(y), _ptr(stats), _ptr(ws),
             ws.numel() * ws.element_size(), _stream(x.device))
     _check("gbn_bn_forward_train", st)
+    return y, stats
+
+
+def bn_forward_train_noalloc(x, gamma=None, beta=None, running_mean=None, running_var=None,
+                             momentum=0.1, eps=1e-5, *, y=None, stats=None):
+    """Training forward whose scratch is the library's fixed device array
+    (for callers that cannot allocate); see gbn_bn_forward_train_noalloc."""
+    _cuda(x, "x")
+    B, C, HW = _bn_dims(x)
+    for name, t in (("gamma", gamma), ("beta", beta), ("running_mean", running_mean),
+                    ("running_var", running_var)):
+        _fp32_vec(t, name, C)
+    y = torch.empty_like(x) if y is None else _cuda(y, "y")
+    stats = bn_stats_tensor(C, x.device) if stats is None else _cuda(stats, "stats")
+    with torch.cuda.device(x.device):
+        st = lib().gbn_bn_forward_train_noalloc(
+            _ptr(x), _code(x.dtype), B, C, HW, _ptr(gamma), _ptr(beta), _ptr(running_mean),
+            _ptr(running_var), float(momentum), float(eps), _ptr(y), _ptr(stats),
+            _stream(x.device))
+    _check("gbn_bn_forward_train_noalloc", st)
     return y, stats
 
 

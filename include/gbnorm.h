@@ -142,6 +142,26 @@ GBN_API int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C,
                          float momentum, float eps, void* y, float* stats,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* The paper has no counterpart to this call: it exists for callers that
+ * cannot allocate device memory (code inside a CUDA-graph capture or a
+ * real-time loop where cudaMalloc is forbidden, plugins whose host framework
+ * owns every allocation, C callers without an allocator).  Same as
+ * gbn_bn_forward_train without `ws`/`ws_bytes`: the stats partials go to a
+ * fixed 64 KiB file-scope device array inside the library, which every GPU
+ * that loads the library holds until the process exits.  Shapes whose
+ * partials need more (16 * grid_y * C bytes; all C <= 4096 fit on GB300) are
+ * rejected with GBN_EWORKSPACE.  Allocates nothing and nothing needs zeroing:
+ * every call rewrites the partials it reads.  All calls share the one array,
+ * so calls that overlap on the GPU (other streams, other threads) race; order
+ * them on one stream.  The first call on a device resolves the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.                                          */
+GBN_API int gbn_bn_forward_train_noalloc(const void* x, int dtype, int64_t B, int64_t C,
+                                         int64_t HW, const float* gamma, const float* beta,
+                                         float* running_mean, float* running_var,
+                                         float momentum, float eps, void* y, float* stats,
+                                         void* stream);
+
 /* Phase 1 of the forward alone: writes the stats partials into ws.        */
 GBN_API int gbn_bn_stats(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                  void* ws, size_t ws_bytes, void* stream);

@@ -11,8 +11,8 @@ One step = one pass of every hot-path operation over its workload:
   bn_bf16_bwd  BatchNorm2d training backward bf16 [128,256,56,56]
 
 Every call goes through the C ABI (ctypes binding).  Each operation is timed
-with CUDA events on the stream it runs on, after a 256 MB write that flushes
-L2 (outside the events); BatchNorm phases (stats | finalize+apply, grad_sums
+with CUDA events on the stream it runs on, after an L2 flush (a 256 MB write
+then a 256 MB read of another buffer, outside the events); BatchNorm phases (stats | finalize+apply, grad_sums
 | finalize+dx) are timed separately.  value = unique bytes of every input and
 output tensor of the step / summed device time (the effective-bandwidth
 convention), in GB/s, over all ranks.
@@ -314,8 +314,17 @@ def run_ours(args, rank, world, local_rank):
 
     names = args.ops.split(",") if args.ops else OPS_ALL
     ops = build_ops(names, dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    # L2 flush: write one 256 MB buffer, then read another, so L2 is left
+    # holding clean lines of the second buffer -- no dirty write-back of the
+    # flush lands in the next timed operation.
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_out)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -325,7 +334,7 @@ def run_ours(args, rank, world, local_rank):
 
     def one_step(record):
         for op in ops:
-            flush.zero_()
+            flush_l2()
             evs = [torch.cuda.Event(enable_timing=True)]
             evs[0].record(stream)
             for _, fn in op.phases:
@@ -398,7 +407,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {
             "workload": "; ".join(op.desc for op in ops),
             "ops": names,
-            "l2": "256 MB write before every operation (outside the timed events)",
+            "l2": "before every operation: 256 MB write + 256 MB read of another buffer "
+                  "(outside the timed events; L2 left clean)",
             "timing": "CUDA events per operation on the launching stream; sum over ops",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },

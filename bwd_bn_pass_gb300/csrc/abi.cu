@@ -167,7 +167,7 @@ int gbn_bn_stats(const void* x, int dtype, int64_t B, int64_t C, int64_t HW, voi
   const DevInfo* dev;
   rc = bn_prepare(dtype, B, C, HW, true, ptrs, 1, ws, ws_bytes, true, &p, &dev);
   if (rc != GBN_OK) return rc;
-  return to_status(bn_launch_stats(x, dtype, p, static_cast<double*>(ws),
+  return to_status(bn_launch_stats(x, dtype, p, static_cast<float2*>(ws),
                                    static_cast<cudaStream_t>(stream)));
 }
 
@@ -189,7 +189,7 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
   rc = bn_prepare(dtype, B, C, HW, true, ptrs, 2, ws, ws_bytes, true, &p, &dev);
   if (rc != GBN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  double* part = static_cast<double*>(const_cast<void*>(ws));
+  float2* part = static_cast<float2*>(const_cast<void*>(ws));
   if (with_stats_pass) {
     cudaError_t e = bn_launch_stats(x, dtype, p, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;
@@ -253,7 +253,7 @@ static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B,
   rc = bn_prepare(dtype, B, C, HW, true, ptrs, 3, ws, ws_bytes, true, &p, &dev);
   if (rc != GBN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  double* part = static_cast<double*>(const_cast<void*>(ws));
+  float2* part = static_cast<float2*>(const_cast<void*>(ws));
   if (sums) {
     cudaError_t e = bn_launch_grad_sums(x, dy, dtype, p, stats, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;

@@ -41,7 +41,7 @@ struct BnGeom {
   uint64_t step;   // offset change for +blockDim vectors of a channel, no wrap
   uint64_t wrap;   // extra change when the in-plane index wraps: C*Pv - Pv
   int64_t P;       // plane size in elements (x[0, c, 0] is element c*P)
-  double M;        // per-channel count
+  float Mh, Ml;    // per-channel count M = Mh + Ml exactly
   int32_t C;
   int32_t Pv;      // vectors per plane
   int32_t Mv;      // vectors per channel
@@ -85,18 +85,29 @@ __device__ __forceinline__ void slice(const BnGeom& g, int j, int32_t& v0, int32
   cnt = n > 0 ? (n + kBnThreads - 1) / kBnThreads : 0;
 }
 
-// Channel c's partials summed over j in a fixed order by warp 0 (all lanes
-// end with the same values: xor-shuffle trees are symmetric).
-__device__ __forceinline__ void reduce_partials(const double* part, const BnGeom& g, int c,
-                                                double& s0, double& s1) {
+// Channel c's partials summed over j in a fixed order by warp 0, in
+// double-fp32 (GB300's fp64 rate is too low to spend in every block).  All
+// lanes end with the same bits: the xor-shuffle tree of df_sum is symmetric.
+__device__ __forceinline__ void reduce_partials(const float2* part, const BnGeom& g, int c,
+                                                DF& s0, DF& s1) {
   const int lane = threadIdx.x & 31;
-  double a = 0.0, b = 0.0;
+  DF a{0.f, 0.f}, b{0.f, 0.f};
   for (int jj = lane; jj < g.grid_y; jj += 32) {
-    a += part[(int64_t)jj * g.C + c];
-    b += part[((int64_t)g.grid_y + jj) * g.C + c];
+    const float2 p0 = part[(int64_t)jj * g.C + c];
+    const float2 p1 = part[((int64_t)g.grid_y + jj) * g.C + c];
+    a = df_sum(a, DF{p0.x, p0.y});
+    b = df_sum(b, DF{p1.x, p1.y});
   }
-  s0 = warp_sum(a);
-  s1 = warp_sum(b);
+  s0 = warp_sum_df(a);
+  s1 = warp_sum_df(b);
+}
+
+// (hi, lo) / M for the per-channel count M (held exactly as mh + ml).
+__device__ __forceinline__ DF div_count(DF a, float mh, float ml) {
+  const float q = a.hi / mh;
+  const DF p = two_prod(q, mh);
+  const float r = (((a.hi - p.hi) - p.lo) + a.lo) - q * ml;
+  return DF{q, r / mh};
 }
 
 template <typename T>
@@ -124,9 +135,9 @@ constexpr int kUDx = 1;
 
 template <typename T, int VEC, typename I>
 __global__ void __launch_bounds__(kBnThreads, 8)
-    bn_stats_kernel(const T* __restrict__ x, BnGeom g, double* __restrict__ part) {
+    bn_stats_kernel(const T* __restrict__ x, BnGeom g, float2* __restrict__ part) {
   using V = Vec<T, VEC>;
-  __shared__ double red[64];
+  __shared__ float2 red[64];
   pdl_launch_dependents();
   const int c = blockIdx.x, j = blockIdx.y;
   int32_t v0, cnt;
@@ -159,11 +170,10 @@ __global__ void __launch_bounds__(kBnThreads, 8)
       }
     }
   }
-  double t1 = df_value(s1), t2 = df_value(s2);
-  block_sum2(t1, t2, red);
+  block_sum2_df(s1, s2, red);
   if (threadIdx.x == 0) {
-    part[(int64_t)j * g.C + c] = t1;
-    part[((int64_t)g.grid_y + j) * g.C + c] = t2;
+    part[(int64_t)j * g.C + c] = make_float2(s1.hi, s1.lo);
+    part[((int64_t)g.grid_y + j) * g.C + c] = make_float2(s2.hi, s2.lo);
   }
 }
 
@@ -171,7 +181,7 @@ __global__ void __launch_bounds__(kBnThreads, 8)
 
 struct ApplyArgs {
   int mode;
-  const double* part;
+  const float2* part;
   const float* gamma;
   const float* beta;
   float* stats;
@@ -191,30 +201,32 @@ __device__ __noinline__ void apply_prologue(const BnGeom& g, const ApplyArgs& a,
   float shift, mean_d, scale;
   const float beta = a.beta ? a.beta[c] : 0.f;
   if (a.mode == kApplyTrain) {
-    double s1, s2;
+    DF s1, s2;
     reduce_partials(a.part, g, c, s1, s2);
-    const double md = s1 / g.M;
-    double var = s2 / g.M - md * md;
-    if (var < 0.0) var = 0.0;
-    const double inv_std = 1.0 / sqrt(var + (double)a.eps);
-    const double sc = (a.gamma ? (double)a.gamma[c] : 1.0) * inv_std;
+    const DF md = df_norm(div_count(s1, g.Mh, g.Ml));       // mean - shift
+    const DF e2 = div_count(s2, g.Mh, g.Ml);                // E[(x - shift)^2]
+    float var = df_round(df_sum(e2, df_neg(df_mul_df(md, md))));
+    if (!(var > 0.f)) var = 0.f;
+    const float inv_std = 1.f / sqrtf(var + a.eps);
     shift = shift_x;
-    mean_d = (float)md;
-    scale = (float)sc;
+    mean_d = md.hi;
+    scale = (a.gamma ? a.gamma[c] : 1.f) * inv_std;
     if (j == 0 && threadIdx.x == 0) {
       const int64_t C = g.C;
-      const double mean = (double)shift + md;
-      a.stats[c] = (float)mean;
-      a.stats[C + c] = (float)var;
-      a.stats[2 * C + c] = (float)inv_std;
+      const float mean = df_round(df_plus(md, shift));
+      const float M = g.Mh + g.Ml;
+      a.stats[c] = mean;
+      a.stats[C + c] = var;
+      a.stats[2 * C + c] = inv_std;
       a.stats[3 * C + c] = scale;
       a.stats[4 * C + c] = shift;
-      a.stats[5 * C + c] = mean_d;
-      reinterpret_cast<double*>(a.stats + 6 * C)[c] = md;
-      const double m = (double)a.momentum;
-      if (a.running_mean) a.running_mean[c] = (float)((1.0 - m) * a.running_mean[c] + m * mean);
+      a.stats[5 * C + c] = md.hi;
+      a.stats[6 * C + c] = md.hi;
+      a.stats[7 * C + c] = md.lo;
+      const float m = a.momentum;
+      if (a.running_mean) a.running_mean[c] = (1.f - m) * a.running_mean[c] + m * mean;
       if (a.running_var)
-        a.running_var[c] = (float)((1.0 - m) * a.running_var[c] + m * var * (g.M / (g.M - 1.0)));
+        a.running_var[c] = (1.f - m) * a.running_var[c] + m * var * (M / (M - 1.f));
     }
   } else if (a.mode == kApplyStats) {
     const int64_t C = g.C;
@@ -282,9 +294,9 @@ __global__ void __launch_bounds__(kBnThreads, 8)
 template <typename T, int VEC, typename I>
 __global__ void __launch_bounds__(kBnThreads, 8)
     bn_grad_sums_kernel(const T* __restrict__ x, const T* __restrict__ dy, BnGeom g,
-                        const float* __restrict__ stats, double* __restrict__ part) {
+                        const float* __restrict__ stats, float2* __restrict__ part) {
   using V = Vec<T, VEC>;
-  __shared__ double red[64];
+  __shared__ float2 red[64];
   pdl_launch_dependents();
   const int c = blockIdx.x, j = blockIdx.y;
   int32_t v0, cnt;
@@ -320,48 +332,51 @@ __global__ void __launch_bounds__(kBnThreads, 8)
       }
     }
   }
-  double t0 = df_value(s0), t1 = df_value(s1);
-  block_sum2(t0, t1, red);
+  block_sum2_df(s0, s1, red);
   if (threadIdx.x == 0) {
-    part[(int64_t)j * g.C + c] = t0;
-    part[((int64_t)g.grid_y + j) * g.C + c] = t1;
+    part[(int64_t)j * g.C + c] = make_float2(s0.hi, s0.lo);
+    part[((int64_t)g.grid_y + j) * g.C + c] = make_float2(s1.hi, s1.lo);
   }
 }
 
 // ---------------------------------------------------- finalize + dx --
 
 // Warp 0: the backward finalize for channel c (block j = 0 writes grads).
+// S = sum dy*(x - mean) = sum dy*(x - shift) - (mean - shift)*sum dy, in
+// double-fp32 with the forward's (mean - shift) pair.
 __device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
-                                            const double* part, float* grads, int c, int j,
-                                            float* fin) {
-  double p0, p1;
+                                         const float2* part, float* grads, int c, int j,
+                                         float* fin) {
+  DF p0, p1;
   reduce_partials(part, g, c, p0, p1);
   const int64_t C = g.C;
-  const double inv_std = stats[2 * C + c];
-  const double scale = stats[3 * C + c];
-  const double md = reinterpret_cast<const double*>(stats + 6 * C)[c];
-  const double S = p1 - md * p0;  // sum dy*(x - mean)
-  const double k1 = -scale * inv_std * inv_std * S / g.M;
-  const double k2 = -scale * p0 / g.M;
+  const float inv_std = stats[2 * C + c];
+  const float scale = stats[3 * C + c];
+  const DF md{stats[6 * C + c], stats[7 * C + c]};
+  const float S = df_round(df_sum(p1, df_neg(df_mul_df(md, p0))));
+  const float dbeta = df_round(p0);
+  const float M = g.Mh + g.Ml;
+  const float k1 = -(scale * inv_std) * inv_std * S / M;
+  const float k2 = -scale * dbeta / M;
   if (j == 0 && threadIdx.x == 0) {
-    grads[c] = (float)(S * inv_std);
-    grads[C + c] = (float)p0;
-    grads[2 * C + c] = (float)k1;
-    grads[3 * C + c] = (float)k2;
+    grads[c] = S * inv_std;
+    grads[C + c] = dbeta;
+    grads[2 * C + c] = k1;
+    grads[3 * C + c] = k2;
   }
   if (threadIdx.x == 0) {
     fin[0] = stats[4 * C + c];
     fin[1] = stats[5 * C + c];
-    fin[2] = (float)scale;
-    fin[3] = (float)k1;
-    fin[4] = (float)k2;
+    fin[2] = scale;
+    fin[3] = k1;
+    fin[4] = k2;
   }
 }
 
 template <typename T, int VEC, typename I>
 __global__ void __launch_bounds__(kBnThreads, 8)
     bn_dx_kernel(const T* __restrict__ x, const T* dy, T* dx, BnGeom g,
-                 const float* __restrict__ stats, const double* __restrict__ part,
+                 const float* __restrict__ stats, const float2* __restrict__ part,
                  float* __restrict__ grads) {
   using V = Vec<T, VEC>;
   __shared__ float fin[5];  // shift, mean_d, scale, k1, k2
@@ -426,7 +441,8 @@ BnGeom make_geom(const BnPlan& p) {
   g.tmod = (int32_t)(kBnThreads % Pv);
   g.step = (uint64_t)(kBnThreads / Pv) * (uint64_t)p.C * (uint64_t)Pv + (uint64_t)g.tmod;
   g.wrap = (uint64_t)p.C * (uint64_t)Pv - (uint64_t)Pv;
-  g.M = (double)p.M;
+  g.Mh = (float)p.M;
+  g.Ml = (float)(p.M - (int64_t)g.Mh);
   return g;
 }
 
@@ -458,7 +474,7 @@ cudaError_t dispatch(const BnPlan& p, int dtype, A&&... args) {
 }
 
 template <typename T, int VEC, typename I> struct StatsL {
-  static cudaError_t run(const void* x, const BnPlan& p, double* part, cudaStream_t st) {
+  static cudaError_t run(const void* x, const BnPlan& p, float2* part, cudaStream_t st) {
     return launch(bn_stats_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, false,
                   static_cast<const T*>(x), make_geom(p), part);
   }
@@ -472,14 +488,14 @@ template <typename T, int VEC, typename I> struct ApplyL {
 };
 template <typename T, int VEC, typename I> struct GradSumsL {
   static cudaError_t run(const void* x, const void* dy, const BnPlan& p, const float* stats,
-                         double* part, cudaStream_t st) {
+                         float2* part, cudaStream_t st) {
     return launch(bn_grad_sums_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, false,
                   static_cast<const T*>(x), static_cast<const T*>(dy), make_geom(p), stats, part);
   }
 };
 template <typename T, int VEC, typename I> struct DxL {
   static cudaError_t run(const void* x, const void* dy, void* dx, const BnPlan& p,
-                         const float* stats, const double* part, float* grads, cudaStream_t st,
+                         const float* stats, const float2* part, float* grads, cudaStream_t st,
                          bool pdl) {
     return launch(bn_dx_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, pdl,
                   static_cast<const T*>(x), static_cast<const T*>(dy), static_cast<T*>(dx),
@@ -504,7 +520,7 @@ bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan)
   if (gy < 1) gy = 1;
   if (gy > 65535) gy = 65535;
   plan->grid_y = (int)gy;
-  const size_t bytes = (size_t)2 * (size_t)gy * (size_t)(C > 0 ? C : 1) * sizeof(double);
+  const size_t bytes = (size_t)2 * (size_t)gy * (size_t)(C > 0 ? C : 1) * sizeof(float2);
   plan->ws_bytes = (bytes + 255) & ~(size_t)255;
   return true;
 }
@@ -523,13 +539,13 @@ int bn_vec_width(int dtype, int64_t P, const void* const* ptrs, int nptrs) {
   return vec;
 }
 
-cudaError_t bn_launch_stats(const void* x, int dtype, const BnPlan& p, double* part,
+cudaError_t bn_launch_stats(const void* x, int dtype, const BnPlan& p, float2* part,
                             cudaStream_t st) {
   return dispatch<StatsL>(p, dtype, x, p, part, st);
 }
 
 cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, int mode,
-                            const double* part, const float* gamma, const float* beta,
+                            const float2* part, const float* gamma, const float* beta,
                             float* stats, float* running_mean, float* running_var,
                             float momentum, float eps, const float* mean, const float* scale,
                             cudaStream_t st, bool pdl) {
@@ -549,12 +565,12 @@ cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, 
 }
 
 cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const BnPlan& p,
-                                const float* stats, double* part, cudaStream_t st) {
+                                const float* stats, float2* part, cudaStream_t st) {
   return dispatch<GradSumsL>(p, dtype, x, dy, p, stats, part, st);
 }
 
 cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
-                         const float* stats, const double* part, float* grads, cudaStream_t st,
+                         const float* stats, const float2* part, float* grads, cudaStream_t st,
                          bool pdl) {
   return dispatch<DxL>(p, dtype, x, dy, dx, p, stats, part, grads, st, pdl);
 }

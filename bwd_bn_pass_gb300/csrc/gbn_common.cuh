@@ -172,6 +172,57 @@ __device__ __forceinline__ void df_acc(DF& acc, DF t) {
 }
 __device__ __forceinline__ float df_round(DF a) { return a.hi + a.lo; }
 
+// a + b for two (hi, lo) pairs.  Symmetric in a and b (the TwoSum error of
+// hi + hi is exact, and lo + lo is commutative), so an xor-shuffle tree gives
+// every lane the same bits.
+__device__ __forceinline__ DF df_sum(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  return DF{s.hi, (a.lo + b.lo) + s.lo};
+}
+// Renormalise so that hi = fl(hi + lo).
+__device__ __forceinline__ DF df_norm(DF a) { return two_sum(a.hi, a.lo); }
+// (hi, lo) * (hi, lo), first-order terms
+__device__ __forceinline__ DF df_mul_df(DF a, DF b) {
+  DF p = two_prod(a.hi, b.hi);
+  p.lo = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, p.lo));
+  return p;
+}
+// (hi, lo) / d for a positive fp32 d: q = hi/d, then the exact remainder
+// hi - q*d (FMA) plus lo gives the low part.
+__device__ __forceinline__ DF df_div(DF a, float d) {
+  const float q = a.hi / d;
+  const float r = fmaf(-q, d, a.hi) + a.lo;
+  return DF{q, r / d};
+}
+__device__ __forceinline__ DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
+
+__device__ __forceinline__ DF shfl_xor_df(DF v, int o) {
+  return DF{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ DF warp_sum_df(DF v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_sum(v, shfl_xor_df(v, o));
+  return v;
+}
+
+// Sum two (hi, lo) pairs over the block in a fixed tree; every thread gets
+// the result.  `red` must hold 2*32 float2.  Contains __syncthreads.
+__device__ __forceinline__ void block_sum2_df(DF& a, DF& b, float2* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  a = warp_sum_df(a);
+  b = warp_sum_df(b);
+  if (lane == 0) {
+    red[warp] = make_float2(a.hi, a.lo);
+    red[32 + warp] = make_float2(b.hi, b.lo);
+  }
+  __syncthreads();
+  const float2 x = lane < nwarps ? red[lane] : make_float2(0.f, 0.f);
+  const float2 y = lane < nwarps ? red[32 + lane] : make_float2(0.f, 0.f);
+  a = warp_sum_df(DF{x.x, x.y});
+  b = warp_sum_df(DF{y.x, y.y});
+}
+
 // --------------------------------------------------------------- reduce --
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -65,17 +65,17 @@ int bn_vec_width(int dtype, int64_t P, const void* const* ptrs, int nptrs);
 
 enum BnApplyMode { kApplyTrain = 0, kApplyStats = 1, kApplyInfer = 2 };
 
-cudaError_t bn_launch_stats(const void* x, int dtype, const BnPlan& p, double* part,
+cudaError_t bn_launch_stats(const void* x, int dtype, const BnPlan& p, float2* part,
                             cudaStream_t st);
 cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, int mode,
-                            const double* part, const float* gamma, const float* beta,
+                            const float2* part, const float* gamma, const float* beta,
                             float* stats, float* running_mean, float* running_var,
                             float momentum, float eps, const float* mean, const float* scale,
                             cudaStream_t st, bool pdl);
 cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const BnPlan& p,
-                                const float* stats, double* part, cudaStream_t st);
+                                const float* stats, float2* part, cudaStream_t st);
 cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
-                         const float* stats, const double* part, float* grads, cudaStream_t st,
+                         const float* stats, const float2* part, float* grads, cudaStream_t st,
                          bool pdl);
 
 // ------------------------------------------------------------ row-wise --

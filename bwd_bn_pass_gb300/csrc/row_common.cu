@@ -4,8 +4,9 @@
 // The row kernels leave one partial row per block: part[o][plane][g][h] with
 // o the column output (dweight; or dgamma, dbeta, dbias), plane 0 the fp32
 // sum and plane 1 its double-fp32 low part (fp32 outputs only).  colsum adds
-// the G rows of each output in a fixed order (8 strided groups, then the 8
-// group sums in order), so the result is deterministic for a given G.
+// the G rows of each output in a fixed order (32 strided groups, then the 32
+// group sums in order), so the result is deterministic for a given G.  Each
+// thread has at most ceil(G/32) independent loads, all in flight at once.
 #include "gbn_common.cuh"
 #include "gbn_internal.h"
 
@@ -19,7 +20,7 @@ cudaError_t ln_configure(int smem_optin);
 namespace {
 
 constexpr int kColTile = 32;
-constexpr int kColGroups = 8;
+constexpr int kColGroups = 32;
 constexpr int kMaxStages = 8;
 
 struct ColOuts {
@@ -38,7 +39,7 @@ __global__ void __launch_bounds__(kColTile* kColGroups)
   if (h < H) {
     const float* hi = part + ((int64_t)o * nplanes) * G * H + h;
     const float* lo = hi + (int64_t)G * H;
-#pragma unroll 4
+#pragma unroll 8
     for (int g = ty; g < G; g += kColGroups) {
       df_add(acc, hi[(int64_t)g * H]);
       if (COMP) acc.lo += lo[(int64_t)g * H];
@@ -53,8 +54,7 @@ __global__ void __launch_bounds__(kColTile* kColGroups)
       df_add(t, sm[k][tx].hi);
       t.lo += sm[k][tx].lo;
     }
-    const float v = (float)((double)t.hi + (double)t.lo);
-    static_cast<T*>(outs.p[o])[h] = from_f32<T>(v);
+    static_cast<T*>(outs.p[o])[h] = from_f32<T>(df_round(t));
   }
 }
 

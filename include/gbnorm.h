@@ -21,7 +21,7 @@
  *   float atomics are used anywhere.
  * - Return value: GBN_OK (0) or a negative GBN_E* code.  On an argument
  *   error nothing is launched and no output is touched.  GBN_ECUDA reports
- *   a launch error (cudaGetLastError after the launches).  Errors that can
+ *   the error returned by a CUDA query or launch.  Errors that can
  *   only be seen on the device (a bounded wait that ran out) are recorded in
  *   the device status word, read with gbn_get_device_status.
  * - Alignment: any element-aligned pointer is accepted for the large
@@ -78,8 +78,9 @@ extern "C" {
 /* stats: 8*C floats (32*C bytes, 8-byte aligned).  Rows 0..3 are public,
  * fp32 [4, C] = (mean, var, inv_std, scale = gamma*inv_std) as in [P4]
  * "One-pass statistics".  Rows 4..7 are private to this library: row 4 the
- * channel's shift x[0,c,0,0] (fp32), row 5 mean - shift (fp32), rows 6..7 the
- * same mean - shift as fp64 [C] (used by the backward).                     */
+ * channel's shift x[0,c,0,0], row 5 mean - shift rounded to fp32, rows 6 and
+ * 7 the same mean - shift as an unevaluated fp32 pair (hi, lo) that the
+ * backward uses.                                                            */
 #define GBN_BN_STATS_FLOATS(C) (8 * (int64_t)(C))
 /* grads: fp32 [4, C] = (dgamma, dbeta, k1, k2), [P4] "Backward finalize".  */
 #define GBN_BN_GRADS_FLOATS(C) (4 * (int64_t)(C))
@@ -115,8 +116,8 @@ GBN_API int gbn_get_device_status(int device, int* status, int clear);
  * Per channel, M = B*HW elements are reduced.
  *
  * The forward is two launches: a device-sized grid of one-pass shifted-sum
- * blocks writes per-block fp64 partials (sum d, sum d^2 with d = x - x[0,c])
- * into `ws` without atomics; a second kernel, launched with programmatic
+ * blocks writes per-block partials (sum d, sum d^2 with d = x - x[0,c], each
+ * an fp32 (hi, lo) pair) into `ws` without atomics; a second kernel, launched with programmatic
  * dependent launch, reduces the partials of its channel in a fixed order
  * (the "finalize"), writes stats and the running-stat update from the
  * channel's first block, and applies y = (x - mean)*scale + beta in the

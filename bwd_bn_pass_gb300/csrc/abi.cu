@@ -75,6 +75,10 @@ const DevInfo* device_info(int device) {
       cudaDeviceGetAttribute(&n.max_threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, device) !=
           cudaSuccess ||
       cudaDeviceGetAttribute(&n.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&n.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                             device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, device) !=
           cudaSuccess)
     return nullptr;
   void* addr = nullptr;

@@ -106,17 +106,17 @@ __device__ __forceinline__ void reduce_partials(const float2* part, const BnGeom
 __device__ __forceinline__ DF div_count(DF a, float mh, float ml) {
   const float q = a.hi / mh;
   const DF p = two_prod(q, mh);
-  const float r = (((a.hi - p.hi) - p.lo) + a.lo) - q * ml;
+  const float r = __fsub_rn(__fadd_rn(__fsub_rn(__fsub_rn(a.hi, p.hi), p.lo), a.lo), __fmul_rn(q, ml));
   return DF{q, r / mh};
 }
 
 template <typename T>
 __device__ __forceinline__ void x_minus_shift(float e, float shift, float& d, float& d_lo) {
-  d = e - shift;
+  d = __fsub_rn(e, shift);
   if constexpr (sizeof(T) == 4) {
     // rounding error of the subtraction (TwoSum); zero when exact
-    const float bb = d - e;
-    d_lo = (e - (d - bb)) + (-shift - bb);
+    const float bb = __fsub_rn(d, e);
+    d_lo = __fadd_rn(__fsub_rn(e, __fsub_rn(d, bb)), __fsub_rn(-shift, bb));
   } else {
     d_lo = 0.f;  // bf16 operands: the fp32 difference is exact
   }
@@ -124,17 +124,17 @@ __device__ __forceinline__ void x_minus_shift(float e, float shift, float& d, fl
 
 // ------------------------------------------------------------- stats --
 
-// Blocks of 256 threads sized for 8 resident blocks per SM (<= 32
-// registers/thread): vectors stay raw until used.  Vectors in flight per
-// thread: stats 4, apply 2, grad_sums 2 of each input, dx 1 of each input
-// (the most the 32-register budget holds without spilling).
-constexpr int kUStats = 4;
-constexpr int kUApply = 2;
-constexpr int kUSums = 2;
-constexpr int kUDx = 1;
+// Blocks of 256 threads sized for kBnBlocksPerSm (4) resident blocks per SM
+// (<= 64 registers/thread); vectors stay raw until used.  16-byte vectors in
+// flight per thread: stats 8, apply 4, grad_sums 4 of each input, dx 2 of
+// each input -- 128 KB of loads in flight per SM for the read passes.
+constexpr int kUStats = 8;
+constexpr int kUApply = 4;
+constexpr int kUSums = 4;
+constexpr int kUDx = 2;
 
 template <typename T, int VEC, typename I>
-__global__ void __launch_bounds__(kBnThreads, 8)
+__global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
     bn_stats_kernel(const T* __restrict__ x, BnGeom g, float2* __restrict__ part) {
   using V = Vec<T, VEC>;
   __shared__ float2 red[64];
@@ -144,29 +144,57 @@ __global__ void __launch_bounds__(kBnThreads, 8)
   slice(g, j, v0, cnt);
   const float shift = to_f32(x[(int64_t)c * g.P]);
 
-  DF s1 = {0.f, 0.f}, s2 = {0.f, 0.f};
+  DF s1, s2;
   Cursor<I> q = cursor_at<I>(g, c, v0 + (int32_t)threadIdx.x);
-  for (int32_t i = 0; i < cnt; i += kUStats) {
-    typename V::raw r[kUStats];
+  if constexpr (VEC >= 2) {
+    // Two packed lanes: pairs of elements per fp32x2 instruction.
+    const f2 sh2 = f2_pack(shift, shift);
+    DF2 a1{0ull, 0ull}, a2{0ull, 0ull};
+    for (int32_t i = 0; i < cnt; i += kUStats) {
+      typename V::raw r[kUStats];
 #pragma unroll
-    for (int u = 0; u < kUStats; ++u) {
-      if (i + u < cnt) r[u] = V::ld(x + (size_t)q.vo * VEC);
-      cursor_fwd(q, g);
-    }
+      for (int u = 0; u < kUStats; ++u) {
+        if (i + u < cnt) r[u] = V::ld(x + (size_t)q.vo * VEC);
+        cursor_fwd(q, g);
+      }
 #pragma unroll
-    for (int u = 0; u < kUStats; ++u) {
-      if (i + u < cnt) {
-        float e[VEC];
-        V::cvt(r[u], e);
-        float a1 = 0.f, a2 = 0.f;
+      for (int u = 0; u < kUStats; ++u) {
+        if (i + u < cnt) {
+          float e[VEC];
+          V::cvt(r[u], e);
+          f2 l1 = 0ull, l2 = 0ull;  // +0.0f in both lanes
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) {
-          const float d = e[k] - shift;
-          a1 += d;
-          a2 = fmaf(d, d, a2);
+          for (int k = 0; k < VEC / 2; ++k) {
+            const f2 d = f2_sub(f2_pack(e[2 * k], e[2 * k + 1]), sh2);
+            l1 = f2_add(l1, d);
+            l2 = f2_fma(d, d, l2);
+          }
+          df2_add(a1, l1);
+          df2_add(a2, l2);
         }
-        df_add(s1, a1);
-        df_add(s2, a2);
+      }
+    }
+    s1 = df2_fold(a1);
+    s2 = df2_fold(a2);
+  } else {
+    s1 = DF{0.f, 0.f};
+    s2 = DF{0.f, 0.f};
+    for (int32_t i = 0; i < cnt; i += kUStats) {
+      typename V::raw r[kUStats];
+#pragma unroll
+      for (int u = 0; u < kUStats; ++u) {
+        if (i + u < cnt) r[u] = V::ld(x + (size_t)q.vo * VEC);
+        cursor_fwd(q, g);
+      }
+#pragma unroll
+      for (int u = 0; u < kUStats; ++u) {
+        if (i + u < cnt) {
+          float e[VEC];
+          V::cvt(r[u], e);
+          const float d = e[0] - shift;
+          df_add(s1, d);
+          df_add(s2, d * d);
+        }
       }
     }
   }
@@ -242,7 +270,7 @@ __device__ __noinline__ void apply_prologue(const BnGeom& g, const ApplyArgs& a,
 }
 
 template <typename T, int VEC, typename I>
-__global__ void __launch_bounds__(kBnThreads, 8)
+__global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
     bn_apply_kernel(const T* __restrict__ x, T* y, BnGeom g, ApplyArgs a) {
   using V = Vec<T, VEC>;
   __shared__ float fin[4];  // shift, mean_d, scale, beta
@@ -292,7 +320,7 @@ __global__ void __launch_bounds__(kBnThreads, 8)
 // --------------------------------------------------------- grad_sums --
 
 template <typename T, int VEC, typename I>
-__global__ void __launch_bounds__(kBnThreads, 8)
+__global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
     bn_grad_sums_kernel(const T* __restrict__ x, const T* __restrict__ dy, BnGeom g,
                         const float* __restrict__ stats, float2* __restrict__ part) {
   using V = Vec<T, VEC>;
@@ -303,31 +331,76 @@ __global__ void __launch_bounds__(kBnThreads, 8)
   slice(g, j, v0, cnt);
   const float shift = stats[4 * (int64_t)g.C + c];
 
-  DF s0 = {0.f, 0.f}, s1 = {0.f, 0.f};
+  DF s0, s1;
   Cursor<I> q = cursor_at<I>(g, c, v0 + (int32_t)threadIdx.x);
-  for (int32_t i = 0; i < cnt; i += kUSums) {
-    typename V::raw rx[kUSums], rd[kUSums];
+  if constexpr (VEC >= 2) {
+    // Packed lanes.  sum dy and sum dy*d with d = x - shift; every product's
+    // exact residual (FMA against the negated product) and, for fp32 input,
+    // the rounding error of x - shift are kept in the low parts.
+    const f2 sh2 = f2_pack(shift, shift);
+    const f2 nsh2 = f2_pack(-shift, -shift);
+    DF2 a0{0ull, 0ull}, a1{0ull, 0ull};
+    for (int32_t i = 0; i < cnt; i += kUSums) {
+      typename V::raw rx[kUSums], rd[kUSums];
 #pragma unroll
-    for (int u = 0; u < kUSums; ++u) {
-      if (i + u < cnt) {
-        rx[u] = V::ld(x + (size_t)q.vo * VEC);
-        rd[u] = V::ld(dy + (size_t)q.vo * VEC);
+      for (int u = 0; u < kUSums; ++u) {
+        if (i + u < cnt) {
+          rx[u] = V::ld(x + (size_t)q.vo * VEC);
+          rd[u] = V::ld(dy + (size_t)q.vo * VEC);
+        }
+        cursor_fwd(q, g);
       }
-      cursor_fwd(q, g);
+#pragma unroll
+      for (int u = 0; u < kUSums; ++u) {
+        if (i + u < cnt) {
+          float ex[VEC], ed[VEC];
+          V::cvt(rx[u], ex);
+          V::cvt(rd[u], ed);
+#pragma unroll
+          for (int k = 0; k < VEC / 2; ++k) {
+            const f2 x2 = f2_pack(ex[2 * k], ex[2 * k + 1]);
+            const f2 dy2 = f2_pack(ed[2 * k], ed[2 * k + 1]);
+            const f2 d = f2_sub(x2, sh2);
+            const f2 nd = f2_sub(sh2, x2);  // exactly -d
+            df2_add(a0, dy2);
+            const f2 prod = f2_mul_rounded(dy2, d);
+            df2_add(a1, prod);
+            a1.lo = f2_add(a1.lo, f2_fma(dy2, d, f2_mul_rounded(dy2, nd)));
+            if constexpr (sizeof(T) == 4) {
+              const f2 bb = f2_sub(d, x2);
+              const f2 d_lo = f2_add(f2_sub(x2, f2_sub(d, bb)), f2_sub(nsh2, bb));
+              a1.lo = f2_fma(dy2, d_lo, a1.lo);
+            }
+          }
+        }
+      }
     }
+    s0 = df2_fold(a0);
+    s1 = df2_fold(a1);
+  } else {
+    s0 = DF{0.f, 0.f};
+    s1 = DF{0.f, 0.f};
+    for (int32_t i = 0; i < cnt; i += kUSums) {
+      typename V::raw rx[kUSums], rd[kUSums];
 #pragma unroll
-    for (int u = 0; u < kUSums; ++u) {
-      if (i + u < cnt) {
-        float ex[VEC], ed[VEC];
-        V::cvt(rx[u], ex);
-        V::cvt(rd[u], ed);
+      for (int u = 0; u < kUSums; ++u) {
+        if (i + u < cnt) {
+          rx[u] = V::ld(x + (size_t)q.vo * VEC);
+          rd[u] = V::ld(dy + (size_t)q.vo * VEC);
+        }
+        cursor_fwd(q, g);
+      }
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) {
+      for (int u = 0; u < kUSums; ++u) {
+        if (i + u < cnt) {
+          float ex[VEC], ed[VEC];
+          V::cvt(rx[u], ex);
+          V::cvt(rd[u], ed);
           float d, d_lo;
-          x_minus_shift<T>(ex[k], shift, d, d_lo);
-          df_add(s0, ed[k]);
-          df_add_prod(s1, ed[k], d);
-          if constexpr (sizeof(T) == 4) s1.lo = fmaf(ed[k], d_lo, s1.lo);
+          x_minus_shift<T>(ex[0], shift, d, d_lo);
+          df_add(s0, ed[0]);
+          df_add_prod(s1, ed[0], d);
+          if constexpr (sizeof(T) == 4) s1.lo = fmaf(ed[0], d_lo, s1.lo);
         }
       }
     }
@@ -374,7 +447,7 @@ __device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
 }
 
 template <typename T, int VEC, typename I>
-__global__ void __launch_bounds__(kBnThreads, 8)
+__global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
     bn_dx_kernel(const T* __restrict__ x, const T* dy, T* dx, BnGeom g,
                  const float* __restrict__ stats, const float2* __restrict__ part,
                  float* __restrict__ grads) {
@@ -511,9 +584,11 @@ bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan)
   plan->C = C;
   plan->P = HW;
   plan->M = B * HW;
-  // Fill every resident 256-thread block slot once ("Reduction grid"), but
-  // give each block at least kBnMinElemsPerBlock elements.
-  const int64_t slots = (int64_t)dev.sms * (dev.max_threads_sm / kBnThreads);
+  // Fill every resident block slot once ("Reduction grid": the page counts
+  // mp_count * max_threads_per_mp / 256 slots; these kernels hold 64
+  // registers per thread, so kBnBlocksPerSm 256-thread blocks are resident
+  // per SM), but give each block at least kBnMinElemsPerBlock elements.
+  const int64_t slots = (int64_t)dev.sms * kBnBlocksPerSm;
   int64_t gy = C > 0 ? slots / C : 1;
   const int64_t by_work = (plan->M + kBnMinElemsPerBlock - 1) / kBnMinElemsPerBlock;
   if (by_work < gy) gy = by_work;

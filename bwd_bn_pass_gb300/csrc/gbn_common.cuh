@@ -123,33 +123,37 @@ struct DF {
   float hi, lo;
 };
 
+// The error-free transformations below use __fadd_rn / __fsub_rn /
+// __fmul_rn: the compiler never contracts those into an FMA, which would
+// silently break TwoSum (e.g. fusing q = p*r into s = hi + q).
+
 // a += v with the rounding error of the addition kept in a.lo (TwoSum).
 __device__ __forceinline__ void df_add(DF& a, float v) {
-  const float s = a.hi + v;
-  const float bb = s - a.hi;
-  const float err = (a.hi - (s - bb)) + (v - bb);
+  const float s = __fadd_rn(a.hi, v);
+  const float bb = __fsub_rn(s, a.hi);
+  const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(v, bb));
   a.hi = s;
-  a.lo += err;
+  a.lo = __fadd_rn(a.lo, err);
 }
 
 // a += p*q with the product's rounding error kept (FMA residual).
 __device__ __forceinline__ void df_add_prod(DF& a, float p, float q) {
-  const float m = p * q;
+  const float m = __fmul_rn(p, q);
   const float e = fmaf(p, q, -m);
   df_add(a, m);
-  a.lo += e;
+  a.lo = __fadd_rn(a.lo, e);
 }
 
 __device__ __forceinline__ double df_value(const DF& a) { return (double)a.hi + (double)a.lo; }
 
 // Error-free building blocks: exact a + b and a * b as (hi, lo) pairs.
 __device__ __forceinline__ DF two_sum(float a, float b) {
-  const float s = a + b;
-  const float bb = s - a;
-  return DF{s, (a - (s - bb)) + (b - bb)};
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return DF{s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
 }
 __device__ __forceinline__ DF two_prod(float a, float b) {
-  const float p = a * b;
+  const float p = __fmul_rn(a, b);
   return DF{p, fmaf(a, b, -p)};
 }
 // (hi, lo) * b, keeping the exact error of hi*b (lo*b is rounded; it is
@@ -162,22 +166,22 @@ __device__ __forceinline__ DF df_mul(DF a, float b) {
 // (hi, lo) + b
 __device__ __forceinline__ DF df_plus(DF a, float b) {
   DF s = two_sum(a.hi, b);
-  s.lo += a.lo;
+  s.lo = __fadd_rn(s.lo, a.lo);
   return s;
 }
 // acc += t for a (hi, lo) term
 __device__ __forceinline__ void df_acc(DF& acc, DF t) {
   df_add(acc, t.hi);
-  acc.lo += t.lo;
+  acc.lo = __fadd_rn(acc.lo, t.lo);
 }
-__device__ __forceinline__ float df_round(DF a) { return a.hi + a.lo; }
+__device__ __forceinline__ float df_round(DF a) { return __fadd_rn(a.hi, a.lo); }
 
 // a + b for two (hi, lo) pairs.  Symmetric in a and b (the TwoSum error of
 // hi + hi is exact, and lo + lo is commutative), so an xor-shuffle tree gives
 // every lane the same bits.
 __device__ __forceinline__ DF df_sum(DF a, DF b) {
   const DF s = two_sum(a.hi, b.hi);
-  return DF{s.hi, (a.lo + b.lo) + s.lo};
+  return DF{s.hi, __fadd_rn(__fadd_rn(a.lo, b.lo), s.lo)};
 }
 // Renormalise so that hi = fl(hi + lo).
 __device__ __forceinline__ DF df_norm(DF a) { return two_sum(a.hi, a.lo); }
@@ -191,7 +195,7 @@ __device__ __forceinline__ DF df_mul_df(DF a, DF b) {
 // hi - q*d (FMA) plus lo gives the low part.
 __device__ __forceinline__ DF df_div(DF a, float d) {
   const float q = a.hi / d;
-  const float r = fmaf(-q, d, a.hi) + a.lo;
+  const float r = __fadd_rn(fmaf(-q, d, a.hi), a.lo);
   return DF{q, r / d};
 }
 __device__ __forceinline__ DF df_neg(DF a) { return DF{-a.hi, -a.lo}; }
@@ -221,6 +225,114 @@ __device__ __forceinline__ void block_sum2_df(DF& a, DF& b, float2* red) {
   const float2 y = lane < nwarps ? red[32 + lane] : make_float2(0.f, 0.f);
   a = warp_sum_df(DF{x.x, x.y});
   b = warp_sum_df(DF{y.x, y.y});
+}
+
+// -------------------------------------------- packed fp32x2 (sm_100+) --
+//
+// Two fp32 lanes in one 64-bit register, operated on by the paired FP32
+// instructions (add/sub/mul/fma .rn.f32x2): every lane is an ordinary IEEE
+// fp32 operation, two per instruction.
+
+using f2 = unsigned long long;
+
+__device__ __forceinline__ f2 f2_pack(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(f2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// 16 bytes of T as NP packed pairs (lane 0 = the lower-addressed element),
+// and back (bf16 rounding is round-to-nearest-even).
+template <typename T> struct Pairs16;
+template <> struct Pairs16<float> {
+  static constexpr int NP = 2;
+  __device__ static void get(uint4 r, f2 (&p)[NP]) {
+    p[0] = f2_pack(__uint_as_float(r.x), __uint_as_float(r.y));
+    p[1] = f2_pack(__uint_as_float(r.z), __uint_as_float(r.w));
+  }
+  __device__ static uint4 put(const f2 (&p)[NP]) {
+    const float2 a = f2_unpack(p[0]), b = f2_unpack(p[1]);
+    return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b.x),
+                      __float_as_uint(b.y));
+  }
+};
+template <> struct Pairs16<bf16> {
+  static constexpr int NP = 4;
+  __device__ static f2 word(uint32_t w) {
+    return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  __device__ static void get(uint4 r, f2 (&p)[NP]) {
+    p[0] = word(r.x);
+    p[1] = word(r.y);
+    p[2] = word(r.z);
+    p[3] = word(r.w);
+  }
+  __device__ static uint32_t bf2(f2 v) {
+    const float2 t = f2_unpack(v);
+    return pack_bf16x2(t.x, t.y);
+  }
+  __device__ static uint4 put(const f2 (&p)[NP]) {
+    return make_uint4(bf2(p[0]), bf2(p[1]), bf2(p[2]), bf2(p[3]));
+  }
+};
+
+__device__ __forceinline__ f2 f2_splat(float v) { return f2_pack(v, v); }
+__device__ __forceinline__ float f2_hsum(f2 v) {
+  const float2 t = f2_unpack(v);
+  return t.x + t.y;
+}
+
+// a*b rounded once, as an FMA with a +0 addend.  A packed mul.rn.f32x2 that
+// feeds a packed add may be fused into an FMA by the assembler, which breaks
+// TwoSum (s = hi + q must be the rounded sum of the rounded product); an
+// FMA's result is never fused again.  Use this for every product that enters
+// an error-free sum.
+__device__ __forceinline__ f2 f2_mul_rounded(f2 a, f2 b) { return f2_fma(a, b, 0ull); }
+
+// Two independent double-fp32 accumulators, one per lane.
+struct DF2 {
+  f2 hi, lo;
+};
+
+// a += v lane-wise, keeping each addition's exact error (TwoSum).
+__device__ __forceinline__ void df2_add(DF2& a, f2 v) {
+  const f2 s = f2_add(a.hi, v);
+  const f2 bb = f2_sub(s, a.hi);
+  const f2 err = f2_add(f2_sub(a.hi, f2_sub(s, bb)), f2_sub(v, bb));
+  a.hi = s;
+  a.lo = f2_add(a.lo, err);
+}
+
+// The two lanes folded into one (hi, lo) pair.
+__device__ __forceinline__ DF df2_fold(const DF2& a) {
+  const float2 h = f2_unpack(a.hi), l = f2_unpack(a.lo);
+  const DF s = two_sum(h.x, h.y);
+  return DF{s.hi, __fadd_rn(__fadd_rn(l.x, l.y), s.lo)};
 }
 
 // --------------------------------------------------------------- reduce --

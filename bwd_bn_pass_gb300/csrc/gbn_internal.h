@@ -14,6 +14,8 @@ struct DevInfo {
   int sms = 0;               // multiprocessor count (152 on GB300)
   int max_threads_sm = 0;    // resident threads per SM (2048)
   int smem_optin = 0;        // max dynamic shared memory per block (bytes)
+  int smem_per_sm = 0;       // shared memory per SM (bytes)
+  int smem_reserved = 0;     // shared memory the runtime reserves per block
   int* status = nullptr;     // device address of the library status word
   bool ok = false;
 };
@@ -46,6 +48,7 @@ cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // ------------------------------------------------------------- BatchNorm --
 
 constexpr int kBnThreads = 256;
+constexpr int kBnBlocksPerSm = 4;   // resident 256-thread blocks per SM the grid fills
 constexpr int64_t kBnMinElemsPerBlock = 4096;
 
 // Shape facts derived once per call on the host.
@@ -54,7 +57,7 @@ struct BnPlan {
   int64_t M = 0;                // per-channel count B*P
   int grid_y = 0;               // blocks per channel
   int vec = 1;                  // elements per vector access
-  size_t ws_bytes = 0;          // partials bytes (2 * grid_y * C doubles, rounded)
+  size_t ws_bytes = 0;          // partials bytes (2 * grid_y * C fp32 pairs, rounded)
 };
 
 // Fills grid_y / ws_bytes (device-dependent) for a shape; false on error.
@@ -90,6 +93,7 @@ struct RowPlan {
   int threads = 0;     // block size
   int kv = 0;          // 16-byte vectors per thread per row (fast path)
   int rb = 1;          // rows per pipeline stage (fast path)
+  int cps = 1;         // blocks per SM the launch is sized for (fast path)
   int nstage = 0;      // pipeline depth (fast path)
   int G = 0;           // blocks (= rows of column partials)
   int nout = 1;        // column outputs

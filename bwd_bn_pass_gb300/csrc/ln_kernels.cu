@@ -77,10 +77,50 @@ __device__ __forceinline__ uint32_t mask_bits(const uint8_t* p) {
   return bits;
 }
 
-template <typename T, int KV, int RB, bool FUSED>
-__global__ void __launch_bounds__(512, 1) ln_bwd_fast_kernel(LnArgs a) {
+// Sum of the nwarps per-warp partials in slot[0..nwarps) as a fixed
+// pairwise tree (every thread computes the same bits).
+__device__ __forceinline__ float sum_warp_slots(const float* slot, int nwarps) {
+  float v[16];
+#pragma unroll
+  for (int w = 0; w < 16; ++w) v[w] = w < nwarps ? slot[w] : 0.f;
+#pragma unroll
+  for (int step = 1; step < 16; step *= 2)
+#pragma unroll
+    for (int w = 0; w < 16; w += 2 * step) v[w] += v[w + step];
+  return v[0];
+}
+
+// One element's LayerNorm input z from the stage (fused: residual +
+// keep*(input + bias), exact (hi, lo) for fp32 outputs).
+template <bool FUSED, bool COMP>
+__device__ __forceinline__ DF ln_z(float xin, float res, float b, float keep) {
+  if constexpr (!FUSED) {
+    return DF{xin, 0.f};
+  } else if constexpr (COMP) {
+    const DF kt = df_mul(two_sum(xin, b), keep);
+    return df_plus(two_sum(res, kt.hi), kt.lo);
+  } else {
+    return DF{fmaf(keep, xin + b, res), 0.f};
+  }
+}
+
+// keep factors (scale where the mask byte is nonzero, else 0) of the two
+// elements of pair p of a 16-byte vector; the vector's mask bytes are in m
+// (two words for bf16, one for fp32).
+__device__ __forceinline__ f2 keep_pair(uint2 m, int p, float s) {
+  const uint32_t w = (p < 2) ? m.x : m.y;
+  const int sh = (p & 1) * 16;
+  const float lo = ((w >> sh) & 0xffu) ? s : 0.f;
+  const float hi = ((w >> (sh + 8)) & 0xffu) ? s : 0.f;
+  return f2_pack(lo, hi);
+}
+
+template <typename T, int KV, int RB, bool FUSED, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
   constexpr int VE = 16 / sizeof(T);
   constexpr bool COMP = sizeof(T) == 4;
+  using PK = Pairs16<T>;
+  constexpr int NP = PK::NP;
   constexpr uint32_t HDR = ln_header(RB);
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
@@ -119,22 +159,94 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_fast_kernel(LnArgs a) {
   if (tid == 0)
     for (int64_t i = 0; i < nmine && i < nst; ++i) issue(i);
 
+  // Per-column constants and accumulators of this thread's columns.  fp32
+  // outputs use scalar double-fp32 sums; bf16 outputs packed fp32x2 sums.
   float gam[KV][VE], bia[KV][VE];
+  f2 gam2[KV][NP], bia2[KV][NP];
+  DF acc_g[KV][VE], acc_b[KV][VE], acc_x[KV][VE];  // dgamma, dbeta, dbias (fp32 outputs)
+  f2 sg_g[KV][NP], sg_b[KV][NP], sg_x[KV][NP];     // the same, packed (bf16 outputs)
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int vi = tid + k * blockDim.x;
-#pragma unroll
-    for (int e = 0; e < VE; ++e) { gam[k][e] = 0.f; bia[k][e] = 0.f; }
+    uint4 rg = make_uint4(0u, 0u, 0u, 0u), rbias = make_uint4(0u, 0u, 0u, 0u);
     if (vi < a.Hv) {
-      ldg16<T>(static_cast<const T*>(a.gamma) + (int64_t)vi * VE, gam[k]);
-      if (FUSED && a.bias != nullptr) ldg16<T>(static_cast<const T*>(a.bias) + (int64_t)vi * VE, bia[k]);
+      rg = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.gamma) + (int64_t)vi * VE);
+      if (FUSED && a.bias != nullptr)
+        rbias = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.bias) + (int64_t)vi * VE);
     }
-  }
-  DF acc_g[KV][VE], acc_b[KV][VE], acc_x[KV][VE];  // dgamma, dbeta, dbias
+    PK::get(rg, gam2[k]);
+    PK::get(rbias, bia2[k]);
 #pragma unroll
-  for (int k = 0; k < KV; ++k)
+    for (int p = 0; p < NP; ++p) {
+      const float2 gg = f2_unpack(gam2[k][p]), bb = f2_unpack(bia2[k][p]);
+      gam[k][2 * p] = gg.x;
+      gam[k][2 * p + 1] = gg.y;
+      bia[k][2 * p] = bb.x;
+      bia[k][2 * p + 1] = bb.y;
+      sg_g[k][p] = sg_b[k][p] = sg_x[k][p] = 0ull;
+    }
 #pragma unroll
     for (int e = 0; e < VE; ++e) { acc_g[k][e] = acc_b[k][e] = acc_x[k][e] = DF{0.f, 0.f}; }
+  }
+
+  // One 16-byte column vector of row rr of the stage as packed pairs: dy, z
+  // (fused: residual + keep*(input + bias)) and keep.
+  auto load_pairs = [&](const unsigned char* st, int rr, int k, f2 (&dy2)[NP], f2 (&z2)[NP],
+                        f2 (&keep2)[NP]) {
+    const int vi = tid + k * blockDim.x;
+    const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
+    PK::get(*reinterpret_cast<const uint4*>(st + a.off_dy + o), dy2);
+    f2 x2[NP];
+    PK::get(*reinterpret_cast<const uint4*>(st + a.off_x + o), x2);
+    if constexpr (FUSED) {
+      f2 r2[NP];
+      PK::get(*reinterpret_cast<const uint4*>(st + a.off_res + o), r2);
+      uint2 m = make_uint2(0x01010101u, 0x01010101u);
+      if (has_mask) {
+        const unsigned char* mp = st + a.off_mask + (size_t)rr * H + (size_t)vi * VE;
+        if constexpr (VE == 8) m = *reinterpret_cast<const uint2*>(mp);
+        else m.x = *reinterpret_cast<const uint32_t*>(mp);
+      }
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        keep2[p] = keep_pair(m, p, a.scale);
+        z2[p] = f2_fma(keep2[p], f2_add(x2[p], bia2[k][p]), r2[p]);
+      }
+    } else {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        keep2[p] = f2_splat(1.f);
+        z2[p] = x2[p];
+      }
+    }
+  };
+
+  // Scalar form for fp32 outputs: dy, exact z (hi, lo), keep.
+  auto load_elem = [&](const unsigned char* st, int rr, int k, float (&dyv)[VE],
+                       DF (&z)[VE], float (&keep)[VE]) {
+    const int vi = tid + k * blockDim.x;
+    const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
+    float xv[VE];
+    Vec16<T>::load(st + a.off_dy + o, dyv);
+    Vec16<T>::load(st + a.off_x + o, xv);
+    if constexpr (FUSED) {
+      float rv[VE];
+      Vec16<T>::load(st + a.off_res + o, rv);
+      const uint32_t mk =
+          has_mask ? mask_bits<VE>(st + a.off_mask + (size_t)rr * H + (size_t)vi * VE) : 0xffu;
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        keep[e] = ((mk >> e) & 1u) ? a.scale : 0.f;
+        z[e] = ln_z<FUSED, COMP>(xv[e], rv[e], bia[k][e], keep[e]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < VE; ++e) {
+        keep[e] = 1.f;
+        z[e] = DF{xv[e], 0.f};
+      }
+    }
+  };
 
   const float inv_H = 1.f / (float)H;
   bool failed = false;
@@ -153,131 +265,111 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_fast_kernel(LnArgs a) {
     const bool ok = mbar_wait_bounded(&bar[s], par);
     const unsigned char* st = data + (size_t)s * a.stage_bytes;
 
-    // Phase 1: load the stage into registers, row sums of g and g*xhat.
-    float dyv[RB][KV][VE], zv[RB][KV][VE];
-    float zlo[RB][KV][VE];  // exact-z residual (fp32 outputs only)
-    uint32_t mk[RB][KV];
-    float sg[RB], sgx[RB];
-#pragma unroll
-    for (int rr = 0; rr < RB; ++rr) {
-      sg[rr] = 0.f;
-      sgx[rr] = 0.f;
-#pragma unroll
-      for (int k = 0; k < KV; ++k) {
-        const int vi = tid + k * blockDim.x;
-        mk[rr][k] = 0xffu;
-        if (ok && rr < nr && vi < a.Hv) {
-          const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
-          Vec16<T>::load(st + a.off_dy + o, dyv[rr][k]);
-          Vec16<T>::load(st + a.off_x + o, zv[rr][k]);
-          if constexpr (FUSED) {
-            float rv[VE];
-            Vec16<T>::load(st + a.off_res + o, rv);
-            if (has_mask) mk[rr][k] = mask_bits<VE>(st + a.off_mask + (size_t)rr * H + (size_t)vi * VE);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-              const float keep = ((mk[rr][k] >> e) & 1u) ? a.scale : 0.f;
-              if constexpr (COMP) {
-                const DF kt = df_mul(two_sum(zv[rr][k][e], bia[k][e]), keep);
-                const DF z = df_plus(two_sum(rv[e], kt.hi), kt.lo);
-                zv[rr][k][e] = z.hi;
-                zlo[rr][k][e] = z.lo;
-              } else {
-                zv[rr][k][e] = fmaf(keep, zv[rr][k][e] + bia[k][e], rv[e]);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < VE; ++e) zlo[rr][k][e] = 0.f;
-          }
-#pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            const float xh = (zv[rr][k][e] - mu[rr]) * rho[rr];
-            const float gg = dyv[rr][k][e] * gam[k][e];
-            sg[rr] += gg;
-            sgx[rr] = fmaf(gg, xh, sgx[rr]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            dyv[rr][k][e] = 0.f;
-            zv[rr][k][e] = 0.f;
-            zlo[rr][k][e] = 0.f;
-          }
-        }
-      }
-    }
+    // Pass 1 over the stage: row sums of g and g*xhat.
     float* slot = red + (i & 1) * (2 * RB * 32);
 #pragma unroll
     for (int rr = 0; rr < RB; ++rr) {
-      const float a0 = warp_sum(sg[rr]);
-      const float a1 = warp_sum(sgx[rr]);
-      if (lane == 0) { slot[(2 * rr) * 32 + warp] = a0; slot[(2 * rr + 1) * 32 + warp] = a1; }
+      float sg = 0.f, sgx = 0.f;
+      if (ok && rr < nr) {
+        const f2 mu2 = f2_splat(mu[rr]), rho2 = f2_splat(rho[rr]);
+        f2 sg2 = 0ull, sgx2 = 0ull;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+          if (tid + k * (int)blockDim.x >= a.Hv) continue;
+          f2 dy2[NP], z2[NP], keep2[NP];
+          load_pairs(st, rr, k, dy2, z2, keep2);
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            const f2 xh2 = f2_mul(f2_sub(z2[p], mu2), rho2);
+            const f2 g2 = f2_mul(dy2[p], gam2[k][p]);
+            sg2 = f2_add(sg2, g2);
+            sgx2 = f2_fma(g2, xh2, sgx2);
+          }
+        }
+        sg = f2_hsum(sg2);
+        sgx = f2_hsum(sgx2);
+      }
+      sg = warp_sum(sg);
+      sgx = warp_sum(sgx);
+      if (lane == 0) { slot[(2 * rr) * 32 + warp] = sg; slot[(2 * rr + 1) * 32 + warp] = sgx; }
     }
     if (__syncthreads_or(!ok)) { failed = true; break; }
-    if (tid == 0 && i + nst < nmine) {
+    if (tid == 0 && i >= 1 && i - 1 + nst < nmine) {
       fence_proxy_async_smem();
-      issue(i + nst);
+      issue(i - 1 + nst);
     }
 
-    // Phase 2: dz, outputs, column sums.
+    // Pass 2 over the stage: dz, outputs, column sums.
 #pragma unroll
     for (int rr = 0; rr < RB; ++rr) {
       if (rr >= nr) break;
-      float SG = 0.f, SGX = 0.f;
-      for (int wi = 0; wi < nwarps; ++wi) {
-        SG += slot[(2 * rr) * 32 + wi];
-        SGX += slot[(2 * rr + 1) * 32 + wi];
-      }
-      const float mg = SG * inv_H, mgx = SGX * inv_H;
+      const float mg = sum_warp_slots(slot + (2 * rr) * 32, nwarps) * inv_H;
+      const float mgx = sum_warp_slots(slot + (2 * rr + 1) * 32, nwarps) * inv_H;
       const int64_t r = r0 + rr;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int vi = tid + k * blockDim.x;
         if (vi >= a.Hv) continue;
         const int64_t go = r * H + (int64_t)vi * VE;
-        float dzx[VE];
-        if (a.dzx != nullptr) {
+        if constexpr (COMP) {
+          float dzx[VE];
+          if (a.dzx != nullptr) {
 #pragma unroll
-          for (int e = 0; e < VE; e += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(a.dzx + go + e);
-            dzx[e] = t.x; dzx[e + 1] = t.y; dzx[e + 2] = t.z; dzx[e + 3] = t.w;
+            for (int e = 0; e < VE; e += 4) {
+              const float4 t = *reinterpret_cast<const float4*>(a.dzx + go + e);
+              dzx[e] = t.x; dzx[e + 1] = t.y; dzx[e + 2] = t.z; dzx[e + 3] = t.w;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < VE; ++e) dzx[e] = 0.f;
           }
-        } else {
+          float dyv[VE], keep[VE];
+          DF z[VE];
+          load_elem(st, rr, k, dyv, z, keep);
+          float o_dz[VE], o_dx[VE];
 #pragma unroll
-          for (int e = 0; e < VE; ++e) dzx[e] = 0.f;
-        }
-        float o_dz[VE], o_dx[VE];
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          const float dyy = dyv[rr][k][e];
-          const float keep = FUSED ? (((mk[rr][k] >> e) & 1u) ? a.scale : 0.f) : 1.f;
-          if constexpr (COMP) {
+          for (int e = 0; e < VE; ++e) {
             // fp32 outputs: column sums of exactly evaluated terms
-            const DF xh = df_mul(df_plus(two_sum(zv[rr][k][e], -mu[rr]), zlo[rr][k][e]), rho[rr]);
+            const float dyy = dyv[e];
+            const DF xh = df_mul(df_plus(two_sum(z[e].hi, -mu[rr]), z[e].lo), rho[rr]);
             DF inner = df_plus(two_prod(dyy, gam[k][e]), -mg);
             const DF xm = df_mul(xh, mgx);
             inner = df_plus(DF{inner.hi, inner.lo - xm.lo}, -xm.hi);
             const DF dz = df_plus(df_mul(inner, rho[rr]), dzx[e]);
-            const DF dxd = df_mul(dz, keep);
+            const DF dxd = df_mul(dz, keep[e]);
             o_dz[e] = df_round(dz);
             o_dx[e] = df_round(dxd);
             df_acc(acc_g[k][e], df_mul(xh, dyy));
             df_add(acc_b[k][e], dyy);
             if (FUSED) df_acc(acc_x[k][e], dxd);
-          } else {
-            const float xh = (zv[rr][k][e] - mu[rr]) * rho[rr];
-            const float gg = dyy * gam[k][e];
-            const float dz = fmaf(rho[rr], gg - mg - xh * mgx, dzx[e]);
-            o_dz[e] = dz;
-            o_dx[e] = FUSED ? dz * keep : dz;
-            acc_g[k][e].hi = fmaf(dyy, xh, acc_g[k][e].hi);
-            acc_b[k][e].hi += dyy;
-            if (FUSED) acc_x[k][e].hi += o_dx[e];
           }
+          Vec16<T>::store(static_cast<T*>(a.dx) + go, o_dx);
+          if (FUSED && a.dres != nullptr) Vec16<T>::store(static_cast<T*>(a.dres) + go, o_dz);
+        } else {
+          f2 dy2[NP], z2[NP], keep2[NP], dz2[NP], dx2[NP];
+          load_pairs(st, rr, k, dy2, z2, keep2);
+          const f2 mu2 = f2_splat(mu[rr]), rho2 = f2_splat(rho[rr]);
+          const f2 mg2 = f2_splat(mg), nmgx2 = f2_splat(-mgx);
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            const f2 xh2 = f2_mul(f2_sub(z2[p], mu2), rho2);
+            const f2 g2 = f2_mul(dy2[p], gam2[k][p]);
+            const f2 inner = f2_fma(xh2, nmgx2, f2_sub(g2, mg2));
+            f2 extra = 0ull;
+            if (a.dzx != nullptr) {
+              const float2 t = *reinterpret_cast<const float2*>(a.dzx + go + 2 * p);
+              extra = f2_pack(t.x, t.y);
+            }
+            dz2[p] = f2_fma(inner, rho2, extra);
+            dx2[p] = FUSED ? f2_mul(dz2[p], keep2[p]) : dz2[p];
+            sg_g[k][p] = f2_fma(dy2[p], xh2, sg_g[k][p]);
+            sg_b[k][p] = f2_add(sg_b[k][p], dy2[p]);
+            if (FUSED) sg_x[k][p] = f2_add(sg_x[k][p], dx2[p]);
+          }
+          *reinterpret_cast<uint4*>(static_cast<T*>(a.dx) + go) = PK::put(dx2);
+          if (FUSED && a.dres != nullptr)
+            *reinterpret_cast<uint4*>(static_cast<T*>(a.dres) + go) = PK::put(dz2);
         }
-        Vec16<T>::store(static_cast<T*>(a.dx) + go, o_dx);
-        if (FUSED && a.dres != nullptr) Vec16<T>::store(static_cast<T*>(a.dres) + go, o_dz);
       }
     }
   }
@@ -285,11 +377,28 @@ __global__ void __launch_bounds__(512, 1) ln_bwd_fast_kernel(LnArgs a) {
   if (failed) {
     report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
     if (tid == 0) {
-      for (int64_t k = i; k < nmine && k < i + nst; ++k)
+      // Blocks issued and not consumed: i .. i + nst - 2 (lagged refill).
+      for (int64_t k = i; k < nmine && k < i + nst - 1; ++k)
         mbar_wait_bounded(&bar[k % nst], (uint32_t)((k / nst) & 1), kWaitLimitNs / 8);
     }
     __syncthreads();
     return;
+  }
+
+  if constexpr (!COMP) {
+#pragma unroll
+    for (int k = 0; k < KV; ++k)
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        const float2 a0 = f2_unpack(sg_g[k][p]), a1 = f2_unpack(sg_b[k][p]),
+                     a2 = f2_unpack(sg_x[k][p]);
+        acc_g[k][2 * p].hi = a0.x;
+        acc_g[k][2 * p + 1].hi = a0.y;
+        acc_b[k][2 * p].hi = a1.x;
+        acc_b[k][2 * p + 1].hi = a1.y;
+        acc_x[k][2 * p].hi = a2.x;
+        acc_x[k][2 * p + 1].hi = a2.y;
+      }
   }
 
   // Column partials [nout][nplanes][G][H]: 0 = dgamma, 1 = dbeta, 2 = dbias.
@@ -425,27 +534,30 @@ __global__ void __launch_bounds__(256) ln_bwd_generic_kernel(LnArgs a) {
   pdl_launch_dependents();
 }
 
-template <typename T, int KV, int RB, bool FUSED>
+template <typename T, int KV, int RB, bool FUSED, int MAXT, int MINB>
 cudaError_t launch_fast(const RowPlan& p, const LnArgs& a, cudaStream_t st) {
-  return launch(ln_bwd_fast_kernel<T, KV, RB, FUSED>, dim3(p.G), dim3(p.threads), p.smem, st,
-                false, a);
+  return launch(ln_bwd_fast_kernel<T, KV, RB, FUSED, MAXT, MINB>, dim3(p.G), dim3(p.threads),
+                p.smem, st, false, a);
 }
 
+// Instances (KV, RB, max threads, min blocks per SM).  Two rows per stage
+// and three blocks per SM for rows of at most 256 16-byte vectors (85
+// registers); one block per SM otherwise (128 registers).  The plan keeps at
+// most 16 owned columns per thread, so kv is 1 or 2.
 template <typename T, bool FUSED>
 cudaError_t launch_typed(const RowPlan& p, const LnArgs& a, cudaStream_t st) {
   if (!p.fast)
     return launch(ln_bwd_generic_kernel<T, FUSED>, dim3(p.G), dim3(p.threads), 0, st, false, a);
-  // The plan keeps at most 16 owned columns per thread: kv is 1 or 2.
-  if (p.rb == 2) return launch_fast<T, 1, 2, FUSED>(p, a, st);
-  if (p.kv == 1) return launch_fast<T, 1, 1, FUSED>(p, a, st);
-  return launch_fast<T, 2, 1, FUSED>(p, a, st);
+  if (p.rb == 2) return launch_fast<T, 1, 2, FUSED, 256, 3>(p, a, st);
+  if (p.kv == 1) return launch_fast<T, 1, 1, FUSED, 512, 1>(p, a, st);
+  return launch_fast<T, 2, 1, FUSED, 512, 1>(p, a, st);
 }
 
-template <typename T, int KV, int RB>
+template <typename T, int KV, int RB, int MAXT, int MINB>
 cudaError_t set_smem(int bytes) {
-  cudaError_t e1 = cudaFuncSetAttribute(ln_bwd_fast_kernel<T, KV, RB, true>,
+  cudaError_t e1 = cudaFuncSetAttribute(ln_bwd_fast_kernel<T, KV, RB, true, MAXT, MINB>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  cudaError_t e2 = cudaFuncSetAttribute(ln_bwd_fast_kernel<T, KV, RB, false>,
+  cudaError_t e2 = cudaFuncSetAttribute(ln_bwd_fast_kernel<T, KV, RB, false, MAXT, MINB>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e1 != cudaSuccess ? e1 : e2;
 }
@@ -453,9 +565,9 @@ cudaError_t set_smem(int bytes) {
 template <typename T>
 cudaError_t set_smem_all(int bytes) {
   cudaError_t e = cudaSuccess, r;
-  if ((r = set_smem<T, 1, 2>(bytes)) != cudaSuccess) e = r;
-  if ((r = set_smem<T, 1, 1>(bytes)) != cudaSuccess) e = r;
-  if ((r = set_smem<T, 2, 1>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 1, 2, 256, 3>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 1, 1, 512, 1>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 2, 1, 512, 1>(bytes)) != cudaSuccess) e = r;
   return e;
 }
 

@@ -27,8 +27,8 @@ namespace gbn {
 
 namespace {
 
-constexpr int kMaxStages = 8;
-constexpr uint32_t kRmsHeader = 64 + 2 * 32 * 4;  // mbarriers + row-sum slots
+// Shared memory: 8 mbarriers, then [2][RB][32] row-sum slots, then stages.
+__host__ __device__ constexpr uint32_t rms_header(int rb) { return 64 + 2 * rb * 32 * 4; }
 
 struct RmsArgs {
   const void* dy;
@@ -45,29 +45,48 @@ struct RmsArgs {
   uint32_t row_bytes;
 };
 
-template <typename T, int KV, bool COMP>
-__global__ void __launch_bounds__(512, 1) rms_bwd_fast_kernel(RmsArgs a) {
-  constexpr int VE = 16 / sizeof(T);
+// Sum of the nwarps per-warp partials in slot[0..nwarps) as a fixed
+// pairwise tree (every thread computes the same bits).
+__device__ __forceinline__ float sum_warp_slots(const float* slot, int nwarps) {
+  float v[16];
+#pragma unroll
+  for (int w = 0; w < 16; ++w) v[w] = w < nwarps ? slot[w] : 0.f;
+#pragma unroll
+  for (int step = 1; step < 16; step *= 2)
+#pragma unroll
+    for (int w = 0; w < 16; w += 2 * step) v[w] += v[w + step];
+  return v[0];
+}
+
+template <typename T, int KV, int RB, bool COMP, int MINB>
+__global__ void __launch_bounds__(512, MINB) rms_bwd_fast_kernel(RmsArgs a) {
+  using PK = Pairs16<T>;
+  constexpr int NP = PK::NP;  // packed pairs per 16-byte vector
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + 64);
-  unsigned char* data = smem + kRmsHeader;
+  float* red = reinterpret_cast<float*>(smem + 64);  // [2][RB][32]
+  unsigned char* data = smem + rms_header(RB);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   const int g = blockIdx.x, G = gridDim.x;
-  const int64_t nrows = (a.R - g + G - 1) / G;
+  const int64_t nblk = (a.R + RB - 1) / RB;
+  const int64_t nmine = (nblk - g + G - 1) / G;
   const int nst = a.nstage;
   const uint32_t rb = a.row_bytes;
+  const uint32_t xoff = RB * rb;  // dy rows follow the x rows in a stage
   const char* gx = static_cast<const char*>(a.x);
   const char* gdy = static_cast<const char*>(a.dy);
 
   auto issue = [&](int64_t i) {
     const int s = (int)(i % nst);
-    const int64_t r = g + i * G;
-    mbar_arrive_expect_tx(&bar[s], 2u * rb);
-    bulk_g2s(data + (size_t)(2 * s) * rb, gx + r * rb, rb, &bar[s]);
-    bulk_g2s(data + (size_t)(2 * s + 1) * rb, gdy + r * rb, rb, &bar[s]);
+    const int64_t r0 = (g + i * G) * RB;
+    const int64_t nr = a.R - r0 < RB ? a.R - r0 : RB;
+    const uint32_t bytes = (uint32_t)nr * rb;
+    unsigned char* st = data + (size_t)s * 2 * xoff;
+    mbar_arrive_expect_tx(&bar[s], 2u * bytes);
+    bulk_g2s(st, gx + r0 * rb, bytes, &bar[s]);
+    bulk_g2s(st + xoff, gdy + r0 * rb, bytes, &bar[s]);
   };
 
   if (tid == 0) {
@@ -76,85 +95,98 @@ __global__ void __launch_bounds__(512, 1) rms_bwd_fast_kernel(RmsArgs a) {
   }
   __syncthreads();
   if (tid == 0)
-    for (int64_t i = 0; i < nrows && i < nst; ++i) issue(i);
+    for (int64_t i = 0; i < nmine && i < nst; ++i) issue(i);
 
-  float wv[KV][VE];
+  // Weights and the dweight accumulators of this thread's columns, packed.
+  f2 w2[KV][NP], acc[KV][NP], acc_lo[KV][NP];
   const T* w = static_cast<const T*>(a.w);
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int vi = tid + k * blockDim.x;
-    if (vi < a.Hv) Vec16<T>::load(w + (int64_t)vi * VE, wv[k]);
-    else
+    const uint4 rw = vi < a.Hv ? *reinterpret_cast<const uint4*>(w + (int64_t)vi * (2 * NP))
+                               : make_uint4(0u, 0u, 0u, 0u);
+    PK::get(rw, w2[k]);
 #pragma unroll
-      for (int e = 0; e < VE; ++e) wv[k][e] = 0.f;
+    for (int p = 0; p < NP; ++p) { acc[k][p] = 0ull; acc_lo[k][p] = 0ull; }
   }
-  DF acc[KV][VE];
-#pragma unroll
-  for (int k = 0; k < KV; ++k)
-#pragma unroll
-    for (int e = 0; e < VE; ++e) acc[k][e] = DF{0.f, 0.f};
 
   const float Hf = (float)a.H;
   bool failed = false;
   int64_t i = 0;
-  for (; i < nrows; ++i) {
+  for (; i < nmine; ++i) {
     const int s = (int)(i % nst);
     const uint32_t par = (uint32_t)((i / nst) & 1);
-    const int64_t r = g + i * G;
-    const float rho = a.rstd[r];
+    const int64_t r0 = (g + i * G) * RB;
+    const int nr = (int)(a.R - r0 < RB ? a.R - r0 : RB);
+    float rho[RB];
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) rho[rr] = rr < nr ? a.rstd[r0 + rr] : 0.f;
     const bool ok = mbar_wait_bounded(&bar[s], par);
+    const unsigned char* sx = data + (size_t)s * 2 * xoff;
+    const unsigned char* sdy = sx + xoff;
 
-    float xv[KV][VE], dv[KV][VE];
-    float part = 0.f;
-    const unsigned char* sx = data + (size_t)(2 * s) * rb;
-    const unsigned char* sdy = data + (size_t)(2 * s + 1) * rb;
+    // Row sums S = sum_j w_j dy_j x_j (two lanes per instruction).
+    float* slot = red + (i & 1) * (RB * 32);
 #pragma unroll
-    for (int k = 0; k < KV; ++k) {
-      const int vi = tid + k * blockDim.x;
-      if (ok && vi < a.Hv) {
-        Vec16<T>::load(sx + (size_t)vi * 16, xv[k]);
-        Vec16<T>::load(sdy + (size_t)vi * 16, dv[k]);
-      } else {
+    for (int rr = 0; rr < RB; ++rr) {
+      f2 part = 0ull;
+      if (ok && rr < nr) {
 #pragma unroll
-        for (int e = 0; e < VE; ++e) { xv[k][e] = 0.f; dv[k][e] = 0.f; }
-      }
+        for (int k = 0; k < KV; ++k) {
+          const int vi = tid + k * blockDim.x;
+          if (vi < a.Hv) {
+            f2 x2[NP], d2[NP];
+            PK::get(*reinterpret_cast<const uint4*>(sx + (size_t)rr * rb + (size_t)vi * 16), x2);
+            PK::get(*reinterpret_cast<const uint4*>(sdy + (size_t)rr * rb + (size_t)vi * 16), d2);
 #pragma unroll
-      for (int e = 0; e < VE; ++e) part = fmaf(wv[k][e] * dv[k][e], xv[k][e], part);
-    }
-    part = warp_sum(part);
-    float* slot = red + (i & 1) * 32;
-    if (lane == 0) slot[warp] = part;
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    // Every thread holds its part of row i in registers: refill the stage.
-    if (tid == 0 && i + nst < nrows) {
-      fence_proxy_async_smem();
-      issue(i + nst);
-    }
-    float S = 0.f;
-    for (int wi = 0; wi < nwarps; ++wi) S += slot[wi];
-    const float coef = rho * rho * rho * S / Hf;
-
-    T* dxr = static_cast<T*>(a.dx) + r * (int64_t)a.H;
-#pragma unroll
-    for (int k = 0; k < KV; ++k) {
-      const int vi = tid + k * blockDim.x;
-      if (vi < a.Hv) {
-        float o[VE];
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          o[e] = fmaf(-xv[k][e], coef, rho * wv[k][e] * dv[k][e]);
-          if constexpr (COMP) {
-            const float p = dv[k][e] * xv[k][e];
-            const float pe = fmaf(dv[k][e], xv[k][e], -p);
-            const float q = p * rho;
-            const float qe = fmaf(p, rho, -q);
-            df_add(acc[k][e], q);
-            acc[k][e].lo += fmaf(pe, rho, qe);
-          } else {
-            acc[k][e].hi = fmaf(dv[k][e] * xv[k][e], rho, acc[k][e].hi);
+            for (int p = 0; p < NP; ++p) part = f2_fma(f2_mul(w2[k][p], d2[p]), x2[p], part);
           }
         }
-        Vec16<T>::store(dxr + (int64_t)vi * VE, o);
+      }
+      const float v = warp_sum(f2_hsum(part));
+      if (lane == 0) slot[rr * 32 + warp] = v;
+    }
+    if (__syncthreads_or(!ok)) { failed = true; break; }
+    // Every thread is past iteration i-1: its stage can be refilled.
+    if (tid == 0 && i >= 1 && i - 1 + nst < nmine) {
+      fence_proxy_async_smem();
+      issue(i - 1 + nst);
+    }
+
+#pragma unroll
+    for (int rr = 0; rr < RB; ++rr) {
+      if (rr >= nr) break;
+      const float S = sum_warp_slots(slot + rr * 32, nwarps);
+      const float coef = rho[rr] * rho[rr] * rho[rr] * S / Hf;
+      const f2 rho2 = f2_splat(rho[rr]);
+      const f2 ncoef2 = f2_splat(-coef);
+      T* dxr = static_cast<T*>(a.dx) + (r0 + rr) * (int64_t)a.H;
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int vi = tid + k * blockDim.x;
+        if (vi >= a.Hv) continue;
+        f2 x2[NP], d2[NP], o2[NP];
+        PK::get(*reinterpret_cast<const uint4*>(sx + (size_t)rr * rb + (size_t)vi * 16), x2);
+        PK::get(*reinterpret_cast<const uint4*>(sdy + (size_t)rr * rb + (size_t)vi * 16), d2);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          // dx = rstd*w*dy - x*rstd^3*S/H
+          o2[p] = f2_fma(x2[p], ncoef2, f2_mul(rho2, f2_mul(w2[k][p], d2[p])));
+          if constexpr (COMP) {
+            // dweight += dy*x*rstd with both products' exact residuals
+            const f2 prod = f2_mul_rounded(d2[p], x2[p]);
+            const f2 pe = f2_fma(d2[p], x2[p], f2_sub(0ull, prod));
+            const f2 q = f2_mul_rounded(prod, rho2);
+            const f2 qe = f2_fma(prod, rho2, f2_sub(0ull, q));
+            DF2 t{acc[k][p], acc_lo[k][p]};
+            df2_add(t, q);
+            acc[k][p] = t.hi;
+            acc_lo[k][p] = f2_add(t.lo, f2_fma(pe, rho2, qe));
+          } else {
+            acc[k][p] = f2_fma(f2_mul(d2[p], x2[p]), rho2, acc[k][p]);
+          }
+        }
+        *reinterpret_cast<uint4*>(dxr + (int64_t)vi * (2 * NP)) = PK::put(o2);
       }
     }
   }
@@ -162,8 +194,8 @@ __global__ void __launch_bounds__(512, 1) rms_bwd_fast_kernel(RmsArgs a) {
   if (failed) {
     report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
     if (tid == 0) {
-      // Let the copies still in flight land before the block exits.
-      for (int64_t k = i; k < nrows && k < i + nst; ++k)
+      // Blocks issued and not consumed: i .. i + nst - 2 (lagged refill).
+      for (int64_t k = i; k < nmine && k < i + nst - 1; ++k)
         mbar_wait_bounded(&bar[k % nst], (uint32_t)((k / nst) & 1), kWaitLimitNs / 8);
     }
     __syncthreads();
@@ -176,13 +208,16 @@ __global__ void __launch_bounds__(512, 1) rms_bwd_fast_kernel(RmsArgs a) {
   for (int k = 0; k < KV; ++k) {
     const int vi = tid + k * blockDim.x;
     if (vi < a.Hv) {
+      float4* h4 = reinterpret_cast<float4*>(hi + (int64_t)vi * (2 * NP));
+      float4* l4 = reinterpret_cast<float4*>(lo + (int64_t)vi * (2 * NP));
 #pragma unroll
-      for (int e = 0; e < VE; e += 4) {
-        *reinterpret_cast<float4*>(hi + (int64_t)vi * VE + e) =
-            make_float4(acc[k][e].hi, acc[k][e + 1].hi, acc[k][e + 2].hi, acc[k][e + 3].hi);
-        if constexpr (COMP)
-          *reinterpret_cast<float4*>(lo + (int64_t)vi * VE + e) =
-              make_float4(acc[k][e].lo, acc[k][e + 1].lo, acc[k][e + 2].lo, acc[k][e + 3].lo);
+      for (int p = 0; p < NP; p += 2) {
+        const float2 a0 = f2_unpack(acc[k][p]), a1 = f2_unpack(acc[k][p + 1]);
+        h4[p / 2] = make_float4(a0.x, a0.y, a1.x, a1.y);
+        if constexpr (COMP) {
+          const float2 b0 = f2_unpack(acc_lo[k][p]), b1 = f2_unpack(acc_lo[k][p + 1]);
+          l4[p / 2] = make_float4(b0.x, b0.y, b1.x, b1.y);
+        }
       }
     }
   }
@@ -226,12 +261,10 @@ __global__ void __launch_bounds__(256) rms_bwd_generic_kernel(RmsArgs a) {
       dx[r * H + j] = from_f32<T>(fmaf(-xv, coef, rho * to_f32(w[j]) * dv));
       if constexpr (COMP) {
         DF acc{hi[j], lo[j]};
-        const float p = dv * xv;
-        const float pe = fmaf(dv, xv, -p);
-        const float q = p * rho;
-        const float qe = fmaf(p, rho, -q);
-        df_add(acc, q);
-        acc.lo += fmaf(pe, rho, qe);
+        const DF p = two_prod(dv, xv);
+        const DF q = two_prod(p.hi, rho);
+        df_add(acc, q.hi);
+        acc.lo = __fadd_rn(acc.lo, fmaf(p.lo, rho, q.lo));
         hi[j] = acc.hi;
         lo[j] = acc.lo;
       } else {
@@ -242,49 +275,56 @@ __global__ void __launch_bounds__(256) rms_bwd_generic_kernel(RmsArgs a) {
   pdl_launch_dependents();
 }
 
-template <typename T, int KV>
+template <typename T, int KV, int RB, int MINB>
 cudaError_t launch_fast(const RowPlan& p, const RmsArgs& a, cudaStream_t st) {
   constexpr bool COMP = sizeof(T) == 4;
-  return launch(rms_bwd_fast_kernel<T, KV, COMP>, dim3(p.G), dim3(p.threads), p.smem, st, false, a);
+  return launch(rms_bwd_fast_kernel<T, KV, RB, COMP, MINB>, dim3(p.G), dim3(p.threads), p.smem,
+                st, false, a);
 }
 
+// Instances: (KV, RB, min blocks per SM).  The plan picks RB = 2 for short
+// rows and 2 blocks per SM whenever the columns a thread owns fit.
 template <typename T>
 cudaError_t launch_typed(const RowPlan& p, const RmsArgs& a, cudaStream_t st) {
   if (!p.fast) {
     constexpr bool COMP = sizeof(T) == 4;
     return launch(rms_bwd_generic_kernel<T, COMP>, dim3(p.G), dim3(p.threads), 0, st, false, a);
   }
+  if (p.rb == 2) return launch_fast<T, 1, 2, 2>(p, a, st);
   switch (p.kv) {
-    case 1: return launch_fast<T, 1>(p, a, st);
-    case 2: return launch_fast<T, 2>(p, a, st);
-    case 3: return launch_fast<T, 3>(p, a, st);
-    default: return launch_fast<T, 4>(p, a, st);
+    case 1: return launch_fast<T, 1, 1, 2>(p, a, st);
+    case 2: return launch_fast<T, 2, 1, 2>(p, a, st);
+    case 3: return launch_fast<T, 3, 1, 1>(p, a, st);
+    default: return launch_fast<T, 4, 1, 1>(p, a, st);
   }
 }
 
-template <typename T, int KV>
+template <typename T, int KV, int RB, int MINB>
 cudaError_t set_smem(int bytes) {
   constexpr bool COMP = sizeof(T) == 4;
-  return cudaFuncSetAttribute(rms_bwd_fast_kernel<T, KV, COMP>,
+  return cudaFuncSetAttribute(rms_bwd_fast_kernel<T, KV, RB, COMP, MINB>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <typename T>
+cudaError_t set_smem_all(int bytes) {
+  cudaError_t e = cudaSuccess, r;
+  if ((r = set_smem<T, 1, 2, 2>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 1, 1, 2>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 2, 1, 2>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 3, 1, 1>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 4, 1, 1>(bytes)) != cudaSuccess) e = r;
+  return e;
 }
 
 }  // namespace
 
-uint32_t rms_smem_header() { return kRmsHeader; }
+uint32_t rms_smem_header(int rb) { return rms_header(rb); }
 
 cudaError_t rms_configure(int smem_optin) {
-  cudaError_t e = cudaSuccess;
-  cudaError_t r;
-  if ((r = set_smem<float, 1>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<float, 2>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<float, 3>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<float, 4>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<bf16, 1>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<bf16, 2>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<bf16, 3>(smem_optin)) != cudaSuccess) e = r;
-  if ((r = set_smem<bf16, 4>(smem_optin)) != cudaSuccess) e = r;
-  return e;
+  cudaError_t e1 = set_smem_all<float>(smem_optin);
+  cudaError_t e2 = set_smem_all<bf16>(smem_optin);
+  return e1 != cudaSuccess ? e1 : e2;
 }
 
 cudaError_t rms_launch(const RowPlan& p, const void* dy, const void* x, const void* w,

@@ -12,7 +12,7 @@
 
 namespace gbn {
 
-uint32_t rms_smem_header();
+uint32_t rms_smem_header(int rb);
 uint32_t ln_smem_header(int rb);
 cudaError_t rms_configure(int smem_optin);
 cudaError_t ln_configure(int smem_optin);
@@ -106,47 +106,57 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
     // LayerNorm, whose three column sums are double-fp32).
     const int64_t max_cols = (kind != GBN_ROW_RMS && dtype == GBN_F32) ? 8 : 16;
     if (kv * VE > max_cols || kv > 4 || (kind != GBN_ROW_RMS && kv > 2)) fast = false;
-    if (fast) {
-      const int rb = (kind != GBN_ROW_RMS && kv == 1) ? 2 : 1;
+    // (rows per stage, blocks per SM) in order of preference; these match
+    // the compiled kernel instances.
+    int cand[2][2];
+    int ncand = 0;
+    if (kind == GBN_ROW_RMS) {
+      cand[ncand][0] = kv == 1 ? 2 : 1;
+      cand[ncand++][1] = kv <= 2 ? 2 : 1;
+    } else if (kv == 1 && threads <= 256) {
+      cand[ncand][0] = 2, cand[ncand++][1] = 3;
+    } else if (kv == 1) {
+      cand[ncand][0] = 1, cand[ncand++][1] = 1;
+    } else {
+      cand[ncand][0] = 1, cand[ncand++][1] = 1;
+    }
+    bool placed = false;
+    for (int ci = 0; fast && ci < ncand && !placed; ++ci) {
+      const int rb = cand[ci][0], cps = cand[ci][1];
       const uint64_t rowb = (uint64_t)H * esize;
       uint32_t off = 0;
-      p->off[0] = off;  // dy
+      p->off[0] = 0;  // dy (LayerNorm) / x (RMSNorm: x rows then dy rows)
+      off = round16(rb * rowb);
+      p->off[1] = off;  // x / input (LayerNorm)
       off = round16(off + rb * rowb);
-      p->off[1] = off;  // x / input
-      off = round16(off + rb * rowb);
-      if (kind == GBN_ROW_RMS) {
-        off = 0;
-        p->off[0] = 0;
-        p->off[1] = (uint32_t)rowb;
-        off = (uint32_t)(2 * rowb);
-      } else {
-        if (fused) {
-          p->off[2] = off;  // residual
-          off = round16(off + rb * rowb);
-          if (has_mask) {
-            p->off[3] = off;  // mask
-            off = round16(off + (uint64_t)rb * H);
-          }
+      if (fused) {
+        p->off[2] = off;  // residual
+        off = round16(off + rb * rowb);
+        if (has_mask) {
+          p->off[3] = off;  // mask
+          off = round16(off + (uint64_t)rb * H);
         }
       }
-      const uint32_t header = kind == GBN_ROW_RMS ? rms_smem_header() : ln_smem_header(rb);
-      const int64_t budget = (int64_t)dev.smem_optin - header;
-      int64_t nst = off > 0 ? budget / off : 0;
+      const uint32_t header = kind == GBN_ROW_RMS ? rms_smem_header(rb) : ln_smem_header(rb);
+      int64_t per_block = (int64_t)dev.smem_per_sm / cps - dev.smem_reserved;
+      if (per_block > dev.smem_optin) per_block = dev.smem_optin;
+      int64_t nst = (per_block - header) / off;
       if (nst > kMaxStages) nst = kMaxStages;
-      if (nst < 2) {
-        fast = false;
-      } else {
-        const int64_t nblk = (R + rb - 1) / rb;
-        p->fast = true;
-        p->threads = (int)threads;
-        p->kv = (int)kv;
-        p->rb = rb;
-        p->nstage = (int)nst;
-        p->stage_bytes = off;
-        p->smem = header + (size_t)nst * off;
-        p->G = (int)(nblk < dev.sms ? nblk : dev.sms);
-      }
+      if (nst < 2) continue;
+      const int64_t nblk = (R + rb - 1) / rb;
+      const int64_t slots = (int64_t)dev.sms * cps;
+      p->fast = true;
+      p->threads = (int)threads;
+      p->kv = (int)kv;
+      p->rb = rb;
+      p->cps = cps;
+      p->nstage = (int)nst;
+      p->stage_bytes = off;
+      p->smem = header + (size_t)nst * off;
+      p->G = (int)(nblk < slots ? nblk : slots);
+      placed = true;
     }
+    if (!placed) fast = false;
   }
   if (!fast) {
     p->fast = false;

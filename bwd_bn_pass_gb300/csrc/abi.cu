@@ -85,6 +85,7 @@ const DevInfo* device_info(int device) {
   if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;
   n.status = static_cast<int*>(addr);
   if (row_kernels_configure(n.smem_optin) != cudaSuccess) return nullptr;
+  if (bn_fused_configure(n.smem_optin, &n.fused_ok) != cudaSuccess) return nullptr;
   n.ok = true;
   d = n;
   return &d;
@@ -194,6 +195,12 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
   if (rc != GBN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float2* part = static_cast<float2*>(const_cast<void*>(ws));
+  BnFusedPlan fp;
+  if (with_stats_pass && aligned(x, 16) && aligned(y, 16) &&
+      bn_fused_plan(dtype, false, B, C, HW, *dev, &fp) && ws_bytes >= fp.ws_bytes)
+    return to_status(bn_fused_forward(fp, dtype, x, y, gamma, beta, stats, running_mean,
+                                      running_var, momentum, eps, const_cast<void*>(ws),
+                                      dev->status, st));
   if (with_stats_pass) {
     cudaError_t e = bn_launch_stats(x, dtype, p, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;
@@ -258,6 +265,11 @@ static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B,
   if (rc != GBN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float2* part = static_cast<float2*>(const_cast<void*>(ws));
+  BnFusedPlan fp;
+  if (sums && finalize && aligned(x, 16) && aligned(dy, 16) && aligned(dx, 16) &&
+      bn_fused_plan(dtype, true, B, C, HW, *dev, &fp) && ws_bytes >= fp.ws_bytes)
+    return to_status(bn_fused_backward(fp, dtype, x, dy, dx, stats, grads, const_cast<void*>(ws),
+                                       dev->status, st));
   if (sums) {
     cudaError_t e = bn_launch_grad_sums(x, dy, dtype, p, stats, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;

@@ -1,0 +1,82 @@
+// Per-channel BatchNorm finalize arithmetic, shared by the two-launch kernels
+// (bn_kernels.cu) and the persistent kernel (bn_fused.cu) so that both paths
+// evaluate the same formulas in the same double-fp32 steps.
+//
+// Method: Aether-ML PR #18 "perf(batchnorm): device-sized grid, one-pass
+// statistics, finalize kernels" -- the finalize step: mean and biased
+// variance from the shifted sums, inv_std = 1/sqrt(var + eps), scale =
+// gamma*inv_std, running_mean/var momentum update with the unbiased factor
+// M/(M-1); and the backward finalize dgamma = S*inv_std, dbeta = sum dy,
+// k1 = -scale*inv_std^2*S/M, k2 = -scale*dbeta/M.
+#pragma once
+
+#include "gbn_common.cuh"
+
+namespace gbn {
+
+// (hi, lo) / M for the per-channel count M (held exactly as mh + ml).
+__device__ __forceinline__ DF div_count(DF a, float mh, float ml) {
+  const float q = a.hi / mh;
+  const DF p = two_prod(q, mh);
+  const float r = __fsub_rn(__fadd_rn(__fsub_rn(__fsub_rn(a.hi, p.hi), p.lo), a.lo), __fmul_rn(q, ml));
+  return DF{q, r / mh};
+}
+
+struct BnFwdFinal {
+  DF md;          // mean - shift
+  float var;      // biased batch variance
+  float inv_std;  // 1 / sqrt(var + eps)
+  float scale;    // gamma * inv_std
+};
+
+// From s1 = sum d and s2 = sum d^2 over the channel (d = x - shift).
+__device__ __forceinline__ BnFwdFinal bn_fwd_final(DF s1, DF s2, float mh, float ml, float gamma,
+                                                   float eps) {
+  BnFwdFinal f;
+  f.md = df_norm(div_count(s1, mh, ml));
+  const DF e2 = div_count(s2, mh, ml);  // E[(x - shift)^2]
+  float var = df_round(df_sum(e2, df_neg(df_mul_df(f.md, f.md))));
+  if (!(var > 0.f)) var = 0.f;
+  f.var = var;
+  f.inv_std = 1.f / sqrtf(var + eps);
+  f.scale = gamma * f.inv_std;
+  return f;
+}
+
+// Stats rows 0-7 of channel c (mean, var, inv_std, scale, shift, mean - shift
+// rounded, and mean - shift as a (hi, lo) pair) and the running update.
+__device__ __forceinline__ void bn_fwd_write(const BnFwdFinal& f, float shift, int64_t C, int c,
+                                             float M, float* stats, float* running_mean,
+                                             float* running_var, float momentum) {
+  const float mean = df_round(df_plus(f.md, shift));
+  stats[c] = mean;
+  stats[C + c] = f.var;
+  stats[2 * C + c] = f.inv_std;
+  stats[3 * C + c] = f.scale;
+  stats[4 * C + c] = shift;
+  stats[5 * C + c] = f.md.hi;
+  stats[6 * C + c] = f.md.hi;
+  stats[7 * C + c] = f.md.lo;
+  const float m = momentum;
+  if (running_mean) running_mean[c] = (1.f - m) * running_mean[c] + m * mean;
+  if (running_var) running_var[c] = (1.f - m) * running_var[c] + m * f.var * (M / (M - 1.f));
+}
+
+struct BnBwdFinal {
+  float dgamma, dbeta, k1, k2;
+};
+
+// From p0 = sum dy and p1 = sum dy*(x - shift); S = sum dy*(x - mean) =
+// p1 - (mean - shift)*p0 in double-fp32 with the forward's (mean - shift).
+__device__ __forceinline__ BnBwdFinal bn_bwd_final(DF p0, DF p1, DF md, float inv_std,
+                                                   float scale, float M) {
+  const float S = df_round(df_sum(p1, df_neg(df_mul_df(md, p0))));
+  BnBwdFinal f;
+  f.dbeta = df_round(p0);
+  f.k1 = -(scale * inv_std) * inv_std * S / M;
+  f.k2 = -scale * f.dbeta / M;
+  f.dgamma = S * inv_std;
+  return f;
+}
+
+}  // namespace gbn

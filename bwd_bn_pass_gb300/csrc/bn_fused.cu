@@ -1,0 +1,736 @@
+// Persistent single-launch BatchNorm2d training forward and backward (NCHW).
+//
+// Method: Aether-ML PR #18 "perf(batchnorm): device-sized grid, one-pass
+// statistics, finalize kernels" computes, per direction, a reduction pass
+// (shifted sums d = x - x[0,c] and d^2; or sum dy and sum dy*(x - shift)),
+// a finalize, and an elementwise pass (y = (x - mean)*scale + beta; or dx =
+// dy*scale + (x - mean)*k1 + k2).  This file runs the three steps in ONE
+// launch; the arithmetic is that of the two-launch kernels in bn_kernels.cu
+// (same finalize helpers, same per-element formulas).
+//
+// GB300 design:
+//   * One CTA per SM (cooperative launch, so every CTA is resident).  The
+//     tensor is viewed channel-major -- channel c's M = B*HW elements in
+//     (b, h, w) order -- and CTA k owns the contiguous range [k*W, (k+1)*W)
+//     of that view: one to a few channel segments, each a run of whole or
+//     partial planes.
+//   * Warp 0 is the producer: one lane streams the range through a ring of
+//     shared-memory stages with 1-D bulk copies (cp.async.bulk, one per plane
+//     run) completing on per-stage "full" mbarriers.  Sixteen consumer warps
+//     reduce each stage and release it on an "empty" mbarrier.
+//   * Phase 1 (reduction) walks the range forward and writes one double-fp32
+//     partial pair per (segment, channel) into partials[2][grid_y][C], slot j
+//     = k - (first CTA of the channel), then publishes a per-CTA flag.
+//   * Phase 2 waits only for the flags of the CTAs that share its channels,
+//     finalizes each channel from those partials (fixed order, so all CTAs
+//     of a channel hold identical values; the CTA holding the channel's first
+//     element writes stats / grads and the running statistics), then walks
+//     the range BACKWARD: the last ring-full of stages is still in shared
+//     memory (no reload), and the stages before it were read last, so they
+//     are the likeliest to be in L2.  Outputs are written with 16-byte stores.
+//   * Flags carry an epoch: (e+1, ~(e+1)) per CTA, with e read at kernel
+//     start from the workspace's epoch pair (or a host nonce if that pair is
+//     not self-consistent); CTA 0 advances the epoch once every CTA has
+//     published.  No memset and no atomics; a relaunch on the same workspace
+//     always waits for fresh flags.
+//   * Every wait is bounded (about one second).  On expiry the CTA records
+//     GBN_DEV_WAIT_TIMEOUT in the status word, stops issuing and computing,
+//     waits (bounded) for its own copies in flight and returns.
+#include <atomic>
+
+#include "bn_finalize.cuh"
+#include "gbn_common.cuh"
+#include "gbn_internal.h"
+
+namespace gbn {
+
+namespace {
+
+constexpr int kFConsumerWarps = 16;
+constexpr int kFConsumers = kFConsumerWarps * 32;  // 512
+constexpr int kFThreads = kFConsumers + 32;        // + the producer warp
+constexpr int kFMaxStages = 8;
+constexpr int kFMaxSegs = 32;                      // channel segments per CTA
+constexpr int kFStaticSmem = 4096;                 // bound on the static shared memory
+
+struct FArgs {
+  const void* x;
+  const void* dy;        // backward
+  void* out;             // y (forward) or dx (backward)
+  const float* gamma;    // forward, may be null (1)
+  const float* beta;     // forward, may be null (0)
+  float* stats;          // forward: written; backward: read
+  float* running_mean;   // forward, may be null
+  float* running_var;    // forward, may be null
+  float* grads;          // backward: written
+  float momentum, eps;
+  unsigned long long* sync;  // [2] epoch pair, then [G][2] flag pairs
+  float2* part;              // [2][grid_y][C]
+  int* status;
+  unsigned long long nonce;
+  int64_t C;
+  int64_t P;         // plane size in elements
+  int64_t Wv;        // vectors per CTA
+  int32_t Mv;        // vectors per channel
+  int32_t Pv;        // vectors per plane
+  int32_t stage_v;   // vectors per stage (per input)
+  int32_t nstage;
+  int32_t grid_y;
+  int32_t G;
+  int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
+  float Mh, Ml;      // per-channel count M = Mh + Ml exactly
+};
+
+// Parameters per segment: [0] shift, [1] mean - shift (rounded),
+// forward [2] scale, [3] beta; backward [2] scale, [3] k1, [4] k2.
+struct FShared {
+  uint64_t full[kFMaxStages];
+  uint64_t empty[kFMaxStages];
+  int issued[kFMaxStages];
+  unsigned long long target;  // flag value of this launch (epoch + 1)
+  int nseg;
+  int nst;                    // stages in the range
+  volatile int abort;
+  int seg_c[kFMaxSegs];
+  int seg_rv0[kFMaxSegs];     // first vector of the segment inside its channel
+  int seg_len[kFMaxSegs];     // vectors
+  int seg_klo[kFMaxSegs];     // first CTA of the channel
+  int seg_khi[kFMaxSegs];     // last CTA of the channel
+  float seg_par[kFMaxSegs][5];
+  float2 red[2][kFConsumerWarps];
+};
+static_assert(sizeof(FShared) <= kFStaticSmem, "static shared memory bound");
+
+__device__ __forceinline__ void consumers_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kFConsumers) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
+  float a, b;
+  asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(a), "=f"(b) : "l"(p) : "memory");
+  return make_float2(a, b);
+}
+
+// Flag pair of CTA k: word 0 is stored last, with release semantics.
+__device__ __forceinline__ bool flag_ready(const unsigned long long* f, unsigned long long t) {
+  return ld_acquire_u64(f) == t && ld_relaxed_u64(f + 1) == ~t;
+}
+__device__ bool wait_flag(const unsigned long long* f, unsigned long long t) {
+  if (flag_ready(f, t)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(100);
+    if (flag_ready(f, t)) return true;
+    if ((it & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// mbarrier wait that also gives up once another warp has aborted.
+__device__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void set_abort(FShared& sh, int* status) {
+  if (!sh.abort) {
+    sh.abort = 1;
+    report_status(status, GBN_DEV_WAIT_TIMEOUT);
+  }
+}
+
+// Warp-uniform stage wait: false (for every lane) if the CTA has aborted or
+// any lane's wait expired.  Every lane waits, so each observes the phase.
+__device__ __forceinline__ bool warp_wait_full(FShared& sh, int slot, uint32_t& fpar,
+                                               int* status) {
+  if (__any_sync(0xffffffffu, sh.abort != 0)) return false;
+  bool ok = wait_or_abort(&sh.full[slot], (fpar >> slot) & 1u, &sh.abort);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) {
+    if ((threadIdx.x & 31) == 0) set_abort(sh, status);
+    return false;
+  }
+  fpar ^= 1u << slot;
+  return true;
+}
+
+// Stage q of segment s: its first vector inside the channel and its length.
+__device__ __forceinline__ void stage_of(const FShared& sh, const FArgs& a, int s, int q,
+                                         int& rv0, int& len) {
+  const int off = q * a.stage_v;
+  rv0 = sh.seg_rv0[s] + off;
+  len = min(a.stage_v, sh.seg_len[s] - off);
+}
+
+__device__ __forceinline__ int stages_in(const FShared& sh, const FArgs& a, int s) {
+  return (sh.seg_len[s] + a.stage_v - 1) / a.stage_v;
+}
+
+// ------------------------------------------------------------- producer --
+
+// Bulk copies of one stage (plane runs of channel c) into `slot`.
+template <typename T, bool BWD>
+__device__ void issue_stage(const FArgs& a, FShared& sh, unsigned char* ring, int slot, int c,
+                            int rv0, int len) {
+  constexpr int VEC = 16 / sizeof(T);
+  const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
+  unsigned char* d0 = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
+  unsigned char* d1 = d0 + in_bytes;
+  uint64_t* bar = &sh.full[slot];
+  mbar_arrive_expect_tx(bar, (uint32_t)len * 16u * (BWD ? 2u : 1u));
+  int n = rv0 / a.Pv;
+  int pv = rv0 - n * a.Pv;
+  for (int off = 0; off < len;) {
+    const int run = min(a.Pv - pv, len - off);
+    const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
+    bulk_g2s(d0 + (size_t)off * 16, static_cast<const T*>(a.x) + gvo * VEC, (uint32_t)run * 16u,
+             bar);
+    if (BWD)
+      bulk_g2s(d1 + (size_t)off * 16, static_cast<const T*>(a.dy) + gvo * VEC,
+               (uint32_t)run * 16u, bar);
+    off += run;
+    pv = 0;
+    ++n;
+  }
+  sh.issued[slot] += 1;
+}
+
+template <typename T, bool BWD>
+__device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
+  const int NS = a.nstage, N1 = sh.nst;
+  uint32_t epar = 0;  // parity of the next "empty" completion per slot
+  // Phase 1: forward.  A slot is refilled once its previous stage is released.
+  int i = 0;
+  for (int s = 0; s < sh.nseg; ++s) {
+    const int nq = stages_in(sh, a, s);
+    for (int q = 0; q < nq; ++q, ++i) {
+      const int slot = i % NS;
+      if (i >= NS) {
+        if (!wait_or_abort(&sh.empty[slot], (epar >> slot) & 1u, &sh.abort)) {
+          set_abort(sh, a.status);
+          return;
+        }
+        epar ^= 1u << slot;
+        fence_proxy_async_smem();
+      }
+      if (sh.abort) return;
+      int rv0, len;
+      stage_of(sh, a, s, q, rv0, len);
+      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len);
+    }
+  }
+  // Phase 2: backward; the last NS stages are still resident.
+  int q2 = 0;
+  for (int s = sh.nseg - 1; s >= 0; --s) {
+    const int nq = stages_in(sh, a, s);
+    for (int q = nq - 1; q >= 0; --q, ++q2) {
+      if (q2 < NS) continue;
+      const int slot = (N1 - 1 - q2) % NS;
+      if (!wait_or_abort(&sh.empty[slot], (epar >> slot) & 1u, &sh.abort)) {
+        set_abort(sh, a.status);
+        return;
+      }
+      epar ^= 1u << slot;
+      fence_proxy_async_smem();
+      if (sh.abort) return;
+      int rv0, len;
+      stage_of(sh, a, s, q, rv0, len);
+      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len);
+    }
+  }
+}
+
+// ------------------------------------------------------------ consumers --
+
+// Phase-1 accumulation of one 16-byte vector.  Forward: sum d and sum d^2
+// (d = x - shift) over the vector's lanes in fp32, then one double-fp32 add
+// per vector (as in the two-launch stats kernel).  Backward: sum dy and
+// sum dy*d per element in double-fp32 with each product's exact residual and,
+// for fp32 input, the rounding error of x - shift.
+template <typename T>
+__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, DF2& a1, DF2& a2) {
+  constexpr int NP = Pairs16<T>::NP;
+  f2 p[NP];
+  Pairs16<T>::get(r, p);
+  f2 l1 = 0ull, l2 = 0ull;
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const f2 d = f2_sub(p[k], sh2);
+    l1 = f2_add(l1, d);
+    l2 = f2_fma(d, d, l2);
+  }
+  df2_add(a1, l1);
+  df2_add(a2, l2);
+}
+
+template <typename T>
+__device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, DF2& a0, DF2& a1) {
+  constexpr int NP = Pairs16<T>::NP;
+  f2 px[NP], pd[NP];
+  Pairs16<T>::get(rx, px);
+  Pairs16<T>::get(rd, pd);
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const f2 d = f2_sub(px[k], sh2);
+    df2_add(a0, pd[k]);
+    const f2 prod = f2_mul_rounded(pd[k], d);
+    df2_add(a1, prod);
+    // exact residual dy*d - prod (the negation flips the sign of both lanes)
+    a1.lo = f2_add(a1.lo, f2_fma(pd[k], d, prod ^ 0x8000000080000000ull));
+    if constexpr (sizeof(T) == 4) {
+      const f2 bb = f2_sub(d, px[k]);
+      const f2 d_lo = f2_add(f2_sub(px[k], f2_sub(d, bb)), f2_sub(nsh2, bb));
+      a1.lo = f2_fma(pd[k], d_lo, a1.lo);
+    }
+  }
+}
+
+// Sum two (hi, lo) pairs over the consumer warps in a fixed tree; the result
+// is valid in consumer warp 0.  Contains two consumer barriers.
+__device__ __forceinline__ void consumers_sum2(FShared& sh, DF& a, DF& b) {
+  const int ct = threadIdx.x - 32, lane = ct & 31, cw = ct >> 5;
+  a = warp_sum_df(a);
+  b = warp_sum_df(b);
+  if (lane == 0) {
+    sh.red[0][cw] = make_float2(a.hi, a.lo);
+    sh.red[1][cw] = make_float2(b.hi, b.lo);
+  }
+  __syncwarp();
+  consumers_sync();
+  if (cw == 0) {
+    const float2 u = lane < kFConsumerWarps ? sh.red[0][lane] : make_float2(0.f, 0.f);
+    const float2 w = lane < kFConsumerWarps ? sh.red[1][lane] : make_float2(0.f, 0.f);
+    a = warp_sum_df(DF{u.x, u.y});
+    b = warp_sum_df(DF{w.x, w.y});
+  }
+  __syncwarp();
+  consumers_sync();
+}
+
+template <typename T, bool BWD>
+__device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char* ring,
+                                uint32_t& fpar) {
+  const int ct = threadIdx.x - 32, lane = ct & 31;
+  const int NS = a.nstage, N1 = sh.nst;
+  const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
+  int i = 0;
+  for (int s = 0; s < sh.nseg; ++s) {
+    const float shift = sh.seg_par[s][0];
+    const f2 sh2 = f2_splat(shift), nsh2 = f2_splat(-shift);
+    DF2 a0{0ull, 0ull}, a1{0ull, 0ull};
+    const int nq = stages_in(sh, a, s);
+    for (int q = 0; q < nq; ++q, ++i) {
+      const int slot = i % NS;
+      if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
+      int rv0, len;
+      stage_of(sh, a, s, q, rv0, len);
+      const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
+      if constexpr (!BWD) {
+        for (int v = ct; v < len; v += kFConsumers)
+          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, a0, a1);
+      } else {
+        for (int v = ct; v < len; v += kFConsumers)
+          bwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
+                     *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2, nsh2,
+                     a0, a1);
+      }
+      // Release the slot only if phase 1 refills it; the last NS stages stay
+      // resident for phase 2.
+      if (i + NS < N1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      }
+    }
+    DF s0 = df2_fold(a0), s1 = df2_fold(a1);
+    consumers_sum2(sh, s0, s1);
+    if (ct == 0 && !sh.abort) {
+      const int j = (int)blockIdx.x - sh.seg_klo[s];
+      const int c = sh.seg_c[s];
+      a.part[(int64_t)j * a.C + c] = make_float2(s0.hi, s0.lo);
+      a.part[((int64_t)a.grid_y + j) * a.C + c] = make_float2(s1.hi, s1.lo);
+    }
+    __syncwarp();
+  }
+  // Publish: every partial of this CTA was written by this thread above.
+  if (ct == 0 && !sh.abort) {
+    unsigned long long* f = a.sync + 2 + 2 * (int64_t)blockIdx.x;
+    __threadfence();
+    st_relaxed_u64(f + 1, ~sh.target);
+    st_release_u64(f, sh.target);
+  }
+  __syncwarp();
+}
+
+// Channel finalize for segment s by one consumer warp.
+template <bool BWD>
+__device__ void finalize_segment(const FArgs& a, FShared& sh, int s) {
+  const int lane = (threadIdx.x - 32) & 31;
+  const int c = sh.seg_c[s], klo = sh.seg_klo[s], n = sh.seg_khi[s] - klo + 1;
+  DF p0{0.f, 0.f}, p1{0.f, 0.f};
+  bool ok = true;
+  for (int jj = lane; jj < n; jj += 32) {
+    // Slot jj was written by CTA klo + jj; this lane acquires that CTA's flag
+    // and then reads the slot itself.
+    ok = ok && wait_flag(a.sync + 2 + 2 * (int64_t)(klo + jj), sh.target);
+    if (ok) {
+      const float2 u = ld_relaxed_f2(a.part + (int64_t)jj * a.C + c);
+      const float2 w = ld_relaxed_f2(a.part + ((int64_t)a.grid_y + jj) * a.C + c);
+      p0 = df_sum(p0, DF{u.x, u.y});
+      p1 = df_sum(p1, DF{w.x, w.y});
+    }
+  }
+  if (!__all_sync(0xffffffffu, ok)) {
+    if (lane == 0) set_abort(sh, a.status);
+    return;
+  }
+  p0 = warp_sum_df(p0);
+  p1 = warp_sum_df(p1);
+  const bool owner = (klo == (int)blockIdx.x);  // holds the channel's first element
+  const float M = a.Mh + a.Ml;
+  if constexpr (!BWD) {
+    const BnFwdFinal f = bn_fwd_final(p0, p1, a.Mh, a.Ml, a.gamma ? a.gamma[c] : 1.f, a.eps);
+    if (lane == 0) {
+      sh.seg_par[s][1] = f.md.hi;
+      sh.seg_par[s][2] = f.scale;
+      sh.seg_par[s][3] = a.beta ? a.beta[c] : 0.f;
+      if (owner)
+        bn_fwd_write(f, sh.seg_par[s][0], a.C, c, M, a.stats, a.running_mean, a.running_var,
+                     a.momentum);
+    }
+  } else {
+    const int64_t C = a.C;
+    const DF md{a.stats[6 * C + c], a.stats[7 * C + c]};
+    const BnBwdFinal f = bn_bwd_final(p0, p1, md, a.stats[2 * C + c], sh.seg_par[s][2], M);
+    if (lane == 0) {
+      sh.seg_par[s][3] = f.k1;
+      sh.seg_par[s][4] = f.k2;
+      if (owner) {
+        a.grads[c] = f.dgamma;
+        a.grads[C + c] = f.dbeta;
+        a.grads[2 * C + c] = f.k1;
+        a.grads[3 * C + c] = f.k2;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <typename T, bool BWD>
+__device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char* ring,
+                                uint32_t& fpar) {
+  constexpr int VEC = 16 / sizeof(T);
+  using V = Vec<T, VEC>;
+  const int ct = threadIdx.x - 32, lane = ct & 31, cw = ct >> 5;
+  const int NS = a.nstage, N1 = sh.nst;
+  const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
+  for (int s = cw; s < sh.nseg; s += kFConsumerWarps)
+    if (!__any_sync(0xffffffffu, sh.abort != 0)) finalize_segment<BWD>(a, sh, s);
+  __syncwarp();
+  consumers_sync();
+  T* out = static_cast<T*>(a.out);
+  int q2 = 0;
+  for (int s = sh.nseg - 1; s >= 0; --s) {
+    const int c = sh.seg_c[s];
+    const float shift = sh.seg_par[s][0], mean_d = sh.seg_par[s][1], scale = sh.seg_par[s][2];
+    const float p3 = sh.seg_par[s][3], p4 = sh.seg_par[s][4];
+    const int nq = stages_in(sh, a, s);
+    for (int q = nq - 1; q >= 0; --q, ++q2) {
+      const int slot = (N1 - 1 - q2) % NS;
+      if (q2 >= NS) {
+        if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
+      } else if (__any_sync(0xffffffffu, sh.abort != 0)) {
+        continue;
+      }
+      int rv0, len;
+      stage_of(sh, a, s, q, rv0, len);
+      const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
+      // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv.
+      const int rv = rv0 + ct;
+      int n = rv / a.Pv;
+      int pv = rv - n * a.Pv;
+      for (int v = ct; v < len; v += kFConsumers) {
+        const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
+        float e[VEC];
+        V::cvt(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), e);
+        if constexpr (!BWD) {
+#pragma unroll
+          for (int k = 0; k < VEC; ++k) e[k] = fmaf((e[k] - shift) - mean_d, scale, p3);
+        } else {
+          float g[VEC];
+          V::cvt(*reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), g);
+#pragma unroll
+          for (int k = 0; k < VEC; ++k) {
+            const float xc = (e[k] - shift) - mean_d;
+            e[k] = fmaf(g[k], scale, fmaf(xc, p3, p4));
+          }
+        }
+        V::store(out + gvo * VEC, e);
+        pv += a.dp;
+        n += a.dn;
+        if (pv >= a.Pv) {
+          pv -= a.Pv;
+          ++n;
+        }
+      }
+      if (q2 + NS < N1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      }
+    }
+  }
+}
+
+template <typename T, bool BWD>
+__global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
+  extern __shared__ __align__(128) unsigned char ring[];
+  __shared__ FShared sh;
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    for (int s = 0; s < a.nstage; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], kFConsumerWarps);
+      sh.issued[s] = 0;
+    }
+    sh.abort = 0;
+    const unsigned long long ea = ld_relaxed_u64(a.sync), eb = ld_relaxed_u64(a.sync + 1);
+    sh.target = (eb == ~ea ? ea : a.nonce) + 1ull;
+    // Segments of this CTA's range [k*Wv, (k+1)*Wv) of the channel-major view.
+    const int64_t e0 = (int64_t)blockIdx.x * a.Wv;
+    const int64_t e1 = min(e0 + a.Wv, a.C * (int64_t)a.Mv);
+    int ns = 0, nst = 0;
+    for (int64_t e = e0; e < e1 && ns < kFMaxSegs;) {
+      const int64_t c = e / a.Mv;
+      const int64_t cend = min((c + 1) * (int64_t)a.Mv, e1);
+      sh.seg_c[ns] = (int)c;
+      sh.seg_rv0[ns] = (int)(e - c * a.Mv);
+      sh.seg_len[ns] = (int)(cend - e);
+      sh.seg_klo[ns] = (int)((c * a.Mv) / a.Wv);
+      sh.seg_khi[ns] = (int)(((c + 1) * a.Mv - 1) / a.Wv);
+      if constexpr (!BWD) {
+        // x[0, c, 0, 0], read before any output of this launch is written.
+        sh.seg_par[ns][0] = to_f32(static_cast<const T*>(a.x)[c * a.P]);
+        sh.seg_par[ns][4] = 0.f;
+      } else {
+        sh.seg_par[ns][0] = a.stats[4 * a.C + c];
+        sh.seg_par[ns][1] = a.stats[5 * a.C + c];
+        sh.seg_par[ns][2] = a.stats[3 * a.C + c];
+      }
+      nst += (sh.seg_len[ns] + a.stage_v - 1) / a.stage_v;
+      ++ns;
+      e = cend;
+    }
+    sh.nseg = ns;
+    sh.nst = nst;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  if (tid < 32) {
+    if (tid == 0) producer<T, BWD>(a, sh, ring);
+    __syncwarp();
+  } else {
+    uint32_t fpar = 0;
+    consumer_phase1<T, BWD>(a, sh, ring, fpar);
+    consumer_phase2<T, BWD>(a, sh, ring, fpar);
+  }
+  __syncthreads();
+
+  if (tid == 0) {
+    // Let every copy this CTA issued land before the CTA exits.
+    for (int s = 0; s < a.nstage; ++s)
+      if (sh.issued[s] > 0 &&
+          !mbar_wait_bounded(&sh.full[s], (uint32_t)(sh.issued[s] - 1) & 1u))
+        report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
+    // CTA 0 advances the epoch once every CTA has published (so every CTA
+    // has read the old one); after a failure it skips one epoch so that no
+    // flag of this launch can match the next launch's target.
+    if (blockIdx.x == 0) {
+      bool all = !sh.abort;
+      for (int k = 0; k < a.G && all; ++k) all = wait_flag(a.sync + 2 + 2 * (int64_t)k, sh.target);
+      if (!all) report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
+      const unsigned long long next = all ? sh.target : sh.target + 1ull;
+      st_relaxed_u64(a.sync + 1, ~next);
+      st_relaxed_u64(a.sync, next);
+    }
+  }
+}
+
+template <typename T, bool BWD>
+cudaError_t launch_fused(const FArgs& a, const BnFusedPlan& p, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.G, 1, 1);
+  cfg.blockDim = dim3(kFThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bn_fused_kernel<T, BWD>, a);
+}
+
+std::atomic<unsigned long long> g_nonce{0};
+
+// A fresh 64-bit value per call (splitmix64 of a process counter): the flag
+// epoch used when the workspace holds no valid epoch pair.
+unsigned long long next_nonce() {
+  unsigned long long z = g_nonce.fetch_add(0x9e3779b97f4a7c15ull) + 0x9e3779b97f4a7c15ull;
+  z ^= reinterpret_cast<uintptr_t>(&g_nonce);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
+
+FArgs make_args(const BnFusedPlan& p, void* ws) {
+  FArgs a = {};
+  a.sync = static_cast<unsigned long long*>(ws);
+  a.part = reinterpret_cast<float2*>(static_cast<unsigned char*>(ws) + p.part_offset);
+  a.nonce = next_nonce();
+  a.C = p.C;
+  a.P = p.P;
+  a.Wv = p.Wv;
+  a.Mv = (int32_t)p.Mv;
+  a.Pv = (int32_t)p.Pv;
+  a.stage_v = p.stage_v;
+  a.nstage = p.nstage;
+  a.grid_y = p.grid_y;
+  a.G = p.G;
+  a.dn = (int32_t)(kFConsumers / p.Pv);
+  a.dp = (int32_t)(kFConsumers % p.Pv);
+  a.Mh = (float)p.M;
+  a.Ml = (float)(p.M - (int64_t)a.Mh);
+  return a;
+}
+
+}  // namespace
+
+bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
+                   const DevInfo& dev, BnFusedPlan* p) {
+  *p = BnFusedPlan();
+  const int esize = dtype == GBN_F32 ? 4 : 2;
+  const int64_t vec = 16 / esize;
+  if (!dev.fused_ok || B <= 0 || C <= 0 || HW <= 0 || HW % vec != 0) return false;
+  p->B = B;
+  p->C = C;
+  p->P = HW;
+  p->M = B * HW;
+  p->Pv = HW / vec;
+  p->Mv = p->M / vec;
+  const int64_t Ev = C * p->Mv;
+  // One CTA per SM, each with at least kBnFusedMinVectors vectors.
+  int64_t G = (Ev + kBnFusedMinVectors - 1) / kBnFusedMinVectors;
+  if (G > dev.sms) G = dev.sms;
+  if (G < 1) G = 1;
+  p->Wv = (Ev + G - 1) / G;
+  p->G = (int)((Ev + p->Wv - 1) / p->Wv);
+  // Segments per CTA: at most ceil(Wv / Mv) + 1.
+  if ((p->Wv + p->Mv - 1) / p->Mv + 1 > kFMaxSegs) return false;
+  // CTAs per channel (partial slots): the largest over channels.
+  int64_t gy = 1;
+  for (int64_t c = 0; c < C; ++c) {
+    const int64_t klo = (c * p->Mv) / p->Wv, khi = ((c + 1) * p->Mv - 1) / p->Wv;
+    if (khi - klo + 1 > gy) gy = khi - klo + 1;
+    if (c >= 4096) {  // a safe bound for the remaining channels
+      gy = (p->Mv + p->Wv - 1) / p->Wv + 1;
+      break;
+    }
+  }
+  p->grid_y = (int)gy;
+  // Ring: kBnFusedStages stages of whole 16-byte vectors (x and, backward, dy),
+  // each a multiple of the consumer count.
+  const int ninputs = backward ? 2 : 1;
+  const int64_t budget = (int64_t)dev.smem_optin - kFStaticSmem;
+  int64_t stage_v = budget / ((int64_t)kBnFusedStages * ninputs * 16);
+  stage_v = stage_v / kFConsumers * kFConsumers;
+  if (stage_v < kFConsumers) return false;
+  p->stage_v = (int)stage_v;
+  p->nstage = kBnFusedStages;
+  p->smem = (size_t)kBnFusedStages * ninputs * (size_t)stage_v * 16;
+  p->part_offset = ((size_t)16 + (size_t)16 * p->G + 255) & ~(size_t)255;
+  p->ws_bytes = p->part_offset + (size_t)2 * p->grid_y * C * sizeof(float2);
+  p->ws_bytes = (p->ws_bytes + 255) & ~(size_t)255;
+  p->ok = true;
+  return true;
+}
+
+cudaError_t bn_fused_forward(const BnFusedPlan& p, int dtype, const void* x, void* y,
+                             const float* gamma, const float* beta, float* stats,
+                             float* running_mean, float* running_var, float momentum, float eps,
+                             void* ws, int* status, cudaStream_t st) {
+  FArgs a = make_args(p, ws);
+  a.x = x;
+  a.out = y;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.stats = stats;
+  a.running_mean = running_mean;
+  a.running_var = running_var;
+  a.momentum = momentum;
+  a.eps = eps;
+  a.status = status;
+  return dtype == GBN_F32 ? launch_fused<float, false>(a, p, st)
+                          : launch_fused<bf16, false>(a, p, st);
+}
+
+cudaError_t bn_fused_backward(const BnFusedPlan& p, int dtype, const void* x, const void* dy,
+                              void* dx, const float* stats, float* grads, void* ws, int* status,
+                              cudaStream_t st) {
+  FArgs a = make_args(p, ws);
+  a.x = x;
+  a.dy = dy;
+  a.out = dx;
+  a.stats = const_cast<float*>(stats);
+  a.grads = grads;
+  a.status = status;
+  return dtype == GBN_F32 ? launch_fused<float, true>(a, p, st)
+                          : launch_fused<bf16, true>(a, p, st);
+}
+
+cudaError_t bn_fused_configure(int smem_optin, bool* ok) {
+  *ok = false;
+  const int dyn = smem_optin - kFStaticSmem;
+  if (dyn <= 0) return cudaSuccess;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(bn_fused_kernel<float, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bn_fused_kernel<float, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bn_fused_kernel<bf16, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(bn_fused_kernel<bf16, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, dyn)) != cudaSuccess)
+    return e;
+  // The launch needs one resident CTA per SM with the full ring.
+  int blocks = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, bn_fused_kernel<bf16, true>,
+                                                    kFThreads, (size_t)dyn);
+  if (e != cudaSuccess) return e;
+  *ok = blocks >= 1;
+  return cudaSuccess;
+}
+
+}  // namespace gbn

@@ -21,13 +21,15 @@
 //     values), and block j = 0 writes stats/grads and the running update.
 //     The consumer is launched with programmatic dependent launch: it loads
 //     its first vectors of x (and dy) before griddepcontrol.wait.
-//   * Partials are fp64.  Per thread, sums are double-fp32 (TwoSum); the
-//     backward also keeps each product's FMA residual and, for fp32 inputs,
-//     the rounding error of x - shift, so sum dy*(x - mean) is accurate even
-//     when it nearly cancels.  The backward forms S = sum dy*(x - shift) -
-//     (mean - shift)*sum dy in fp64 from the forward's fp64 (mean - shift).
+//   * Partials are double-fp32 (hi, lo) pairs.  Per thread, sums are
+//     double-fp32 (TwoSum); the backward also keeps each product's FMA
+//     residual and, for fp32 inputs, the rounding error of x - shift, so
+//     sum dy*(x - mean) is accurate even when it nearly cancels.  The
+//     backward forms S = sum dy*(x - shift) - (mean - shift)*sum dy in
+//     double-fp32 from the forward's (mean - shift) pair.
 //   * The consumer walks its slice in reverse, so the tail that the producer
 //     read last (still in L2) is read first.
+#include "bn_finalize.cuh"
 #include "gbn_common.cuh"
 #include "gbn_internal.h"
 
@@ -102,14 +104,6 @@ __device__ __forceinline__ void reduce_partials(const float2* part, const BnGeom
   s1 = warp_sum_df(b);
 }
 
-// (hi, lo) / M for the per-channel count M (held exactly as mh + ml).
-__device__ __forceinline__ DF div_count(DF a, float mh, float ml) {
-  const float q = a.hi / mh;
-  const DF p = two_prod(q, mh);
-  const float r = __fsub_rn(__fadd_rn(__fsub_rn(__fsub_rn(a.hi, p.hi), p.lo), a.lo), __fmul_rn(q, ml));
-  return DF{q, r / mh};
-}
-
 template <typename T>
 __device__ __forceinline__ void x_minus_shift(float e, float shift, float& d, float& d_lo) {
   d = __fsub_rn(e, shift);
@@ -118,7 +112,10 @@ __device__ __forceinline__ void x_minus_shift(float e, float shift, float& d, fl
     const float bb = __fsub_rn(d, e);
     d_lo = __fadd_rn(__fsub_rn(e, __fsub_rn(d, bb)), __fsub_rn(-shift, bb));
   } else {
-    d_lo = 0.f;  // bf16 operands: the fp32 difference is exact
+    // bf16 operands: the fp32 difference is exact unless x and shift differ
+    // in magnitude by more than 2^16; then d carries one fp32 rounding, a
+    // per-term relative error of 2^-24 that does not grow with the sum.
+    d_lo = 0.f;
   }
 }
 
@@ -231,31 +228,13 @@ __device__ __noinline__ void apply_prologue(const BnGeom& g, const ApplyArgs& a,
   if (a.mode == kApplyTrain) {
     DF s1, s2;
     reduce_partials(a.part, g, c, s1, s2);
-    const DF md = df_norm(div_count(s1, g.Mh, g.Ml));       // mean - shift
-    const DF e2 = div_count(s2, g.Mh, g.Ml);                // E[(x - shift)^2]
-    float var = df_round(df_sum(e2, df_neg(df_mul_df(md, md))));
-    if (!(var > 0.f)) var = 0.f;
-    const float inv_std = 1.f / sqrtf(var + a.eps);
+    const BnFwdFinal f = bn_fwd_final(s1, s2, g.Mh, g.Ml, a.gamma ? a.gamma[c] : 1.f, a.eps);
     shift = shift_x;
-    mean_d = md.hi;
-    scale = (a.gamma ? a.gamma[c] : 1.f) * inv_std;
-    if (j == 0 && threadIdx.x == 0) {
-      const int64_t C = g.C;
-      const float mean = df_round(df_plus(md, shift));
-      const float M = g.Mh + g.Ml;
-      a.stats[c] = mean;
-      a.stats[C + c] = var;
-      a.stats[2 * C + c] = inv_std;
-      a.stats[3 * C + c] = scale;
-      a.stats[4 * C + c] = shift;
-      a.stats[5 * C + c] = md.hi;
-      a.stats[6 * C + c] = md.hi;
-      a.stats[7 * C + c] = md.lo;
-      const float m = a.momentum;
-      if (a.running_mean) a.running_mean[c] = (1.f - m) * a.running_mean[c] + m * mean;
-      if (a.running_var)
-        a.running_var[c] = (1.f - m) * a.running_var[c] + m * var * (M / (M - 1.f));
-    }
+    mean_d = f.md.hi;
+    scale = f.scale;
+    if (j == 0 && threadIdx.x == 0)
+      bn_fwd_write(f, shift, g.C, c, g.Mh + g.Ml, a.stats, a.running_mean, a.running_var,
+                   a.momentum);
   } else if (a.mode == kApplyStats) {
     const int64_t C = g.C;
     shift = a.stats[4 * C + c];
@@ -426,14 +405,11 @@ __device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
   const float inv_std = stats[2 * C + c];
   const float scale = stats[3 * C + c];
   const DF md{stats[6 * C + c], stats[7 * C + c]};
-  const float S = df_round(df_sum(p1, df_neg(df_mul_df(md, p0))));
-  const float dbeta = df_round(p0);
-  const float M = g.Mh + g.Ml;
-  const float k1 = -(scale * inv_std) * inv_std * S / M;
-  const float k2 = -scale * dbeta / M;
+  const BnBwdFinal f = bn_bwd_final(p0, p1, md, inv_std, scale, g.Mh + g.Ml);
+  const float k1 = f.k1, k2 = f.k2;
   if (j == 0 && threadIdx.x == 0) {
-    grads[c] = S * inv_std;
-    grads[C + c] = dbeta;
+    grads[c] = f.dgamma;
+    grads[C + c] = f.dbeta;
     grads[2 * C + c] = k1;
     grads[3 * C + c] = k2;
   }
@@ -597,6 +573,11 @@ bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan)
   plan->grid_y = (int)gy;
   const size_t bytes = (size_t)2 * (size_t)gy * (size_t)(C > 0 ? C : 1) * sizeof(float2);
   plan->ws_bytes = (bytes + 255) & ~(size_t)255;
+  // The same workspace also serves the persistent path of either dtype.
+  BnFusedPlan fp;
+  for (int dtype : {GBN_F32, GBN_BF16})
+    if (bn_fused_plan(dtype, false, B, C, HW, dev, &fp) && fp.ws_bytes > plan->ws_bytes)
+      plan->ws_bytes = fp.ws_bytes;
   return true;
 }
 

@@ -17,6 +17,7 @@ struct DevInfo {
   int smem_per_sm = 0;       // shared memory per SM (bytes)
   int smem_reserved = 0;     // shared memory the runtime reserves per block
   int* status = nullptr;     // device address of the library status word
+  bool fused_ok = false;     // the persistent BatchNorm kernel fits one CTA per SM
   bool ok = false;
 };
 
@@ -80,6 +81,39 @@ cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const 
 cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
                          const float* stats, const float2* part, float* grads, cudaStream_t st,
                          bool pdl);
+
+// Persistent single-launch BatchNorm (bn_fused.cu): one CTA per SM owns a
+// contiguous range of the channel-major view; see that file.
+constexpr int64_t kBnFusedMinVectors = 2048;  // 16-byte vectors per CTA, at least
+constexpr int kBnFusedStages = 4;             // shared-memory ring depth
+
+struct BnFusedPlan {
+  bool ok = false;
+  int64_t B = 0, C = 0, P = 0, M = 0;
+  int64_t Pv = 0, Mv = 0;  // 16-byte vectors per plane / per channel
+  int64_t Wv = 0;          // vectors per CTA
+  int G = 0;               // CTAs
+  int grid_y = 0;          // partial slots per channel
+  int stage_v = 0;         // vectors per stage and input
+  int nstage = 0;
+  size_t smem = 0;         // dynamic shared memory (the ring)
+  size_t part_offset = 0;  // partials offset in the workspace (sync words first)
+  size_t ws_bytes = 0;
+};
+
+// False when the shape or device does not take the persistent path (plane
+// not a whole number of 16-byte vectors, too many channels per CTA, ...).
+bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
+                   const DevInfo& dev, BnFusedPlan* plan);
+cudaError_t bn_fused_forward(const BnFusedPlan& p, int dtype, const void* x, void* y,
+                             const float* gamma, const float* beta, float* stats,
+                             float* running_mean, float* running_var, float momentum, float eps,
+                             void* ws, int* status, cudaStream_t st);
+cudaError_t bn_fused_backward(const BnFusedPlan& p, int dtype, const void* x, const void* dy,
+                              void* dx, const float* stats, float* grads, void* ws, int* status,
+                              cudaStream_t st);
+// Shared-memory limits and the one-CTA-per-SM check (called from device_info).
+cudaError_t bn_fused_configure(int smem_optin, bool* ok);
 
 // ------------------------------------------------------------ row-wise --
 

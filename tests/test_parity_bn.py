@@ -189,26 +189,43 @@ def test_bn_misaligned_views(gbn):
     tol.check_f32(stats[C:2 * C], ref["var"], "misaligned var")
 
 
-def test_bn_phase_entry_points_match_composite(gbn):
-    inp = synth.bn_inputs(synth.CASES["bn_offset_f32"])
+def _run_phases(gbn, inp):
     x, dy = inp["x"].to(DEV), inp["dy"].to(DEV)
     g, b = inp["gamma"].to(DEV), inp["beta"].to(DEV)
-    rm1, rv1 = inp["running_mean"].to(DEV), inp["running_var"].to(DEV)
-    rm2, rv2 = rm1.clone(), rv1.clone()
-    y1, s1 = gbn.bn_forward_train(x, g, b, rm1, rv1, 0.1, 1e-5)
-    dx1, g1 = gbn.bn_backward(x, dy, s1)
+    rm, rv = inp["running_mean"].to(DEV), inp["running_var"].to(DEV)
     ws = gbn.bn_workspace(x)
-    y2 = torch.empty_like(x)
-    s2 = gbn.bn_stats_tensor(x.shape[1], x.device)
+    y = torch.empty_like(x)
+    stats = gbn.bn_stats_tensor(x.shape[1], x.device)
     gbn.bn_stats(x, ws)
-    gbn.bn_finalize_apply(x, g, b, rm2, rv2, 0.1, 1e-5, y2, s2, ws)
-    dx2 = torch.empty_like(x)
-    g2 = torch.empty_like(g1)
-    gbn.bn_grad_sums(x, dy, s2, ws)
-    gbn.bn_finalize_dx(x, dy, s2, dx2, g2, ws)
+    gbn.bn_finalize_apply(x, g, b, rm, rv, inp["momentum"], inp["eps"], y, stats, ws)
+    dx = torch.empty_like(x)
+    grads = torch.empty(4 * x.shape[1], dtype=torch.float32, device=DEV)
+    gbn.bn_grad_sums(x, dy, stats, ws)
+    gbn.bn_finalize_dx(x, dy, stats, dx, grads, ws)
     torch.cuda.synchronize()
-    for a, c in ((y1, y2), (s1, s2), (dx1, dx2), (g1, g2), (rm1, rm2), (rv1, rv2)):
-        assert torch.equal(a, c)
+    C = x.shape[1]
+    s, gr = stats.cpu(), grads.cpu()
+    return {"y": y.cpu(), "dx": dx.cpu(), "mean": s[:C], "var": s[C:2 * C],
+            "inv_std": s[2 * C:3 * C], "scale": s[3 * C:4 * C], "running_mean": rm.cpu(),
+            "running_var": rv.cpu(), "dgamma": gr[:C], "dbeta": gr[C:2 * C],
+            "k1": gr[2 * C:3 * C], "k2": gr[3 * C:]}
+
+
+@pytest.mark.parametrize("name", ["bn_offset_f32", "bn_ragged_f32"])
+def test_bn_phase_entry_points(gbn, name):
+    """The four phase entry points chained by hand (the two-launch kernels)
+    match the oracle and are bit-deterministic.  The composite calls may take
+    the single-launch persistent kernel, whose per-CTA split of the channel
+    sums differs, so the two paths agree within the parity tolerance (each is
+    checked against the oracle) rather than bit for bit."""
+    case = synth.CASES[name]
+    inp = synth.bn_inputs(case)
+    a = _run_phases(gbn, inp)
+    compare(a, run_oracle(inp), case.dtype, what=f"{name} phases")
+    b = _run_phases(gbn, inp)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    compare(run_gpu(gbn, inp), run_oracle(inp), case.dtype, what=f"{name} composite")
 
 
 def test_bn_apply_modes(gbn):

@@ -12,8 +12,9 @@ One step = one pass of every hot-path operation over its workload:
 
 Every call goes through the C ABI (ctypes binding).  Each operation is timed
 with CUDA events on the stream it runs on, after an L2 flush (a 256 MB write
-then a 256 MB read of another buffer, outside the events); BatchNorm phases (stats | finalize+apply, grad_sums
-| finalize+dx) are timed separately.  value = unique bytes of every input and
+then a 256 MB read of another buffer, outside the events).  BatchNorm runs
+through the composite calls (bn_forward_train, bn_backward), one launch each.
+value = unique bytes of every input and
 output tensor of the step / summed device time (the effective-bandwidth
 convention), in GB/s, over all ranks.
 
@@ -195,29 +196,28 @@ def build_ops(names, dev):
             small = _nbytes(g, b, rm, rv) + 4 * C * 4
             shape = "x".join(map(str, case.shape))
             if name.endswith("fwd"):
+                # the composite call a user makes: statistics, finalize and apply
                 phases = [
-                    ("bn_stats", lambda x=x, ws=ws: G.bn_stats(x, ws)),
-                    ("bn_finalize_apply",
+                    ("bn_forward_train",
                      lambda x=x, g=g, b=b, rm=rm, rv=rv, y=y, stats=stats, ws=ws, c=case:
-                     G.bn_finalize_apply(x, g, b, rm, rv, c.momentum, c.eps, y, stats, ws)),
+                     G.bn_forward_train(x, g, b, rm, rv, c.momentum, c.eps, y=y, stats=stats,
+                                        ws=ws)),
                 ]
                 hy = torch.empty_like(hx).pin_memory()
                 ops.append(Op(name, f"BatchNorm2d fwd {case.dtype} [{shape}]", phases,
-                              2 * T + small, {"bn_stats": T, "bn_finalize_apply": 2 * T}, 2,
+                              2 * T + small, {"bn_forward_train": 2 * T + small}, 1,
                               [(hx, x)], [(y, hy)], None))
             else:
                 dx = torch.empty_like(x)
                 grads = torch.empty(4 * C, dtype=torch.float32, device=dev)
                 phases = [
-                    ("bn_grad_sums", lambda x=x, dy=dy, s=stats, ws=ws:
-                     G.bn_grad_sums(x, dy, s, ws)),
-                    ("bn_finalize_dx", lambda x=x, dy=dy, s=stats, dx=dx, gr=grads, ws=ws:
-                     G.bn_finalize_dx(x, dy, s, dx, gr, ws)),
+                    ("bn_backward", lambda x=x, dy=dy, s=stats, dx=dx, gr=grads, ws=ws:
+                     G.bn_backward(x, dy, s, dx=dx, grads=gr, ws=ws)),
                 ]
                 hdx = torch.empty_like(hx).pin_memory()
+                ub = 3 * T + 8 * C * 4 + 4 * C * 4
                 ops.append(Op(name, f"BatchNorm2d bwd {case.dtype} [{shape}]", phases,
-                              3 * T + 8 * C * 4 + 4 * C * 4,
-                              {"bn_grad_sums": 2 * T, "bn_finalize_dx": 3 * T}, 2,
+                              ub, {"bn_backward": ub}, 1,
                               [(hx, x), (hdy, dy)], [(dx, hdx)], None))
         elif name.startswith("rms_"):
             case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]

@@ -14,10 +14,11 @@
 //     (b, h, w) order -- and CTA k owns the contiguous range [k*W, (k+1)*W)
 //     of that view: one to a few channel segments, each a run of whole or
 //     partial planes.
-//   * Warp 0 is the producer: one lane streams the range through a ring of
+//   * Warp 0 is the producer: it streams the range through a ring of
 //     shared-memory stages with 1-D bulk copies (cp.async.bulk, one per plane
-//     run) completing on per-stage "full" mbarriers.  Sixteen consumer warps
-//     reduce each stage and release it on an "empty" mbarrier.
+//     run, issued by the 32 lanes in parallel) completing on per-stage "full"
+//     mbarriers.  Sixteen consumer warps reduce each stage and release it on
+//     an "empty" mbarrier.
 //   * Phase 1 (reduction) walks the range forward and writes one double-fp32
 //     partial pair per (segment, channel) into partials[2][grid_y][C], slot j
 //     = k - (first CTA of the channel), then publishes a per-CTA flag.
@@ -176,6 +177,16 @@ __device__ __forceinline__ bool warp_wait_full(FShared& sh, int slot, uint32_t& 
   return true;
 }
 
+// 16-byte output store with the streaming (evict-first) cache hint, so the
+// outputs do not push the inputs that phase 2 still re-reads out of L2.
+__device__ __forceinline__ void store16_cs(float* p, const float (&e)[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(e[0], e[1], e[2], e[3]));
+}
+__device__ __forceinline__ void store16_cs(bf16* p, const float (&e)[8]) {
+  __stcs(reinterpret_cast<uint4*>(p), make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                                                pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7])));
+}
+
 // Stage q of segment s: its first vector inside the channel and its length.
 __device__ __forceinline__ void stage_of(const FShared& sh, const FArgs& a, int s, int q,
                                          int& rv0, int& len) {
@@ -190,33 +201,50 @@ __device__ __forceinline__ int stages_in(const FShared& sh, const FArgs& a, int 
 
 // ------------------------------------------------------------- producer --
 
-// Bulk copies of one stage (plane runs of channel c) into `slot`.
+// Bulk copies of one stage (plane runs of channel c) into `slot`, issued by
+// the whole producer warp: lane l copies runs l, l + 32, ... (one per plane
+// the stage touches), so the per-copy address arithmetic runs in parallel.
 template <typename T, bool BWD>
 __device__ void issue_stage(const FArgs& a, FShared& sh, unsigned char* ring, int slot, int c,
                             int rv0, int len) {
   constexpr int VEC = 16 / sizeof(T);
+  const int lane = threadIdx.x & 31;
   const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
   unsigned char* d0 = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
-  unsigned char* d1 = d0 + in_bytes;
   uint64_t* bar = &sh.full[slot];
-  mbar_arrive_expect_tx(bar, (uint32_t)len * 16u * (BWD ? 2u : 1u));
-  int n = rv0 / a.Pv;
-  int pv = rv0 - n * a.Pv;
-  for (int off = 0; off < len;) {
-    const int run = min(a.Pv - pv, len - off);
-    const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
-    bulk_g2s(d0 + (size_t)off * 16, static_cast<const T*>(a.x) + gvo * VEC, (uint32_t)run * 16u,
-             bar);
-    if (BWD)
-      bulk_g2s(d1 + (size_t)off * 16, static_cast<const T*>(a.dy) + gvo * VEC,
-               (uint32_t)run * 16u, bar);
-    off += run;
-    pv = 0;
-    ++n;
+  if (lane == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)len * 16u * (BWD ? 2u : 1u));
+    sh.issued[slot] += 1;
   }
-  sh.issued[slot] += 1;
+  __syncwarp();
+  const int n0 = rv0 / a.Pv;
+  const int nruns = (rv0 + len - 1) / a.Pv - n0 + 1;
+  for (int r = lane; r < nruns; r += 32) {
+    const int n = n0 + r;
+    const int b = max(rv0, n * a.Pv), e = min(rv0 + len, (n + 1) * a.Pv);
+    const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + (b - n * a.Pv);
+    const uint32_t bytes = (uint32_t)(e - b) * 16u;
+    unsigned char* dst = d0 + (size_t)(b - rv0) * 16;
+    bulk_g2s(dst, static_cast<const T*>(a.x) + gvo * VEC, bytes, bar);
+    if (BWD) bulk_g2s(dst + in_bytes, static_cast<const T*>(a.dy) + gvo * VEC, bytes, bar);
+  }
 }
 
+// Warp-uniform wait of the producer warp for a slot's release.
+__device__ __forceinline__ bool producer_wait_empty(FShared& sh, int slot, uint32_t& epar,
+                                                    int* status) {
+  bool ok = wait_or_abort(&sh.empty[slot], (epar >> slot) & 1u, &sh.abort);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) {
+    if ((threadIdx.x & 31) == 0) set_abort(sh, status);
+    return false;
+  }
+  epar ^= 1u << slot;
+  fence_proxy_async_smem();
+  return true;
+}
+
+// The producer warp (all 32 lanes).
 template <typename T, bool BWD>
 __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
   const int NS = a.nstage, N1 = sh.nst;
@@ -227,15 +255,8 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
     const int nq = stages_in(sh, a, s);
     for (int q = 0; q < nq; ++q, ++i) {
       const int slot = i % NS;
-      if (i >= NS) {
-        if (!wait_or_abort(&sh.empty[slot], (epar >> slot) & 1u, &sh.abort)) {
-          set_abort(sh, a.status);
-          return;
-        }
-        epar ^= 1u << slot;
-        fence_proxy_async_smem();
-      }
-      if (sh.abort) return;
+      if (i >= NS && !producer_wait_empty(sh, slot, epar, a.status)) return;
+      if (__any_sync(0xffffffffu, sh.abort != 0)) return;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len);
@@ -248,13 +269,8 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
     for (int q = nq - 1; q >= 0; --q, ++q2) {
       if (q2 < NS) continue;
       const int slot = (N1 - 1 - q2) % NS;
-      if (!wait_or_abort(&sh.empty[slot], (epar >> slot) & 1u, &sh.abort)) {
-        set_abort(sh, a.status);
-        return;
-      }
-      epar ^= 1u << slot;
-      fence_proxy_async_smem();
-      if (sh.abort) return;
+      if (!producer_wait_empty(sh, slot, epar, a.status)) return;
+      if (__any_sync(0xffffffffu, sh.abort != 0)) return;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len);
@@ -486,7 +502,7 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
             e[k] = fmaf(g[k], scale, fmaf(xc, p3, p4));
           }
         }
-        V::store(out + gvo * VEC, e);
+        store16_cs(out + gvo * VEC, e);
         pv += a.dp;
         n += a.dn;
         if (pv >= a.Pv) {
@@ -529,15 +545,6 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
       sh.seg_len[ns] = (int)(cend - e);
       sh.seg_klo[ns] = (int)((c * a.Mv) / a.Wv);
       sh.seg_khi[ns] = (int)(((c + 1) * a.Mv - 1) / a.Wv);
-      if constexpr (!BWD) {
-        // x[0, c, 0, 0], read before any output of this launch is written.
-        sh.seg_par[ns][0] = to_f32(static_cast<const T*>(a.x)[c * a.P]);
-        sh.seg_par[ns][4] = 0.f;
-      } else {
-        sh.seg_par[ns][0] = a.stats[4 * a.C + c];
-        sh.seg_par[ns][1] = a.stats[5 * a.C + c];
-        sh.seg_par[ns][2] = a.stats[3 * a.C + c];
-      }
       nst += (sh.seg_len[ns] + a.stage_v - 1) / a.stage_v;
       ++ns;
       e = cend;
@@ -549,9 +556,23 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
   __syncthreads();
 
   if (tid < 32) {
-    if (tid == 0) producer<T, BWD>(a, sh, ring);
+    producer<T, BWD>(a, sh, ring);
     __syncwarp();
   } else {
+    // Per-segment parameters (global loads, off the producer's start path).
+    if (tid - 32 < sh.nseg) {
+      const int s = tid - 32;
+      const int64_t c = sh.seg_c[s];
+      if constexpr (!BWD) {
+        sh.seg_par[s][0] = to_f32(static_cast<const T*>(a.x)[c * a.P]);  // x[0, c, 0, 0]
+        sh.seg_par[s][4] = 0.f;
+      } else {
+        sh.seg_par[s][0] = a.stats[4 * a.C + c];
+        sh.seg_par[s][1] = a.stats[5 * a.C + c];
+        sh.seg_par[s][2] = a.stats[3 * a.C + c];
+      }
+    }
+    consumers_sync();
     uint32_t fpar = 0;
     consumer_phase1<T, BWD>(a, sh, ring, fpar);
     consumer_phase2<T, BWD>(a, sh, ring, fpar);
@@ -564,12 +585,17 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
       if (sh.issued[s] > 0 &&
           !mbar_wait_bounded(&sh.full[s], (uint32_t)(sh.issued[s] - 1) & 1u))
         report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
-    // CTA 0 advances the epoch once every CTA has published (so every CTA
-    // has read the old one); after a failure it skips one epoch so that no
-    // flag of this launch can match the next launch's target.
-    if (blockIdx.x == 0) {
-      bool all = !sh.abort;
-      for (int k = 0; k < a.G && all; ++k) all = wait_flag(a.sync + 2 + 2 * (int64_t)k, sh.target);
+  }
+  // CTA 0 advances the epoch once every CTA has published (so every CTA has
+  // read the old one); its threads check the G flags in parallel.  After a
+  // failure it skips one epoch so that no flag of this launch can match the
+  // next launch's target.
+  if (blockIdx.x == 0) {
+    bool ok = !sh.abort;
+    for (int k = tid; k < a.G && ok; k += kFThreads)
+      ok = wait_flag(a.sync + 2 + 2 * (int64_t)k, sh.target);
+    const bool all = __syncthreads_and(ok) != 0;
+    if (tid == 0) {
       if (!all) report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
       const unsigned long long next = all ? sh.target : sh.target + 1ull;
       st_relaxed_u64(a.sync + 1, ~next);

@@ -79,7 +79,8 @@ const DevInfo* device_info(int device) {
       cudaDeviceGetAttribute(&n.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
                              device) != cudaSuccess ||
       cudaDeviceGetAttribute(&n.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, device) !=
-          cudaSuccess)
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&n.l2_bytes, cudaDevAttrL2CacheSize, device) != cudaSuccess)
     return nullptr;
   void* addr = nullptr;
   if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return nullptr;

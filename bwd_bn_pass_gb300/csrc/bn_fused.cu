@@ -79,6 +79,7 @@ struct FArgs {
   int32_t grid_y;
   int32_t G;
   int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
+  int32_t l2_window; // phase-1 stages before the resident tail kept at normal L2 priority
   float Mh, Ml;      // per-channel count M = Mh + Ml exactly
 };
 
@@ -206,7 +207,7 @@ __device__ __forceinline__ int stages_in(const FShared& sh, const FArgs& a, int 
 // the stage touches), so the per-copy address arithmetic runs in parallel.
 template <typename T, bool BWD>
 __device__ void issue_stage(const FArgs& a, FShared& sh, unsigned char* ring, int slot, int c,
-                            int rv0, int len) {
+                            int rv0, int len, uint64_t policy) {
   constexpr int VEC = 16 / sizeof(T);
   const int lane = threadIdx.x & 31;
   const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
@@ -225,8 +226,9 @@ __device__ void issue_stage(const FArgs& a, FShared& sh, unsigned char* ring, in
     const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + (b - n * a.Pv);
     const uint32_t bytes = (uint32_t)(e - b) * 16u;
     unsigned char* dst = d0 + (size_t)(b - rv0) * 16;
-    bulk_g2s(dst, static_cast<const T*>(a.x) + gvo * VEC, bytes, bar);
-    if (BWD) bulk_g2s(dst + in_bytes, static_cast<const T*>(a.dy) + gvo * VEC, bytes, bar);
+    bulk_g2s_hint(dst, static_cast<const T*>(a.x) + gvo * VEC, bytes, bar, policy);
+    if (BWD)
+      bulk_g2s_hint(dst + in_bytes, static_cast<const T*>(a.dy) + gvo * VEC, bytes, bar, policy);
   }
 }
 
@@ -244,10 +246,16 @@ __device__ __forceinline__ bool producer_wait_empty(FShared& sh, int slot, uint3
   return true;
 }
 
-// The producer warp (all 32 lanes).
+// The producer warp (all 32 lanes).  L2 policy of the loads: phase 2 reads
+// the resident tail from shared memory, then the l2_window stages before it
+// (which phase 1 loaded at normal priority, so they are likely still in L2),
+// then the rest from DRAM; every other load is marked evict-first so that it
+// does not displace that window.
 template <typename T, bool BWD>
 __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
   const int NS = a.nstage, N1 = sh.nst;
+  const uint64_t keep = l2_policy_evict_normal(), drop = l2_policy_evict_first();
+  const int keep_lo = N1 - NS - a.l2_window, keep_hi = N1 - NS;  // phase-1 stages kept in L2
   uint32_t epar = 0;  // parity of the next "empty" completion per slot
   // Phase 1: forward.  A slot is refilled once its previous stage is released.
   int i = 0;
@@ -259,7 +267,8 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
       if (__any_sync(0xffffffffu, sh.abort != 0)) return;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
-      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len);
+      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len,
+                          (i >= keep_lo && i < keep_hi) ? keep : drop);
     }
   }
   // Phase 2: backward; the last NS stages are still resident.
@@ -273,7 +282,7 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
       if (__any_sync(0xffffffffu, sh.abort != 0)) return;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
-      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len);
+      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len, drop);
     }
   }
 }
@@ -647,6 +656,7 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
   a.G = p.G;
   a.dn = (int32_t)(kFConsumers / p.Pv);
   a.dp = (int32_t)(kFConsumers % p.Pv);
+  a.l2_window = p.l2_window;
   a.Mh = (float)p.M;
   a.Ml = (float)(p.M - (int64_t)a.Mh);
   return a;
@@ -696,6 +706,10 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
   p->stage_v = (int)stage_v;
   p->nstage = kBnFusedStages;
   p->smem = (size_t)kBnFusedStages * ninputs * (size_t)stage_v * 16;
+  // Stages per CTA whose phase-1 loads stay at normal L2 priority: about
+  // three quarters of L2, shared by the G CTAs.
+  const int64_t stage_bytes = (int64_t)ninputs * stage_v * 16;
+  p->l2_window = (int)((int64_t)dev.l2_bytes * 3 / 4 / ((int64_t)p->G * stage_bytes));
   p->part_offset = ((size_t)16 + (size_t)16 * p->G + 255) & ~(size_t)255;
   p->ws_bytes = p->part_offset + (size_t)2 * p->grid_y * C * sizeof(float2);
   p->ws_bytes = (p->ws_bytes + 255) & ~(size_t)255;

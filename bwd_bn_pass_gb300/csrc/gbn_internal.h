@@ -16,6 +16,7 @@ struct DevInfo {
   int smem_optin = 0;        // max dynamic shared memory per block (bytes)
   int smem_per_sm = 0;       // shared memory per SM (bytes)
   int smem_reserved = 0;     // shared memory the runtime reserves per block
+  int l2_bytes = 0;          // L2 cache size
   int* status = nullptr;     // device address of the library status word
   bool fused_ok = false;     // the persistent BatchNorm kernel fits one CTA per SM
   bool ok = false;
@@ -96,6 +97,7 @@ struct BnFusedPlan {
   int grid_y = 0;          // partial slots per channel
   int stage_v = 0;         // vectors per stage and input
   int nstage = 0;
+  int l2_window = 0;       // phase-1 stages per CTA kept at normal L2 priority
   size_t smem = 0;         // dynamic shared memory (the ring)
   size_t part_offset = 0;  // partials offset in the workspace (sync words first)
   size_t ws_bytes = 0;

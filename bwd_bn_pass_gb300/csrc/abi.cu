@@ -144,7 +144,8 @@ size_t gbn_bn_workspace_bytes(int64_t B, int64_t C, int64_t HW, int device) {
 
 static int bn_prepare(int dtype, int64_t B, int64_t C, int64_t HW, bool training,
                       const void* const* ptrs, int nptrs, const void* ws, size_t ws_bytes,
-                      bool need_ws, BnPlan* plan, const DevInfo** dev_out) {
+                      bool need_ws, BnPlan* plan, const DevInfo** dev_out,
+                      bool partials_only = false) {
   int64_t M;
   const int rc = bn_check(dtype, B, C, HW, training, &M);
   if (rc != GBN_OK) return rc;
@@ -153,7 +154,8 @@ static int bn_prepare(int dtype, int64_t B, int64_t C, int64_t HW, bool training
   if (!dev) return GBN_ECUDA;
   if (!bn_plan(B, C, HW, *dev, plan)) return GBN_EINVAL;
   if (need_ws && (ws == nullptr)) return GBN_EINVAL;
-  if (need_ws && ws_bytes < plan->ws_bytes) return GBN_EWORKSPACE;
+  if (need_ws && ws_bytes < (partials_only ? plan->ws_partials : plan->ws_bytes))
+    return GBN_EWORKSPACE;
   plan->vec = bn_vec_width(dtype, HW, ptrs, nptrs);
   *dev_out = dev;
   return GBN_OK;
@@ -181,7 +183,7 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
                                   const float* gamma, const float* beta, float* running_mean,
                                   float* running_var, float momentum, float eps, void* y,
                                   float* stats, const void* ws, size_t ws_bytes, void* stream,
-                                  bool with_stats_pass) {
+                                  bool with_stats_pass, bool partials_only = false) {
   int64_t M;
   int rc = bn_check(dtype, B, C, HW, true, &M);
   if (rc != GBN_OK) return rc;
@@ -192,7 +194,7 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
   const void* ptrs[2] = {x, y};
   BnPlan p;
   const DevInfo* dev;
-  rc = bn_prepare(dtype, B, C, HW, true, ptrs, 2, ws, ws_bytes, true, &p, &dev);
+  rc = bn_prepare(dtype, B, C, HW, true, ptrs, 2, ws, ws_bytes, true, &p, &dev, partials_only);
   if (rc != GBN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float2* part = static_cast<float2*>(const_cast<void*>(ws));
@@ -210,6 +212,31 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
                                    running_mean, running_var, momentum, eps, nullptr, nullptr, st,
                                    /*pdl=*/true));
 }
+
+}  // extern "C"
+
+namespace gbn {
+
+size_t bn_partials_bytes(int64_t B, int64_t C, int64_t HW) {
+  int64_t M;
+  if (bn_check(GBN_F32, B, C, HW, false, &M) != GBN_OK) return 0;
+  const DevInfo* dev = device_info(-1);
+  BnPlan p;
+  if (!dev || !bn_plan(B, C, HW, *dev, &p)) return 0;
+  return p.ws_partials;
+}
+
+int bn_forward_train_scratch(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                             const float* gamma, const float* beta, float* running_mean,
+                             float* running_var, float momentum, float eps, void* y,
+                             float* stats, void* ws, size_t ws_bytes, void* stream) {
+  return bn_finalize_apply_impl(x, dtype, B, C, HW, gamma, beta, running_mean, running_var,
+                                momentum, eps, y, stats, ws, ws_bytes, stream, true, true);
+}
+
+}  // namespace gbn
+
+extern "C" {
 
 int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                          const float* gamma, const float* beta, float* running_mean,

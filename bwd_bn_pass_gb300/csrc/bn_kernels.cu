@@ -572,7 +572,8 @@ bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan)
   if (gy > 65535) gy = 65535;
   plan->grid_y = (int)gy;
   const size_t bytes = (size_t)2 * (size_t)gy * (size_t)(C > 0 ? C : 1) * sizeof(float2);
-  plan->ws_bytes = (bytes + 255) & ~(size_t)255;
+  plan->ws_partials = (bytes + 255) & ~(size_t)255;
+  plan->ws_bytes = plan->ws_partials;
   // The same workspace also serves the persistent path of either dtype.
   BnFusedPlan fp;
   for (int dtype : {GBN_F32, GBN_BF16})

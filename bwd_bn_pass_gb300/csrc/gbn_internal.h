@@ -59,7 +59,8 @@ struct BnPlan {
   int64_t M = 0;                // per-channel count B*P
   int grid_y = 0;               // blocks per channel
   int vec = 1;                  // elements per vector access
-  size_t ws_bytes = 0;          // partials bytes (2 * grid_y * C fp32 pairs, rounded)
+  size_t ws_partials = 0;       // two-launch partials bytes (2 * grid_y * C fp32 pairs, rounded)
+  size_t ws_bytes = 0;          // workspace of the public calls: also fits the persistent path
 };
 
 // Fills grid_y / ws_bytes (device-dependent) for a shape; false on error.
@@ -116,6 +117,16 @@ cudaError_t bn_fused_backward(const BnFusedPlan& p, int dtype, const void* x, co
                               cudaStream_t st);
 // Shared-memory limits and the one-CTA-per-SM check (called from device_info).
 cudaError_t bn_fused_configure(int smem_optin, bool* ok);
+
+// Training forward with a caller-fixed scratch buffer (the allocation-free
+// entry point): `ws` must hold at least bn_partials_bytes(B, C, HW) bytes;
+// the persistent kernel is used when `ws_bytes` also fits its workspace,
+// else the two-launch kernels.  Same status codes as gbn_bn_forward_train.
+size_t bn_partials_bytes(int64_t B, int64_t C, int64_t HW);
+int bn_forward_train_scratch(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                             const float* gamma, const float* beta, float* running_mean,
+                             float* running_var, float momentum, float eps, void* y,
+                             float* stats, void* ws, size_t ws_bytes, void* stream);
 
 // ------------------------------------------------------------ row-wise --
 

@@ -12,16 +12,21 @@
 // The entry point allocates nothing: it resolves the array's device address
 // once per device (the host-side symbol is only a stand-in, never a device
 // address) and then runs the ordinary forward with that address as the
-// workspace.
+// workspace.  Nothing needs zeroing: the partials are rewritten by every
+// call, and the persistent kernel's flags carry a launch epoch that the
+// kernel validates and advances itself.
 #include <mutex>
 
 #include "gbn_internal.h"
 
 namespace {
 
-// 64 KiB: the stats partials take 16 * grid_y * C bytes, and grid_y * C is at
-// most one resident block slot per SM (1216 on GB300) whenever C <= 1216, so
-// every shape with C <= 4096 channels fits on GB300.
+// 64 KiB: the two-launch kernels' stats partials take 16 * grid_y * C bytes,
+// and grid_y * C is at most one resident block slot per SM (608 on GB300)
+// whenever C <= 608, so every shape with C <= 4096 channels fits on GB300.
+// The single-launch persistent kernel also needs its per-CTA flags (16 bytes
+// per SM) and its own partials; it runs whenever those fit too, otherwise
+// the two-launch kernels do.
 constexpr size_t kNoAllocScratchBytes = 64 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -54,8 +59,9 @@ extern "C" int gbn_bn_forward_train_noalloc(const void* x, int dtype, int64_t B,
                                             void* stream) {
   void* scratch = scratch_on_current_device();
   if (scratch == nullptr) return GBN_ECUDA;
-  const size_t need = gbn_bn_workspace_bytes(B, C, HW, -1);
+  const size_t need = gbn::bn_partials_bytes(B, C, HW);
   if (need > kNoAllocScratchBytes) return GBN_EWORKSPACE;
-  return gbn_bn_forward_train(x, dtype, B, C, HW, gamma, beta, running_mean, running_var,
-                              momentum, eps, y, stats, scratch, kNoAllocScratchBytes, stream);
+  return gbn::bn_forward_train_scratch(x, dtype, B, C, HW, gamma, beta, running_mean,
+                                       running_var, momentum, eps, y, stats, scratch,
+                                       kNoAllocScratchBytes, stream);
 }

@@ -147,12 +147,15 @@ GBN_API int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C,
  * cannot allocate device memory (code inside a CUDA-graph capture or a
  * real-time loop where cudaMalloc is forbidden, plugins whose host framework
  * owns every allocation, C callers without an allocator).  Same as
- * gbn_bn_forward_train without `ws`/`ws_bytes`: the stats partials go to a
- * fixed 64 KiB file-scope device array inside the library, which every GPU
- * that loads the library holds until the process exits.  Shapes whose
+ * gbn_bn_forward_train without `ws`/`ws_bytes`: the scratch (stats partials
+ * and, for the single-launch kernel, its per-block flags) goes to a fixed
+ * 64 KiB file-scope device array inside the library, which every GPU that
+ * loads the library holds until the process exits.  Shapes whose two-launch
  * partials need more (16 * grid_y * C bytes; all C <= 4096 fit on GB300) are
- * rejected with GBN_EWORKSPACE.  Allocates nothing and nothing needs zeroing:
- * every call rewrites the partials it reads.  All calls share the one array,
+ * rejected with GBN_EWORKSPACE; shapes whose single-launch scratch does not
+ * fit run the two-launch kernels.  Allocates nothing and nothing needs
+ * zeroing: every call rewrites the partials it reads and the flags carry a
+ * launch epoch checked on the device.  All calls share the one array,
  * so calls that overlap on the GPU (other streams, other threads) race; order
  * them on one stream.  The first call on a device resolves the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first

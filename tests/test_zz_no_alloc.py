@@ -72,7 +72,11 @@ def test_noalloc_forward_matches_workspace_forward_twice(gbn):
         pytest.skip("no CUDA device")
     cases = [synth.CASES["bn_ragged_f32"],
              synth.BNCase("noalloc_bf16", (16, 64, 28, 28), "bf16", mu_range=(-100, 100),
-                          sigma_range=(0.01, 10), seed=7)]
+                          sigma_range=(0.01, 10), seed=7),
+             # many channels: the single-launch kernel's scratch would not fit
+             # the fixed array, so the call runs the two-launch kernels
+             synth.BNCase("noalloc_wide_f32", (64, 3000, 8, 8), "f32", mu_range=(-10, 10),
+                          seed=8)]
     refs = [_run(gbn, c, noalloc=False) for c in cases]
     for c, ref in zip(cases, refs):          # two calls in a row
         got = _run(gbn, c, noalloc=True)

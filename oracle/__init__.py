@@ -20,10 +20,12 @@ from .bn import (
     batch_norm_apply,
     batch_norm_backward,
 )
-from .rmsnorm import rms_norm_rstd, rms_norm_backward
+from .rmsnorm import rms_norm_rstd, rms_norm_forward, rms_norm_backward
 from .layernorm import (
     dropout_add,
     layer_norm_saved_stats,
+    layer_norm_forward,
+    fused_bias_dropout_add_layer_norm_forward,
     layer_norm_backward,
     fused_bias_dropout_add_layer_norm_backward,
 )
@@ -33,9 +35,12 @@ __all__ = [
     "batch_norm_apply",
     "batch_norm_backward",
     "rms_norm_rstd",
+    "rms_norm_forward",
     "rms_norm_backward",
     "dropout_add",
     "layer_norm_saved_stats",
+    "layer_norm_forward",
+    "fused_bias_dropout_add_layer_norm_forward",
     "layer_norm_backward",
     "fused_bias_dropout_add_layer_norm_backward",
 ]

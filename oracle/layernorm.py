@@ -61,6 +61,32 @@ def layer_norm_saved_stats(z, eps):
     return mu, 1.0 / np.sqrt(var + eps)
 
 
+def layer_norm_forward(z, gamma, beta, eps):
+    """Training forward whose saved statistics the backward takes (T5/T7):
+    ``y = (z - mean) * rstd * gamma + beta`` per row, with the biased
+    variance.  gamma / beta may be None (ones / zeros).  Returns dict
+    y [R, H], mean [R], rstd [R]."""
+    z = _f64(z)
+    H = z.shape[1]
+    mu, rstd = layer_norm_saved_stats(z, eps)
+    g = np.ones(H) if gamma is None else _f64(gamma)
+    b = np.zeros(H) if beta is None else _f64(beta)
+    centred = z - mu[:, None]
+    y = centred * rstd[:, None] * g[None, :] + b[None, :]
+    return {"y": y, "mean": mu, "rstd": rstd}
+
+
+def fused_bias_dropout_add_layer_norm_forward(inp, residual, bias, mask, scale, gamma, beta,
+                                              eps):
+    """The forward whose backward is ``nvfuser_fusion_id9``: z = residual +
+    mask * scale * (inp + bias) (the residual-stream output), then the
+    LayerNorm of z.  Returns dict z, y [R, H], mean, rstd [R]."""
+    z = dropout_add(inp, residual, bias, mask, scale)
+    out = layer_norm_forward(z, gamma, beta, eps)
+    out["z"] = z
+    return out
+
+
 def _ln_core(dy, z, mean, rstd, gamma, dz_extra):
     dy = _f64(dy)
     z = _f64(z)

@@ -6,7 +6,7 @@ Source: nvFuser issue #3629, "Performance gap between manual nvfuser
 definition and thunder.jit for rmsnorm".
 
 * Forward (section with ``rmsnorm_prims`` / ``F.rms_norm``):
-  ``y = w * x / sqrt(mean(x^2, dim=1) + eps)``.
+  ``y = w * x / sqrt(mean(x^2, dim=1) + eps)`` (``rms_norm_forward``).
 * Backward (section "nvfuser pre-generated definition", ``rmsnorm_bwd_fusion``):
   with the saved per-row statistic, ``dx = dy*w/rms - x * sum(dy*w*x) /
   (H * rms^3)`` and ``dweight = sum over rows of dy * x / rms``.
@@ -27,6 +27,19 @@ def rms_norm_rstd(x, eps):
     """Setup helper: the saved statistic rstd = 1/sqrt(mean(x^2) + eps) per row."""
     x = np.asarray(x, dtype=np.float64)
     return 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
+
+
+def rms_norm_forward(x, w, eps):
+    """Training forward (the ``rmsnorm_prims`` / ``F.rms_norm`` section):
+    ``y = w * x * rstd`` with ``rstd = 1/sqrt(mean(x^2) + eps)`` per row.
+
+    x: [R, H]; w: [H] or None (all ones).  Returns dict y [R, H], rstd [R]
+    (the statistic the backward takes)."""
+    x = np.asarray(x, dtype=np.float64)
+    rstd = rms_norm_rstd(x, eps)
+    wv = np.ones(x.shape[1]) if w is None else np.asarray(w, dtype=np.float64)
+    y = x * rstd[:, None] * wv[None, :]
+    return {"y": y, "rstd": rstd}
 
 
 def rms_norm_backward(x, dy, w, rstd):

@@ -283,8 +283,22 @@ def pin_rms_exact_rational(rms):
     _close(out["dx"][0], grad, rtol=1e-13, what="exact rms dx")
 
 
+def pin_rms_forward(rms):
+    """The training forward against torch's float64 F.rms_norm, and the
+    closed form mean(y^2) = ms / (ms + eps) for unit weights."""
+    x, _, w = _rms_data(14, R=5, H=10)
+    eps = 0.05
+    out = rms.rms_norm_forward(x, w, eps)
+    ty = F.rms_norm(torch.tensor(x), (x.shape[1],), torch.tensor(w), eps=eps)
+    _close(out["y"], ty.numpy(), what="rms forward y vs torch")
+    o1 = rms.rms_norm_forward(x, None, eps)
+    ms = (x * x).mean(axis=1)
+    _close((o1["y"] ** 2).mean(axis=1), ms / (ms + eps), what="mean y^2")
+    _close(o1["y"], x * o1["rstd"][:, None], what="unit weights: y = x*rstd")
+
+
 RMS_PINS = [pin_rms_vs_torch, pin_rms_finite_differences, pin_rms_invariants,
-            pin_rms_exact_rational]
+            pin_rms_exact_rational, pin_rms_forward]
 
 
 # ---------------------------------------------------------------- LayerNorm
@@ -400,5 +414,27 @@ def pin_ln_invariants(ln):
     _close(out["dbeta"], dy.sum(axis=0), what="dbeta = sum dy")
 
 
+def pin_ln_forward(ln):
+    """The training forwards against torch's float64 native_layer_norm
+    (which returns y, mean and rstd), the fused z against the same
+    bias-dropout-add written in torch, and the closed forms of a unit-affine
+    LayerNorm: zero row mean, mean(y^2) = var / (var + eps)."""
+    inp, res, bias, mask, gamma, beta, _, _ = _ln_data(25, R=4, H=11)
+    eps, s = 0.1, 1.25
+    tz = (torch.tensor(res) + torch.tensor(mask) * s
+          * (torch.tensor(inp) + torch.tensor(bias)[None, :]))
+    ty, tmu, trstd = torch.native_layer_norm(tz, (inp.shape[1],), torch.tensor(gamma),
+                                             torch.tensor(beta), eps)
+    out = ln.fused_bias_dropout_add_layer_norm_forward(inp, res, bias, mask, s, gamma, beta, eps)
+    _close(out["z"], tz.numpy(), what="fused forward z vs torch")
+    _close(out["y"], ty.numpy(), what="fused forward y vs torch")
+    _close(out["mean"], tmu.numpy().reshape(-1), what="forward mean vs torch")
+    _close(out["rstd"], trstd.numpy().reshape(-1), what="forward rstd vs torch")
+    p = ln.layer_norm_forward(res, None, None, eps)
+    var = res.var(axis=1)
+    _close(p["y"].mean(axis=1), np.zeros(res.shape[0]), atol=1e-12, what="row mean of y")
+    _close((p["y"] ** 2).mean(axis=1), var / (var + eps), what="mean y^2")
+
+
 LN_PINS = [pin_ln_plain_vs_torch, pin_ln_fused_vs_torch,
-           pin_ln_finite_differences, pin_ln_invariants]
+           pin_ln_finite_differences, pin_ln_invariants, pin_ln_forward]

@@ -54,6 +54,14 @@ MUTATIONS = [
     (oln, pins.LN_PINS, "g = dy * gamma", "g = dy"),
     (oln, pins.LN_PINS, "dbias = None if bias is None else dx.sum(axis=0)",
      "dbias = None if bias is None else dresidual.sum(axis=0)"),
+    # forwards
+    (orms, pins.RMS_PINS, "y = x * rstd[:, None] * wv[None, :]", "y = x * rstd[:, None]"),
+    (orms, pins.RMS_PINS, "return 1.0 / np.sqrt((x * x).mean(axis=1) + eps)",
+     "return 1.0 / np.sqrt((x * x).mean(axis=1))"),
+    (oln, pins.LN_PINS, "y = centred * rstd[:, None] * g[None, :] + b[None, :]",
+     "y = centred * rstd[:, None] * g[None, :]"),
+    (oln, pins.LN_PINS, "return mu, 1.0 / np.sqrt(var + eps)", "return mu, 1.0 / np.sqrt(var)"),
+    (oln, pins.LN_PINS, "var = (c * c).mean(axis=1)", "var = (c * c).sum(axis=1) / (z.shape[1] - 1)"),
 ]
 
 

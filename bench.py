@@ -10,6 +10,11 @@ One step = one pass of every hot-path operation over its workload:
   bn_bf16_fwd  BatchNorm2d training forward  bf16 [128,256,56,56]
   bn_bf16_bwd  BatchNorm2d training backward bf16 [128,256,56,56]
 
+Also available through --ops (not part of the default step, whose
+operations are the configured workloads): rms_bf16_fwd, rms_f32_fwd
+(RMSNorm training forward [2048, 8192]) and ln_bf16_fwd (bias+dropout+add
+LayerNorm training forward [16*512, 1600]).
+
 Every call goes through the C ABI (ctypes binding).  Each operation is timed
 with CUDA events on the stream it runs on, after an L2 flush (a 256 MB write
 then a 256 MB read of another buffer, outside the events).  BatchNorm runs
@@ -219,6 +224,42 @@ def build_ops(names, dev):
                 ops.append(Op(name, f"BatchNorm2d bwd {case.dtype} [{shape}]", phases,
                               ub, {"bn_backward": ub}, 1,
                               [(hx, x), (hdy, dy)], [(dx, hdx)], None))
+        elif name in ("rms_bf16_fwd", "rms_f32_fwd"):
+            case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]
+            inp = synth.rms_inputs(case)
+            hx, hw = _pin(inp["x"]), _pin(inp["w"])
+            x, w = hx.to(dev), hw.to(dev)
+            y = torch.empty_like(x)
+            rstd = torch.empty(case.rows, dtype=torch.float32, device=dev)
+            phases = [("rms_fwd", lambda x=x, w=w, y=y, rstd=rstd, e=case.eps:
+                        G.rmsnorm_forward(x, w, e, y=y, rstd=rstd))]
+            ub = _nbytes(x, w, y, rstd)
+            hy, hr = torch.empty_like(hx).pin_memory(), torch.empty_like(rstd, device="cpu").pin_memory()
+            ops.append(Op(name, f"RMSNorm fwd {case.dtype} [{case.rows}x{case.hidden}]",
+                          phases, ub, {"rms_fwd": ub}, 1, [(hx, x), (hw, w)],
+                          [(y, hy), (rstd, hr)], None))
+        elif name == "ln_bf16_fwd":
+            case = synth.CASES["ln_fused_bf16"]
+            inp = synth.ln_inputs(case)
+            host = {k: _pin(v) for k, v in inp.items() if torch.is_tensor(v)}
+            d = {k: v.to(dev) for k, v in host.items()}
+            s = inp["dropout_scale"]
+            y, z = torch.empty_like(d["inp"]), torch.empty_like(d["inp"])
+            mean = torch.empty(case.rows, dtype=torch.float32, device=dev)
+            rstd = torch.empty_like(mean)
+            phases = [("ln_fwd", lambda d=d, s=s, y=y, z=z, mean=mean, rstd=rstd, e=case.eps:
+                       G.layernorm_forward(d["inp"], d["gamma"], d["beta"], e,
+                                           residual=d["residual"], bias=d["bias"],
+                                           mask=d["mask"], dropout_scale=s, y=y, z=z,
+                                           mean=mean, rstd=rstd))]
+            ub = _nbytes(d["inp"], d["residual"], d["mask"], d["bias"], d["gamma"], d["beta"],
+                         y, z, mean, rstd)
+            order = ["inp", "residual", "mask", "bias", "gamma", "beta"]
+            outs = [(t, torch.empty_like(t, device="cpu").pin_memory())
+                    for t in (y, z, mean, rstd)]
+            ops.append(Op(name, f"bias+dropout+add+LayerNorm fwd bf16 "
+                          f"[{case.rows}x{case.hidden}]", phases, ub, {"ln_fwd": ub}, 1,
+                          [(host[k], d[k]) for k in order], outs, None))
         elif name.startswith("rms_"):
             case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]
             inp = synth.rms_inputs(case)

@@ -87,6 +87,7 @@ const DevInfo* device_info(int device) {
   n.status = static_cast<int*>(addr);
   if (row_kernels_configure(n.smem_optin) != cudaSuccess) return nullptr;
   if (bn_fused_configure(n.smem_optin, &n.fused_ok) != cudaSuccess) return nullptr;
+  if (row_fwd_configure() != cudaSuccess) return nullptr;
   n.ok = true;
   d = n;
   return &d;
@@ -412,6 +413,66 @@ int gbn_layernorm_backward(const void* dy, const void* x_or_input, int dtype, co
   q.dbias = dbias;
   return to_status(ln_launch(p, q, static_cast<float*>(ws), dev->status,
                              static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------ row-wise forward --
+
+int gbn_rmsnorm_forward(const void* x, const void* w, int dtype, int64_t R, int64_t H, float eps,
+                        void* y, float* rstd, void* stream) {
+  int rc = row_check(dtype, R, H);
+  if (rc != GBN_OK) return rc;
+  if (!(eps >= 0.f)) return GBN_EINVAL;
+  if (R == 0) return GBN_OK;
+  if (rstd == nullptr) return GBN_EINVAL;
+  if (H > 0 && (x == nullptr || y == nullptr)) return GBN_EINVAL;
+  if (H == 0) return GBN_EINVAL;  // the mean over an empty row is undefined
+  const DevInfo* dev = device_info(-1);
+  if (!dev) return GBN_ECUDA;
+  const int64_t esize = dtype == GBN_F32 ? 4 : 2;
+  const bool vec_ok = (H * esize) % 16 == 0 && aligned(x, 16) && aligned(w, 16) && aligned(y, 16);
+  RowFwdPtrs q;
+  q.x = x;
+  q.w = w;
+  q.y = y;
+  q.rstd = rstd;
+  return to_status(row_fwd_launch(GBN_ROW_RMS, dtype, q, R, H, eps, 1.f, vec_ok, *dev,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+int gbn_layernorm_forward(const void* x_or_input, int dtype, int64_t R, int64_t H,
+                          const void* residual, const void* bias, const uint8_t* mask,
+                          float dropout_scale, const void* gamma, const void* beta, float eps,
+                          void* y, void* z, float* mean, float* rstd, void* stream) {
+  int rc = row_check(dtype, R, H);
+  if (rc != GBN_OK) return rc;
+  const bool fused = residual != nullptr;
+  if (!fused && (bias || mask || z)) return GBN_EINVAL;
+  if (!(eps >= 0.f) || dropout_scale != dropout_scale) return GBN_EINVAL;
+  if (R == 0) return GBN_OK;
+  if (mean == nullptr || rstd == nullptr) return GBN_EINVAL;
+  if (H == 0) return GBN_EINVAL;  // the mean over an empty row is undefined
+  if (x_or_input == nullptr || y == nullptr) return GBN_EINVAL;
+  const DevInfo* dev = device_info(-1);
+  if (!dev) return GBN_ECUDA;
+  const int64_t esize = dtype == GBN_F32 ? 4 : 2;
+  const bool vec_ok = (H * esize) % 16 == 0 && (mask == nullptr || H % 16 == 0) &&
+                      aligned(x_or_input, 16) && aligned(residual, 16) && aligned(bias, 16) &&
+                      aligned(mask, 16) && aligned(gamma, 16) && aligned(beta, 16) &&
+                      aligned(y, 16) && aligned(z, 16);
+  RowFwdPtrs q;
+  q.x = x_or_input;
+  q.residual = residual;
+  q.bias = bias;
+  q.mask = mask;
+  q.w = gamma;
+  q.beta = beta;
+  q.y = y;
+  q.z = z;
+  q.mean = mean;
+  q.rstd = rstd;
+  return to_status(row_fwd_launch(fused ? GBN_ROW_LN_FUSED : GBN_ROW_LN, dtype, q, R, H, eps,
+                                  fused ? dropout_scale : 1.f, vec_ok, *dev,
+                                  static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -181,6 +181,28 @@ cudaError_t rms_launch(const RowPlan& p, const void* dy, const void* x, const vo
 cudaError_t ln_launch(const RowPlan& p, const LnPtrs& a, float* part, int* status,
                       cudaStream_t st);
 
+// Row-wise training forwards (fwd_kernels.cu).
+struct RowFwdPtrs {
+  const void* x = nullptr;         // RMSNorm x / LayerNorm input
+  const void* residual = nullptr;  // fused LayerNorm
+  const void* bias = nullptr;
+  const uint8_t* mask = nullptr;
+  const void* w = nullptr;         // RMSNorm weight / LayerNorm gamma
+  const void* beta = nullptr;
+  void* y = nullptr;
+  void* z = nullptr;
+  float* mean = nullptr;
+  float* rstd = nullptr;
+};
+
+// kind: GBN_ROW_RMS, GBN_ROW_LN or GBN_ROW_LN_FUSED.  vec_ok: every tensor
+// is 16-byte aligned and a row is a whole number of 16-byte vectors (and of
+// 8-byte mask words), so the register-resident vector kernels may run.
+cudaError_t row_fwd_launch(int kind, int dtype, const RowFwdPtrs& p, int64_t R, int64_t H,
+                           float eps, float scale, bool vec_ok, const DevInfo& dev,
+                           cudaStream_t st);
+cudaError_t row_fwd_configure();  // shared-memory limits (called from device_info)
+
 // Column-partials reduction: out[o][h] = sum_g part[o][*][g][h] in a fixed
 // order; outs[o] may be nullptr (skipped).  Launched with PDL after the row
 // kernel when `pdl` is set.

@@ -69,6 +69,9 @@ _SIGNATURES = {
     "gbn_rmsnorm_backward": (_INT, [_P, _P, _P, _INT, _P, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "gbn_layernorm_backward": (_INT, [_P, _P, _INT, _P, _P, _P, _I64, _I64, _P, _P, _P, _F,
                                       _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "gbn_rmsnorm_forward": (_INT, [_P, _P, _INT, _I64, _I64, _F, _P, _P, _P]),
+    "gbn_layernorm_forward": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _F, _P, _P, _F, _P, _P,
+                                     _P, _P, _P]),
 }
 
 
@@ -392,3 +395,59 @@ def layernorm_backward(dy, x, mean, rstd, gamma, *, residual=None, bias=None, ma
     _check("gbn_layernorm_backward", st)
     return {"dx": dx, "dresidual": dresidual, "dgamma": dgamma, "dbeta": dbeta,
             "dbias": dbias}
+
+
+def rmsnorm_forward(x, w=None, eps=1e-5, *, y=None, rstd=None):
+    """RMSNorm training forward.  Returns (y, rstd) with rstd fp32 [rows]."""
+    R, H = _rows(x, "x")
+    if w is not None and (_cuda(w, "w").dtype != x.dtype or w.numel() != H):
+        raise ValueError("w must match x's dtype and last dimension")
+    y = torch.empty_like(x) if y is None else _cuda(y, "y")
+    rstd = torch.empty(R, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    if _cuda(rstd, "rstd").dtype != torch.float32 or rstd.numel() != R:
+        raise TypeError("rstd must be float32 with one value per row")
+    _same_device(x, ("w", w), ("y", y), ("rstd", rstd))
+    with torch.cuda.device(x.device):
+        st = lib().gbn_rmsnorm_forward(_ptr(x), _ptr(w), _code(x.dtype), R, H, float(eps),
+                                       _ptr(y), _ptr(rstd), _stream(x.device))
+    _check("gbn_rmsnorm_forward", st)
+    return y, rstd
+
+
+def layernorm_forward(x, gamma=None, beta=None, eps=1e-5, *, residual=None, bias=None,
+                      mask=None, dropout_scale=1.0, y=None, z=None, mean=None, rstd=None,
+                      want_z=True):
+    """LayerNorm training forward; fused with bias+dropout+add when
+    ``residual`` is given (then ``x`` is the dropout input and z = residual +
+    mask*dropout_scale*(x + bias) is returned as the residual-stream output).
+    Returns a dict with y, z (None when not fused or not wanted), mean, rstd."""
+    R, H = _rows(x, "x")
+    fused = residual is not None
+    for name, t in (("gamma", gamma), ("beta", beta), ("bias", bias)):
+        if t is not None and (_cuda(t, name).dtype != x.dtype or t.numel() != H):
+            raise ValueError(f"{name} must match x's dtype and last dimension")
+    if fused and (_cuda(residual, "residual").shape != x.shape or residual.dtype != x.dtype):
+        raise ValueError("residual must match x")
+    if mask is not None:
+        _cuda(mask, "mask")
+        if mask.dtype == torch.bool:
+            mask = mask.view(torch.uint8)
+        if mask.dtype != torch.uint8:
+            raise TypeError("mask must be bool or uint8")
+    y = torch.empty_like(x) if y is None else _cuda(y, "y")
+    if fused and z is None and want_z:
+        z = torch.empty_like(x)
+    mean = torch.empty(R, dtype=torch.float32, device=x.device) if mean is None else mean
+    rstd = torch.empty(R, dtype=torch.float32, device=x.device) if rstd is None else rstd
+    for name, t in (("mean", mean), ("rstd", rstd)):
+        if _cuda(t, name).dtype != torch.float32 or t.numel() != R:
+            raise TypeError(f"{name} must be float32 with one value per row")
+    _same_device(x, ("gamma", gamma), ("beta", beta), ("residual", residual), ("bias", bias),
+                 ("mask", mask), ("y", y), ("z", z), ("mean", mean), ("rstd", rstd))
+    with torch.cuda.device(x.device):
+        st = lib().gbn_layernorm_forward(
+            _ptr(x), _code(x.dtype), R, H, _ptr(residual), _ptr(bias), _ptr(mask),
+            float(dropout_scale), _ptr(gamma), _ptr(beta), float(eps), _ptr(y), _ptr(z),
+            _ptr(mean), _ptr(rstd), _stream(x.device))
+    _check("gbn_layernorm_forward", st)
+    return {"y": y, "z": z, "mean": mean, "rstd": rstd}

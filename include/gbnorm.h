@@ -262,6 +262,39 @@ GBN_API int gbn_layernorm_backward(const void* dy, const void* x_or_input, int d
                            void* dgamma, void* dbeta, void* dbias, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* =========================================================================
+ * Row-wise training forwards: RMSNorm ([P3]) and LayerNorm ([P2]), writing
+ * the statistics the backward passes above take.  Tensors are [R, H]
+ * row-major in `dtype`; statistics are fp32 [R].  Each row is loaded once
+ * into registers (one warp per row up to 256 16-byte vectors, one block per
+ * row up to 2048), reduced with warp shuffles and written back; longer or
+ * unaligned rows take a block-per-row kernel that re-reads the row from L2.
+ * No workspace.  H must be positive when R > 0.
+ * ======================================================================= */
+
+/* RMSNorm forward ([P3] the rmsnorm_prims / F.rms_norm section):
+ *   rstd_r = 1/sqrt(mean_j x_rj^2 + eps),   y_rj = x_rj*rstd_r*w_j.
+ * x, y: [R, H]; w: [H] or NULL (ones); rstd: fp32 [R] (written); eps >= 0.
+ * Returns GBN_EINVAL for a null x / y / rstd or H == 0 with R > 0.        */
+GBN_API int gbn_rmsnorm_forward(const void* x, const void* w, int dtype, int64_t R,
+                                int64_t H, float eps, void* y, float* rstd, void* stream);
+
+/* LayerNorm forward, plain or fused with bias+dropout+add ([P2]: the
+ * forward whose saved mean (T5) and rstd (T7) the backward repros take).
+ * Plain (residual == NULL; bias, mask, z must be NULL): z = x_or_input.
+ * Fused (residual != NULL): z = residual + mask*dropout_scale*(x_or_input +
+ *   bias) in fp32, written to `z` (the residual-stream output) unless NULL.
+ * Then mean_r = mean_j z_rj, rstd_r = 1/sqrt(mean_j (z_rj - mean_r)^2 + eps)
+ * (biased variance, as a second pass) and
+ *   y_rj = (z_rj - mean_r)*rstd_r*gamma_j + beta_j.
+ * gamma, beta, bias: [H] or NULL (ones / zeros / none); mask: uint8 [R, H]
+ * (nonzero = kept) or NULL; mean, rstd: fp32 [R] (written).               */
+GBN_API int gbn_layernorm_forward(const void* x_or_input, int dtype, int64_t R, int64_t H,
+                                  const void* residual, const void* bias,
+                                  const uint8_t* mask, float dropout_scale,
+                                  const void* gamma, const void* beta, float eps, void* y,
+                                  void* z, float* mean, float* rstd, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -131,9 +131,40 @@ def test_layernorm_argument_errors(gbn):
     assert _ln(L, ws=A4) == EALIGN
 
 
+def _rmsf(L, dtype=1, R=4, H=64, x=A16, w=A16, eps=1e-5, y=A16, rstd=A16):
+    return L.gbn_rmsnorm_forward(x, w, dtype, R, H, eps, y, rstd, NULL)
+
+
+def _lnf(L, dtype=1, R=4, H=64, x=A16, residual=NULL, bias=NULL, mask=NULL, scale=1.0,
+         eps=1e-5, y=A16, z=NULL, mean=A16, rstd=A16):
+    return L.gbn_layernorm_forward(x, dtype, R, H, residual, bias, mask, scale, A16, A16, eps,
+                                   y, z, mean, rstd, NULL)
+
+
+def test_forward_argument_errors(gbn):
+    L = gbn.lib()
+    assert _rmsf(L, dtype=3) == EDTYPE
+    assert _rmsf(L, R=-1) == EINVAL
+    assert _rmsf(L, H=0) == EINVAL               # empty rows have no mean
+    assert _rmsf(L, x=NULL) == EINVAL
+    assert _rmsf(L, rstd=NULL) == EINVAL
+    assert _rmsf(L, eps=-1.0) == EINVAL
+    assert _rmsf(L, R=0) == OK                   # nothing to do
+    assert _lnf(L, dtype=3) == EDTYPE
+    assert _lnf(L, bias=A16) == EINVAL           # bias without residual
+    assert _lnf(L, mask=A16) == EINVAL           # mask without residual
+    assert _lnf(L, z=A16) == EINVAL              # z output without residual
+    assert _lnf(L, mean=NULL) == EINVAL
+    assert _lnf(L, y=NULL) == EINVAL
+    assert _lnf(L, residual=A16, scale=float("nan")) == EINVAL
+    assert _lnf(L, eps=float("nan")) == EINVAL
+
+
 @pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="host without GPU only")
 def test_valid_call_without_gpu_reports_cuda_error(gbn):
     L = gbn.lib()
     assert _fwd(L) == ECUDA
     assert _rms(L) == ECUDA
+    assert _rmsf(L) == ECUDA
+    assert _lnf(L, residual=A16, bias=A16, mask=A16, z=A16) == ECUDA
     assert L.gbn_init(-1) == ECUDA

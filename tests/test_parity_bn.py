@@ -123,6 +123,16 @@ def test_bn_bit_deterministic(gbn, name):
         assert torch.equal(a[k], b[k]), f"{k} differs between two runs"
 
 
+def test_bn_many_channels(gbn):
+    """3000 channels of 64 elements per plane: every CTA of the single-launch
+    kernel spans ~20 channel segments (one per-segment reduction, partial and
+    finalize each)."""
+    case = synth.BNCase("bn_wide_f32", (64, 3000, 8, 8), "f32", mu_range=(-50.0, 50.0),
+                        seed=97)
+    inp = synth.bn_inputs(case)
+    compare(run_gpu(gbn, inp), run_oracle(inp), case.dtype, what="bn 3000 channels")
+
+
 def test_bn_bf16_bit_deterministic(gbn):
     case = synth.BNCase("det_bf16", (32, 64, 28, 28), "bf16", mu_range=(-100, 100),
                         sigma_range=(0.01, 10), seed=99)

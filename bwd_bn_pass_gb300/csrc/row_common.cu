@@ -108,12 +108,13 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
     if (kv * VE > max_cols || kv > 4 || (kind != GBN_ROW_RMS && kv > 2)) fast = false;
     // (rows per stage, blocks per SM) in order of preference; these match
     // the compiled kernel instances.
-    int cand[2][2];
+    int cand[3][2];
     int ncand = 0;
     if (kind == GBN_ROW_RMS) {
       cand[ncand][0] = kv == 1 ? 2 : 1;
       cand[ncand++][1] = kv <= 2 ? 2 : 1;
     } else if (kv == 1 && threads <= 256) {
+      cand[ncand][0] = 4, cand[ncand++][1] = 2;
       cand[ncand][0] = 2, cand[ncand++][1] = 3;
     } else if (kv == 1) {
       cand[ncand][0] = 1, cand[ncand++][1] = 1;

@@ -28,6 +28,7 @@ from .layernorm import (
     fused_bias_dropout_add_layer_norm_forward,
     layer_norm_backward,
     fused_bias_dropout_add_layer_norm_backward,
+    layer_norm_backward_saved_z,
 )
 
 __all__ = [
@@ -43,4 +44,5 @@ __all__ = [
     "fused_bias_dropout_add_layer_norm_forward",
     "layer_norm_backward",
     "fused_bias_dropout_add_layer_norm_backward",
+    "layer_norm_backward_saved_z",
 ]

@@ -135,3 +135,18 @@ def fused_bias_dropout_add_layer_norm_backward(dy, inp, residual, bias, mask,
     dbias = None if bias is None else dx.sum(axis=0)
     return {"dx": dx, "dresidual": dresidual, "dbias": dbias,
             "dgamma": dgamma, "dbeta": dbeta}
+
+
+def layer_norm_backward_saved_z(dy, z, mask, scale, mean, rstd, gamma, dz_extra=None,
+                                with_dbias=True):
+    """The fused backward given the saved LayerNorm input z (the
+    residual-stream output of the forward) instead of the operands that
+    produced it: the same dz, dresidual = dz, dx = dz * scale * mask and
+    dbias = sum_rows dx (nvfuser_fusion_id9 with T6 read, not recomputed).
+    mask may be None (everything kept).  Returns dict dx, dresidual, dbias
+    (None unless with_dbias), dgamma, dbeta."""
+    dz, dgamma, dbeta = _ln_core(dy, z, mean, rstd, gamma, dz_extra)
+    keep = 1.0 if mask is None else np.asarray(mask, dtype=np.float64)
+    dx = dz * float(scale) * keep
+    return {"dx": dx, "dresidual": dz, "dbias": dx.sum(axis=0) if with_dbias else None,
+            "dgamma": dgamma, "dbeta": dbeta}

@@ -436,5 +436,30 @@ def pin_ln_forward(ln):
     _close((p["y"] ** 2).mean(axis=1), var / (var + eps), what="mean y^2")
 
 
+def pin_ln_saved_z_vs_torch(ln):
+    """The saved-z backward against torch float64 autograd of
+    LayerNorm(residual + mask * s * (inp + bias)): the gradients of inp,
+    residual and bias, with z given as the value torch computed."""
+    inp, res, bias, mask, gamma, beta, dy, dzx = _ln_data(26)
+    eps, s = 1e-5, 1.0 / 0.8
+    H = inp.shape[1]
+    ti = torch.tensor(inp, requires_grad=True)
+    tr = torch.tensor(res, requires_grad=True)
+    tbias = torch.tensor(bias, requires_grad=True)
+    tg = torch.tensor(gamma, requires_grad=True)
+    z = tr + torch.tensor(mask) * s * (ti + tbias)
+    y, mu, rstd = torch.native_layer_norm(z, (H,), tg, torch.tensor(beta), eps)
+    loss = (y * torch.tensor(dy)).sum() + (z * torch.tensor(dzx)).sum()
+    loss.backward()
+    out = ln.layer_norm_backward_saved_z(dy, z.detach().numpy(), mask, s,
+                                         mu.detach().numpy().reshape(-1),
+                                         rstd.detach().numpy().reshape(-1), gamma, dz_extra=dzx)
+    _close(out["dx"], ti.grad.numpy(), what="saved-z dx")
+    _close(out["dresidual"], tr.grad.numpy(), what="saved-z dresidual")
+    _close(out["dbias"], tbias.grad.numpy(), what="saved-z dbias")
+    _close(out["dgamma"], tg.grad.numpy(), what="saved-z dgamma")
+
+
 LN_PINS = [pin_ln_plain_vs_torch, pin_ln_fused_vs_torch,
-           pin_ln_finite_differences, pin_ln_invariants, pin_ln_forward]
+           pin_ln_finite_differences, pin_ln_invariants, pin_ln_forward,
+           pin_ln_saved_z_vs_torch]

@@ -62,6 +62,9 @@ MUTATIONS = [
      "y = centred * rstd[:, None] * g[None, :]"),
     (oln, pins.LN_PINS, "return mu, 1.0 / np.sqrt(var + eps)", "return mu, 1.0 / np.sqrt(var)"),
     (oln, pins.LN_PINS, "var = (c * c).mean(axis=1)", "var = (c * c).sum(axis=1) / (z.shape[1] - 1)"),
+    (oln, pins.LN_PINS, "    dx = dz * float(scale) * keep\n", "    dx = dz * keep\n"),
+    (oln, pins.LN_PINS, '"dbias": dx.sum(axis=0) if with_dbias else None',
+     '"dbias": dz.sum(axis=0) if with_dbias else None'),
 ]
 
 

@@ -368,15 +368,18 @@ int gbn_rmsnorm_backward(const void* dy, const void* x, const void* w, int dtype
                               static_cast<cudaStream_t>(stream)));
 }
 
-int gbn_layernorm_backward(const void* dy, const void* x_or_input, int dtype, const float* mean,
-                           const float* rstd, const void* gamma, int64_t R, int64_t H,
-                           const void* residual, const void* bias, const uint8_t* mask,
-                           float dropout_scale, const float* dz_extra, void* dx,
-                           void* dresidual, void* dgamma, void* dbeta, void* dbias, void* ws,
-                           size_t ws_bytes, void* stream) {
+int gbn_layernorm_backward_ex(const void* dy, const void* x_or_input, int dtype,
+                              const float* mean, const float* rstd, const void* gamma, int64_t R,
+                              int64_t H, const void* residual, const void* bias,
+                              const uint8_t* mask, float dropout_scale, const float* dz_extra,
+                              void* dx, void* dresidual, void* dgamma, void* dbeta, void* dbias,
+                              void* ws, size_t ws_bytes, int flags, void* stream) {
   int rc = row_check(dtype, R, H);
   if (rc != GBN_OK) return rc;
-  const bool fused = residual != nullptr;
+  if (flags & ~(GBN_LN_SAVED_Z | GBN_LN_DRES_F32)) return GBN_EINVAL;
+  const bool saved_z = (flags & GBN_LN_SAVED_Z) != 0;
+  if (saved_z && (residual || bias)) return GBN_EINVAL;  // z already holds them
+  const bool fused = residual != nullptr || saved_z;
   if (!fused && (bias || mask || dresidual || dbias)) return GBN_EINVAL;
   if (H == 0) return GBN_OK;
   if (gamma == nullptr || ws == nullptr) return GBN_EINVAL;
@@ -411,8 +414,21 @@ int gbn_layernorm_backward(const void* dy, const void* x_or_input, int dtype, co
   q.dgamma = dgamma;
   q.dbeta = dbeta;
   q.dbias = dbias;
+  q.saved_z = saved_z;
+  q.dres_f32 = (flags & GBN_LN_DRES_F32) != 0 && dtype != GBN_F32;
   return to_status(ln_launch(p, q, static_cast<float*>(ws), dev->status,
                              static_cast<cudaStream_t>(stream)));
+}
+
+int gbn_layernorm_backward(const void* dy, const void* x_or_input, int dtype, const float* mean,
+                           const float* rstd, const void* gamma, int64_t R, int64_t H,
+                           const void* residual, const void* bias, const uint8_t* mask,
+                           float dropout_scale, const float* dz_extra, void* dx,
+                           void* dresidual, void* dgamma, void* dbeta, void* dbias, void* ws,
+                           size_t ws_bytes, void* stream) {
+  return gbn_layernorm_backward_ex(dy, x_or_input, dtype, mean, rstd, gamma, R, H, residual,
+                                   bias, mask, dropout_scale, dz_extra, dx, dresidual, dgamma,
+                                   dbeta, dbias, ws, ws_bytes, 0, stream);
 }
 
 // ------------------------------------------------------ row-wise forward --

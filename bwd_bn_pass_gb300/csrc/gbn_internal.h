@@ -167,6 +167,8 @@ struct LnPtrs {
   void* dgamma = nullptr;
   void* dbeta = nullptr;
   void* dbias = nullptr;
+  bool saved_z = false;   // x is the saved LayerNorm input z (fused outputs, no residual)
+  bool dres_f32 = false;  // dres is fp32
 };
 
 // Plans the launch.  `fast_ok` says whether pointers/shape allow the

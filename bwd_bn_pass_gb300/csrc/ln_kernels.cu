@@ -47,6 +47,8 @@ struct LnArgs {
   int32_t Hv;
   int32_t nstage;
   int32_t nplanes;
+  int32_t zin;       // fused outputs from a saved z (x is z; no residual / bias)
+  int32_t dres_f32;  // dresidual written as fp32
   uint32_t stage_bytes;
   uint32_t off_dy, off_x, off_res, off_mask;
 };
@@ -156,10 +158,11 @@ __global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
     const uint32_t bt = (uint32_t)nr * rowb;
     const uint32_t bm = (uint32_t)(nr * H);
     unsigned char* st = data + (size_t)s * a.stage_bytes;
-    mbar_arrive_expect_tx(&bar[s], bt * (FUSED ? 3u : 2u) + (has_mask ? bm : 0u));
+    const bool with_res = FUSED && !a.zin;
+    mbar_arrive_expect_tx(&bar[s], bt * (with_res ? 3u : 2u) + (has_mask ? bm : 0u));
     bulk_g2s(st + a.off_dy, static_cast<const char*>(a.dy) + r0 * rowb, bt, &bar[s]);
     bulk_g2s(st + a.off_x, static_cast<const char*>(a.x) + r0 * rowb, bt, &bar[s]);
-    if (FUSED) bulk_g2s(st + a.off_res, static_cast<const char*>(a.res) + r0 * rowb, bt, &bar[s]);
+    if (with_res) bulk_g2s(st + a.off_res, static_cast<const char*>(a.res) + r0 * rowb, bt, &bar[s]);
     if (has_mask) bulk_g2s(st + a.off_mask, a.mask + r0 * H, bm, &bar[s]);
   };
 
@@ -212,7 +215,7 @@ __global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
     PK::get(*reinterpret_cast<const uint4*>(st + a.off_x + o), x2);
     if constexpr (FUSED) {
       f2 r2[NP];
-      PK::get(*reinterpret_cast<const uint4*>(st + a.off_res + o), r2);
+      if (!a.zin) PK::get(*reinterpret_cast<const uint4*>(st + a.off_res + o), r2);
       uint2 m = make_uint2(0x01010101u, 0x01010101u);
       if (has_mask) {
         const unsigned char* mp = st + a.off_mask + (size_t)rr * H + (size_t)vi * VE;
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         keep2[p] = keep_pair(m, p, a.scale);
-        z2[p] = f2_fma(keep2[p], f2_add(x2[p], bia2[k][p]), r2[p]);
+        z2[p] = a.zin ? x2[p] : f2_fma(keep2[p], f2_add(x2[p], bia2[k][p]), r2[p]);
       }
     } else {
 #pragma unroll
@@ -243,13 +246,13 @@ __global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
     Vec16<T>::load(st + a.off_x + o, xv);
     if constexpr (FUSED) {
       float rv[VE];
-      Vec16<T>::load(st + a.off_res + o, rv);
+      if (!a.zin) Vec16<T>::load(st + a.off_res + o, rv);
       const uint32_t mk =
           has_mask ? mask_bits<VE>(st + a.off_mask + (size_t)rr * H + (size_t)vi * VE) : 0xffu;
 #pragma unroll
       for (int e = 0; e < VE; ++e) {
         keep[e] = ((mk >> e) & 1u) ? a.scale : 0.f;
-        z[e] = ln_z<FUSED, COMP>(xv[e], rv[e], bia[k][e], keep[e]);
+        z[e] = a.zin ? DF{xv[e], 0.f} : ln_z<FUSED, COMP>(xv[e], rv[e], bia[k][e], keep[e]);
       }
     } else {
 #pragma unroll
@@ -379,8 +382,18 @@ __global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
             if (FUSED) sg_x[k][p] = f2_add(sg_x[k][p], dx2[p]);
           }
           *reinterpret_cast<uint4*>(static_cast<T*>(a.dx) + go) = PK::put(dx2);
-          if (FUSED && a.dres != nullptr)
-            *reinterpret_cast<uint4*>(static_cast<T*>(a.dres) + go) = PK::put(dz2);
+          if (FUSED && a.dres != nullptr) {
+            if (a.dres_f32) {
+              float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.dres) + go);
+#pragma unroll
+              for (int p = 0; p < NP; p += 2) {
+                const float2 u = f2_unpack(dz2[p]), w = f2_unpack(dz2[p + 1]);
+                d4[p / 2] = make_float4(u.x, u.y, w.x, w.y);
+              }
+            } else {
+              *reinterpret_cast<uint4*>(static_cast<T*>(a.dres) + go) = PK::put(dz2);
+            }
+          }
         }
       }
     }
@@ -465,6 +478,7 @@ __global__ void __launch_bounds__(256) ln_bwd_generic_kernel(LnArgs a) {
     keep = 1.f;
     if constexpr (FUSED) {
       keep = (a.mask == nullptr || a.mask[r * H + j] != 0) ? a.scale : 0.f;
+      if (a.zin) return z;
       const float b = bias ? to_f32(bias[j]) : 0.f;
       const float rv = to_f32(res[r * H + j]);
       if constexpr (COMP) {
@@ -536,7 +550,10 @@ __global__ void __launch_bounds__(256) ln_bwd_generic_kernel(LnArgs a) {
         const float dz = fmaf(rho, dyy * gm - mg - xh * mgx, zx);
         const float dxv = FUSED ? dz * keep : dz;
         static_cast<T*>(a.dx)[r * H + j] = from_f32<T>(dxv);
-        if (FUSED && a.dres != nullptr) static_cast<T*>(a.dres)[r * H + j] = from_f32<T>(dz);
+        if (FUSED && a.dres != nullptr) {
+          if (a.dres_f32) static_cast<float*>(a.dres)[r * H + j] = dz;
+          else static_cast<T*>(a.dres)[r * H + j] = from_f32<T>(dz);
+        }
         P(0, 0)[j] = fmaf(dyy, xh, P(0, 0)[j]);
         acc_add(1, j, dyy);
         if (FUSED) acc_add(2, j, dxv);
@@ -621,6 +638,8 @@ cudaError_t ln_launch(const RowPlan& p, const LnPtrs& q, float* part, int* statu
     a.Hv = (int32_t)(p.H * (p.dtype == GBN_F32 ? 4 : 2) / 16);
     a.nstage = p.nstage;
     a.nplanes = p.nplanes;
+    a.zin = q.saved_z ? 1 : 0;
+    a.dres_f32 = q.dres_f32 ? 1 : 0;
     a.stage_bytes = p.stage_bytes;
     a.off_dy = p.off[0];
     a.off_x = p.off[1];

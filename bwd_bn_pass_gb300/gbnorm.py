@@ -69,6 +69,8 @@ _SIGNATURES = {
     "gbn_rmsnorm_backward": (_INT, [_P, _P, _P, _INT, _P, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "gbn_layernorm_backward": (_INT, [_P, _P, _INT, _P, _P, _P, _I64, _I64, _P, _P, _P, _F,
                                       _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "gbn_layernorm_backward_ex": (_INT, [_P, _P, _INT, _P, _P, _P, _I64, _I64, _P, _P, _P, _F,
+                                         _P, _P, _P, _P, _P, _P, _P, _SZ, _INT, _P]),
     "gbn_rmsnorm_forward": (_INT, [_P, _P, _INT, _I64, _I64, _F, _P, _P, _P]),
     "gbn_layernorm_forward": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _F, _P, _P, _F, _P, _P,
                                      _P, _P, _P]),
@@ -349,14 +351,22 @@ def rmsnorm_backward(dy, x, w, rstd, *, dx=None, dw=None, ws=None):
     return dx, dw
 
 
+GBN_LN_SAVED_Z = 1
+GBN_LN_DRES_F32 = 2
+
+
 def layernorm_backward(dy, x, mean, rstd, gamma, *, residual=None, bias=None, mask=None,
                        dropout_scale=1.0, dz_extra=None, dx=None, dresidual=None, dgamma=None,
-                       dbeta=None, dbias=None, ws=None, want_dresidual=True, want_dbias=True):
+                       dbeta=None, dbias=None, ws=None, want_dresidual=True, want_dbias=True,
+                       saved_z=False, dres_f32=False):
     """LayerNorm backward; fused with bias+dropout+add when ``residual`` is
-    given (then ``x`` is the dropout input).  Returns a dict with dx,
+    given (then ``x`` is the dropout input), or from the saved LayerNorm
+    input when ``saved_z`` (then ``x`` is z, there is no residual or bias, and
+    the mask / dropout_scale still give dx, dresidual and dbias).
+    ``dres_f32`` writes dresidual in fp32.  Returns a dict with dx,
     dresidual, dgamma, dbeta, dbias (None where not computed)."""
     R, H = _rows(x, "x")
-    fused = residual is not None
+    fused = residual is not None or saved_z
     for name, t in (("dy", dy), ("mean", mean), ("rstd", rstd), ("gamma", gamma)):
         _cuda(t, name)
     if dy.shape != x.shape or dy.dtype != x.dtype or gamma.dtype != x.dtype:
@@ -373,10 +383,11 @@ def layernorm_backward(dy, x, mean, rstd, gamma, *, residual=None, bias=None, ma
         raise TypeError("dz_extra must be float32")
     dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx")
     if fused:
-        _cuda(residual, "residual")
+        if residual is not None:
+            _cuda(residual, "residual")
         if dresidual is None and want_dresidual:
-            dresidual = torch.empty_like(x)
-        if dbias is None and want_dbias and bias is not None:
+            dresidual = torch.empty_like(x, dtype=torch.float32 if dres_f32 else x.dtype)
+        if dbias is None and want_dbias and (bias is not None or saved_z):
             dbias = torch.empty_like(gamma)
     dgamma = torch.empty_like(gamma) if dgamma is None else dgamma
     dbeta = torch.empty_like(gamma) if dbeta is None else dbeta
@@ -387,12 +398,13 @@ def layernorm_backward(dy, x, mean, rstd, gamma, *, residual=None, bias=None, ma
                  ("dx", dx), ("dresidual", dresidual), ("dgamma", dgamma), ("dbeta", dbeta),
                  ("dbias", dbias), ("ws", ws))
     with torch.cuda.device(x.device):
-        st = lib().gbn_layernorm_backward(
+        flags = (GBN_LN_SAVED_Z if saved_z else 0) | (GBN_LN_DRES_F32 if dres_f32 else 0)
+        st = lib().gbn_layernorm_backward_ex(
             _ptr(dy), _ptr(x), _code(x.dtype), _ptr(mean), _ptr(rstd), _ptr(gamma), R, H,
             _ptr(residual), _ptr(bias), _ptr(mask), float(dropout_scale), _ptr(dz_extra),
             _ptr(dx), _ptr(dresidual), _ptr(dgamma), _ptr(dbeta), _ptr(dbias), _ptr(ws),
-            ws.numel() * ws.element_size(), _stream(x.device))
-    _check("gbn_layernorm_backward", st)
+            ws.numel() * ws.element_size(), flags, _stream(x.device))
+    _check("gbn_layernorm_backward_ex", st)
     return {"dx": dx, "dresidual": dresidual, "dgamma": dgamma, "dbeta": dbeta,
             "dbias": dbias}
 

@@ -262,6 +262,29 @@ GBN_API int gbn_layernorm_backward(const void* dy, const void* x_or_input, int d
                            void* dgamma, void* dbeta, void* dbias, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* Flags of gbn_layernorm_backward_ex.                                       */
+#define GBN_LN_SAVED_Z  1  /* x_or_input is the saved LayerNorm input z        */
+#define GBN_LN_DRES_F32 2  /* dresidual is written as fp32 (T77 of [P2])       */
+
+/* gbn_layernorm_backward with variants ([P2] nvfuser_fusion_id9, where the
+ * LayerNorm input T6 and the residual gradient T77 are fp32):
+ *   GBN_LN_SAVED_Z: x_or_input is z itself (e.g. the z written by
+ *     gbn_layernorm_forward) instead of the dropout input; residual and bias
+ *     must be NULL.  The fused outputs are still produced from mask and
+ *     dropout_scale: dresidual = dz (+ dz_extra), dx = dresidual*scale*mask,
+ *     dbias = sum_rows dx (each may be NULL).
+ *   GBN_LN_DRES_F32: dresidual is an fp32 [R, H] tensor (no effect when
+ *     dtype is already GBN_F32).
+ * Unknown flag bits return GBN_EINVAL.  flags = 0 is gbn_layernorm_backward. */
+GBN_API int gbn_layernorm_backward_ex(const void* dy, const void* x_or_input, int dtype,
+                                      const float* mean, const float* rstd,
+                                      const void* gamma, int64_t R, int64_t H,
+                                      const void* residual, const void* bias,
+                                      const uint8_t* mask, float dropout_scale,
+                                      const float* dz_extra, void* dx, void* dresidual,
+                                      void* dgamma, void* dbeta, void* dbias, void* ws,
+                                      size_t ws_bytes, int flags, void* stream);
+
 /* =========================================================================
  * Row-wise training forwards: RMSNorm ([P3]) and LayerNorm ([P2]), writing
  * the statistics the backward passes above take.  Tensors are [R, H]

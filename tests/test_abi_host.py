@@ -141,6 +141,19 @@ def _lnf(L, dtype=1, R=4, H=64, x=A16, residual=NULL, bias=NULL, mask=NULL, scal
                                    y, z, mean, rstd, NULL)
 
 
+def test_layernorm_backward_flag_errors(gbn):
+    L = gbn.lib()
+
+    def ex(flags, residual=NULL, bias=NULL):
+        return L.gbn_layernorm_backward_ex(A16, A16, 1, A16, A16, A16, 4, 64, residual, bias,
+                                           NULL, 1.0, NULL, A16, A16, A16, A16, NULL, A16,
+                                           1 << 20, flags, NULL)
+    assert ex(4) == EINVAL                      # unknown flag bit
+    assert ex(1, residual=A16) == EINVAL        # saved z with a residual
+    assert ex(1, bias=A16) == EINVAL            # saved z with a bias
+    assert ex(2) == EINVAL                      # fp32 dresidual without a fused form
+
+
 def test_forward_argument_errors(gbn):
     L = gbn.lib()
     assert _rmsf(L, dtype=3) == EDTYPE

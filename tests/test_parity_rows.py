@@ -220,3 +220,70 @@ def test_ln_bit_deterministic(gbn):
 def test_device_status_clean(gbn):
     torch.cuda.synchronize()
     assert gbn.get_device_status() == 0
+
+
+# ------------------------------------------- LayerNorm backward variants --
+
+def saved_z_case(R, H, dtype, seed=13, with_dz_extra=False):
+    """A fused case whose LayerNorm input z is stored in `dtype` (as the
+    forward writes it) and handed to the backward instead of the operands."""
+    inp = synth.ln_inputs(synth.LNCase(f"lnz_{R}x{H}", R, H, dtype, seed=seed,
+                                       with_dz_extra=with_dz_extra))
+    z = oracle.dropout_add(_f64(inp["inp"]), _f64(inp["residual"]), _f64(inp["bias"]),
+                           _f64(inp["mask"]), inp["dropout_scale"])
+    inp["z"] = torch.tensor(z).to(inp["inp"].dtype)
+    mu, rs = oracle.layer_norm_saved_stats(_f64(inp["z"]), inp["eps"])
+    inp["mean"] = torch.tensor(mu, dtype=torch.float32)
+    inp["rstd"] = torch.tensor(rs, dtype=torch.float32)
+    return inp
+
+
+def saved_z_gpu(gbn, inp, dres_f32=False):
+    d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    out = gbn.layernorm_backward(d["dy"], d["z"], d["mean"], d["rstd"], d["gamma"],
+                                 mask=d["mask"], dropout_scale=inp["dropout_scale"],
+                                 dz_extra=d["dz_extra"], saved_z=True, dres_f32=dres_f32)
+    torch.cuda.synchronize()
+    return {k: (None if v is None else v.cpu()) for k, v in out.items()}
+
+
+def saved_z_ref(inp):
+    return oracle.layer_norm_backward_saved_z(
+        _f64(inp["dy"]), _f64(inp["z"]), _f64(inp["mask"]), inp["dropout_scale"],
+        _f64(inp["mean"]), _f64(inp["rstd"]), _f64(inp["gamma"]), dz_extra=_f64(inp["dz_extra"]))
+
+
+@pytest.mark.parametrize("R,H,dtype", [(8192, 1600, "bf16"), (129, 1024, "f32"),
+                                       (23, 1000, "bf16"), (7, 5000, "f32")])
+def test_ln_backward_from_saved_z(gbn, R, H, dtype):
+    """The fused outputs from the saved z match the oracle (bulk-copy path for
+    the aligned shapes, the generic kernel for H % 16 != 0 or wide rows)."""
+    inp = saved_z_case(R, H, dtype)
+    ln_compare(saved_z_gpu(gbn, inp), saved_z_ref(inp), dtype, f"saved z {R}x{H}")
+
+
+def test_ln_backward_saved_z_with_dz_extra_and_fp32_dresidual(gbn):
+    inp = saved_z_case(96, 1600, "bf16", with_dz_extra=True)
+    got = saved_z_gpu(gbn, inp, dres_f32=True)
+    ref = saved_z_ref(inp)
+    assert got["dresidual"].dtype == torch.float32
+    tol.check_f32(got["dresidual"], ref["dresidual"], "saved z fp32 dresidual")
+    for k in ("dx", "dbias", "dgamma", "dbeta"):
+        _check(got[k], ref[k], "bf16", f"saved z {k}")
+
+
+@pytest.mark.parametrize("R,H", [(256, 1600), (23, 1000)])
+def test_ln_fused_backward_fp32_dresidual(gbn, R, H):
+    """dresidual in fp32 (the page's T77) from bf16 operands, on the bulk-copy
+    and the generic kernel; the other outputs are unchanged."""
+    inp = ln_case(R, H, "bf16")
+    d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in inp.items()}
+    out = gbn.layernorm_backward(d["dy"], d["inp"], d["mean"], d["rstd"], d["gamma"],
+                                 residual=d["residual"], bias=d["bias"], mask=d["mask"],
+                                 dropout_scale=inp["dropout_scale"], dres_f32=True)
+    torch.cuda.synchronize()
+    ref = ln_ref(inp)
+    assert out["dresidual"].dtype == torch.float32
+    tol.check_f32(out["dresidual"].cpu(), ref["dresidual"], "fp32 dresidual")
+    for k in ("dx", "dbias", "dgamma", "dbeta"):
+        _check(out[k].cpu(), ref[k], "bf16", f"fp32-dres run {k}")

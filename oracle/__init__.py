@@ -19,6 +19,8 @@ from .bn import (
     batch_norm_forward_train,
     batch_norm_apply,
     batch_norm_backward,
+    batch_norm_act_forward_train,
+    batch_norm_act_backward,
 )
 from .rmsnorm import rms_norm_rstd, rms_norm_forward, rms_norm_backward
 from .layernorm import (
@@ -35,6 +37,8 @@ __all__ = [
     "batch_norm_forward_train",
     "batch_norm_apply",
     "batch_norm_backward",
+    "batch_norm_act_forward_train",
+    "batch_norm_act_backward",
     "rms_norm_rstd",
     "rms_norm_forward",
     "rms_norm_backward",

@@ -26,6 +26,12 @@ Readings where the pages are silent
   compares it with "the float64 variance of the same data".
 * running_var takes the unbiased ``var * M / (M - 1)``; momentum follows
   ``new = (1 - m) * old + m * batch`` (the PyTorch BatchNorm2d convention).
+* Fusing ReLU / LeakyReLU into BatchNorm is the page's "Part 2" (section
+  "Context"; "Follow-ups": ReLU costs more per step than the BatchNorm
+  forward).  The page gives no definition beyond the names, so the reading
+  here is the composition: y = act(pre) with pre the BatchNorm output, and
+  the backward gates dy by d act / d pre -- 1 where pre > 0, else 0 (ReLU)
+  or the negative slope (LeakyReLU) -- before the BatchNorm backward.
 """
 
 import numpy as np
@@ -118,3 +124,48 @@ def batch_norm_backward(x, dy, gamma, eps):
         "k1": k1,
         "k2": k2,
     }
+
+
+ACT_NONE, ACT_RELU, ACT_LEAKY_RELU = 0, 1, 2
+
+
+def activation(pre, act, slope=0.0):
+    """ReLU max(pre, 0), LeakyReLU (pre if pre > 0 else slope * pre), or pre."""
+    pre = np.asarray(pre, dtype=np.float64)
+    if act == ACT_RELU:
+        return np.where(pre > 0, pre, 0.0)
+    if act == ACT_LEAKY_RELU:
+        return np.where(pre > 0, pre, float(slope) * pre)
+    return pre
+
+
+def activation_gate(pre, act, slope=0.0):
+    """d act / d pre: 1 where pre > 0, else 0 (ReLU) or slope (LeakyReLU)."""
+    pre = np.asarray(pre, dtype=np.float64)
+    if act == ACT_RELU:
+        return np.where(pre > 0, 1.0, 0.0)
+    if act == ACT_LEAKY_RELU:
+        return np.where(pre > 0, 1.0, float(slope))
+    return np.ones_like(pre)
+
+
+def batch_norm_act_forward_train(x, gamma, beta, running_mean, running_var, momentum, eps, act,
+                                 slope=0.0):
+    """Training forward of act(BatchNorm(x)).  The dict of
+    batch_norm_forward_train with y = act(pre) and pre = the BatchNorm output."""
+    out = batch_norm_forward_train(x, gamma, beta, running_mean, running_var, momentum, eps)
+    out["pre"] = out["y"]
+    out["y"] = activation(out["pre"], act, slope)
+    return out
+
+
+def batch_norm_act_backward(x, dy, gamma, beta, eps, act, slope=0.0):
+    """Backward of act(BatchNorm(x)) given the forward's input: pre is
+    recomputed from x, dy is gated by d act / d pre, then the BatchNorm
+    backward.  Returns the dict of batch_norm_backward plus pre."""
+    C = np.asarray(gamma).shape[0]
+    pre = batch_norm_forward_train(x, gamma, beta, np.zeros(C), np.ones(C), 0.0, eps)["y"]
+    gated = np.asarray(dy, dtype=np.float64) * activation_gate(pre, act, slope)
+    out = batch_norm_backward(x, gated, gamma, eps)
+    out["pre"] = pre
+    return out

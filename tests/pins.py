@@ -193,9 +193,30 @@ def pin_bn_exact_rational(bn):
     _close(b["dgamma"], [dgamma], rtol=1e-13, what="exact dgamma")
 
 
+def pin_bn_act_vs_torch(bn):
+    """act(BatchNorm) forward and backward against torch float64 autograd of
+    F.relu / F.leaky_relu(F.batch_norm(...))."""
+    x, gamma, beta, dy, rm, rv = _bn_data(31, offset=20.0)
+    beta = beta + np.linspace(-0.8, 0.8, beta.size)  # both signs of pre in every channel
+    eps = 1e-5
+    for act, slope, fn in ((bn.ACT_RELU, 0.0, lambda t: F.relu(t)),
+                           (bn.ACT_LEAKY_RELU, 0.1, lambda t: F.leaky_relu(t, 0.1))):
+        tx = torch.tensor(x, requires_grad=True)
+        tg = torch.tensor(gamma, requires_grad=True)
+        tb = torch.tensor(beta, requires_grad=True)
+        y = fn(F.batch_norm(tx, None, None, tg, tb, training=True, eps=eps))
+        y.backward(torch.tensor(dy))
+        f = bn.batch_norm_act_forward_train(x, gamma, beta, rm, rv, 0.1, eps, act, slope)
+        _close(f["y"], y.detach().numpy(), what=f"act {act} y")
+        b = bn.batch_norm_act_backward(x, dy, gamma, beta, eps, act, slope)
+        _close(b["dx"], tx.grad.numpy(), what=f"act {act} dx")
+        _close(b["dgamma"], tg.grad.numpy(), what=f"act {act} dgamma")
+        _close(b["dbeta"], tb.grad.numpy(), what=f"act {act} dbeta")
+
+
 BN_PINS = [pin_bn_forward_vs_torch, pin_bn_backward_vs_torch,
            pin_bn_finite_differences, pin_bn_invariants, pin_bn_running_ema,
-           pin_bn_exact_rational]
+           pin_bn_exact_rational, pin_bn_act_vs_torch]
 
 
 # ------------------------------------------------------------------ RMSNorm

@@ -33,6 +33,12 @@ MUTATIONS = [
      "dx = dy3 * _channel(gamma) + centred * _channel(k1)"),
     (obn, pins.BN_PINS, "new_rm = (1.0 - m) * np.asarray(running_mean, np.float64) + m * mean",
      "new_rm = m * np.asarray(running_mean, np.float64) + (1.0 - m) * mean"),
+    (obn, pins.BN_PINS, "return np.where(pre > 0, 1.0, float(slope))",
+     "return np.where(pre > 0, 1.0, 0.0)"),
+    (obn, pins.BN_PINS, "gated = np.asarray(dy, dtype=np.float64) * activation_gate(pre, act, slope)",
+     "gated = np.asarray(dy, dtype=np.float64)"),
+    (obn, pins.BN_PINS, "return np.where(pre > 0, pre, float(slope) * pre)",
+     "return np.where(pre > 0, pre, 0.0)"),
     # RMSNorm
     (orms, pins.RMS_PINS, "x * (rstd3 * row_sum / H)", "x * (rstd3 * row_sum)"),
     (orms, pins.RMS_PINS, "rstd3 = rstd * rstd * rstd", "rstd3 = rstd * rstd"),

@@ -164,6 +164,12 @@ static int bn_prepare(int dtype, int64_t B, int64_t C, int64_t HW, bool training
 
 static bool bn_empty(int64_t B, int64_t C, int64_t HW) { return C == 0 || B == 0 || HW == 0; }
 
+// act one of GBN_ACT_*; LeakyReLU's slope finite.
+static bool act_ok(int act, float slope) {
+  if (act == GBN_ACT_NONE || act == GBN_ACT_RELU) return true;
+  return act == GBN_ACT_LEAKY_RELU && slope - slope == 0.f;
+}
+
 int gbn_bn_stats(const void* x, int dtype, int64_t B, int64_t C, int64_t HW, void* ws,
                  size_t ws_bytes, void* stream) {
   int64_t M;
@@ -184,10 +190,12 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
                                   const float* gamma, const float* beta, float* running_mean,
                                   float* running_var, float momentum, float eps, void* y,
                                   float* stats, const void* ws, size_t ws_bytes, void* stream,
-                                  bool with_stats_pass, bool partials_only = false) {
+                                  bool with_stats_pass, bool partials_only = false,
+                                  int act = GBN_ACT_NONE, float slope = 0.f) {
   int64_t M;
   int rc = bn_check(dtype, B, C, HW, true, &M);
   if (rc != GBN_OK) return rc;
+  if (!act_ok(act, slope)) return GBN_EINVAL;
   if (C == 0) return GBN_OK;
   if (x == nullptr || y == nullptr || stats == nullptr || ws == nullptr) return GBN_EINVAL;
   if (!aligned(stats, 8)) return GBN_EALIGN;
@@ -203,15 +211,15 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
   if (with_stats_pass && aligned(x, 16) && aligned(y, 16) &&
       bn_fused_plan(dtype, false, B, C, HW, *dev, &fp) && ws_bytes >= fp.ws_bytes)
     return to_status(bn_fused_forward(fp, dtype, x, y, gamma, beta, stats, running_mean,
-                                      running_var, momentum, eps, const_cast<void*>(ws),
-                                      dev->status, st));
+                                      running_var, momentum, eps, act, slope,
+                                      const_cast<void*>(ws), dev->status, st));
   if (with_stats_pass) {
     cudaError_t e = bn_launch_stats(x, dtype, p, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;
   }
   return to_status(bn_launch_apply(x, y, dtype, p, kApplyTrain, part, gamma, beta, stats,
-                                   running_mean, running_var, momentum, eps, nullptr, nullptr, st,
-                                   /*pdl=*/true));
+                                   running_mean, running_var, momentum, eps, nullptr, nullptr, act,
+                                   slope, st, /*pdl=*/true));
 }
 
 }  // extern "C"
@@ -255,12 +263,22 @@ int gbn_bn_finalize_apply(const void* x, int dtype, int64_t B, int64_t C, int64_
                                 momentum, eps, y, stats, ws, ws_bytes, stream, false);
 }
 
-int gbn_bn_apply(const void* x, int dtype, int64_t B, int64_t C, int64_t HW, const float* stats,
-                 const float* mean, const float* scale, const float* beta, void* y,
-                 void* stream) {
+int gbn_bn_forward_train_act(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                             const float* gamma, const float* beta, float* running_mean,
+                             float* running_var, float momentum, float eps, int act, float slope,
+                             void* y, float* stats, void* ws, size_t ws_bytes, void* stream) {
+  return bn_finalize_apply_impl(x, dtype, B, C, HW, gamma, beta, running_mean, running_var,
+                                momentum, eps, y, stats, ws, ws_bytes, stream, true, false, act,
+                                slope);
+}
+
+static int bn_apply_impl(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                         const float* stats, const float* mean, const float* scale,
+                         const float* beta, int act, float slope, void* y, void* stream) {
   int64_t M;
   int rc = bn_check(dtype, B, C, HW, false, &M);
   if (rc != GBN_OK) return rc;
+  if (!act_ok(act, slope)) return GBN_EINVAL;
   if (bn_empty(B, C, HW)) return GBN_OK;
   if (x == nullptr || y == nullptr) return GBN_EINVAL;
   if (stats == nullptr && (mean == nullptr || scale == nullptr)) return GBN_EINVAL;
@@ -272,17 +290,32 @@ int gbn_bn_apply(const void* x, int dtype, int64_t B, int64_t C, int64_t HW, con
   if (rc != GBN_OK) return rc;
   return to_status(bn_launch_apply(x, y, dtype, p, stats ? kApplyStats : kApplyInfer, nullptr,
                                    nullptr, beta, const_cast<float*>(stats), nullptr, nullptr,
-                                   0.f, 0.f, mean, scale, static_cast<cudaStream_t>(stream),
-                                   /*pdl=*/false));
+                                   0.f, 0.f, mean, scale, act, slope,
+                                   static_cast<cudaStream_t>(stream), /*pdl=*/false));
+}
+
+int gbn_bn_apply(const void* x, int dtype, int64_t B, int64_t C, int64_t HW, const float* stats,
+                 const float* mean, const float* scale, const float* beta, void* y,
+                 void* stream) {
+  return bn_apply_impl(x, dtype, B, C, HW, stats, mean, scale, beta, GBN_ACT_NONE, 0.f, y,
+                       stream);
+}
+
+int gbn_bn_apply_act(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                     const float* stats, const float* mean, const float* scale, const float* beta,
+                     int act, float slope, void* y, void* stream) {
+  return bn_apply_impl(x, dtype, B, C, HW, stats, mean, scale, beta, act, slope, y, stream);
 }
 
 static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B, int64_t C,
                             int64_t HW, const float* stats, void* dx, float* grads,
                             const void* ws, size_t ws_bytes, void* stream, bool sums,
-                            bool finalize) {
+                            bool finalize, const float* beta = nullptr, int act = GBN_ACT_NONE,
+                            float slope = 0.f) {
   int64_t M;
   int rc = bn_check(dtype, B, C, HW, true, &M);
   if (rc != GBN_OK) return rc;
+  if (!act_ok(act, slope)) return GBN_EINVAL;
   if (C == 0) return GBN_OK;
   if (x == nullptr || dy == nullptr || stats == nullptr || ws == nullptr) return GBN_EINVAL;
   if (finalize && (dx == nullptr || grads == nullptr)) return GBN_EINVAL;
@@ -297,14 +330,15 @@ static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B,
   BnFusedPlan fp;
   if (sums && finalize && aligned(x, 16) && aligned(dy, 16) && aligned(dx, 16) &&
       bn_fused_plan(dtype, true, B, C, HW, *dev, &fp) && ws_bytes >= fp.ws_bytes)
-    return to_status(bn_fused_backward(fp, dtype, x, dy, dx, stats, grads, const_cast<void*>(ws),
-                                       dev->status, st));
+    return to_status(bn_fused_backward(fp, dtype, x, dy, dx, stats, beta, act, slope, grads,
+                                       const_cast<void*>(ws), dev->status, st));
   if (sums) {
-    cudaError_t e = bn_launch_grad_sums(x, dy, dtype, p, stats, part, st);
+    cudaError_t e = bn_launch_grad_sums(x, dy, dtype, p, stats, part, beta, act, slope, st);
     if (e != cudaSuccess) return GBN_ECUDA;
   }
   if (finalize)
-    return to_status(bn_launch_dx(x, dy, dx, dtype, p, stats, part, grads, st, /*pdl=*/true));
+    return to_status(bn_launch_dx(x, dy, dx, dtype, p, stats, part, grads, beta, act, slope, st,
+                                  /*pdl=*/true));
   return GBN_OK;
 }
 
@@ -313,6 +347,13 @@ int gbn_bn_backward(const void* x, const void* dy, int dtype, int64_t B, int64_t
                     void* stream) {
   return bn_backward_impl(x, dy, dtype, B, C, HW, stats, dx, grads, ws, ws_bytes, stream, true,
                           true);
+}
+
+int gbn_bn_backward_act(const void* x, const void* dy, int dtype, int64_t B, int64_t C,
+                        int64_t HW, const float* stats, const float* beta, int act, float slope,
+                        void* dx, float* grads, void* ws, size_t ws_bytes, void* stream) {
+  return bn_backward_impl(x, dy, dtype, B, C, HW, stats, dx, grads, ws, ws_bytes, stream, true,
+                          true, beta, act, slope);
 }
 
 int gbn_bn_grad_sums(const void* x, const void* dy, int dtype, int64_t B, int64_t C, int64_t HW,

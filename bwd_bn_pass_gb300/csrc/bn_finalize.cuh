@@ -11,6 +11,7 @@
 #pragma once
 
 #include "gbn_common.cuh"
+#include "gbnorm.h"
 
 namespace gbn {
 
@@ -77,6 +78,20 @@ __device__ __forceinline__ BnBwdFinal bn_bwd_final(DF p0, DF p1, DF md, float in
   f.k2 = -scale * f.dbeta / M;
   f.dgamma = S * inv_std;
   return f;
+}
+
+// Fused activation of the BatchNorm output pre (Aether-ML PR #18, "Part 2":
+// ReLU / LeakyReLU fused into BatchNorm): the output act(pre) and the gate
+// d act / d pre applied to the incoming gradient -- 1 where pre > 0, else 0
+// (ReLU) or the negative slope (LeakyReLU).  pre is always
+// fmaf((x - shift) - mean_d, scale, beta), in the forward and when the
+// backward recomputes it, so both take the same decision.
+__device__ __forceinline__ float act_out(float pre, int act, float slope) {
+  if (act == GBN_ACT_NONE || pre > 0.f) return pre;
+  return act == GBN_ACT_RELU ? 0.f : pre * slope;
+}
+__device__ __forceinline__ float act_gate(float pre, int act, float slope) {
+  return pre > 0.f ? 1.f : (act == GBN_ACT_RELU ? 0.f : slope);
 }
 
 }  // namespace gbn

@@ -59,12 +59,14 @@ struct FArgs {
   const void* dy;        // backward
   void* out;             // y (forward) or dx (backward)
   const float* gamma;    // forward, may be null (1)
-  const float* beta;     // forward, may be null (0)
+  const float* beta;     // may be null (0); the backward needs it only with an activation
   float* stats;          // forward: written; backward: read
   float* running_mean;   // forward, may be null
   float* running_var;    // forward, may be null
   float* grads;          // backward: written
   float momentum, eps;
+  int32_t act;           // GBN_ACT_*: output act(pre) forward, gate on dy backward
+  float slope;           // LeakyReLU negative slope
   unsigned long long* sync;  // [2] epoch pair, then [G][2] flag pairs
   float2* part;              // [2][grid_y][C]
   int* status;
@@ -84,7 +86,7 @@ struct FArgs {
 };
 
 // Parameters per segment: [0] shift, [1] mean - shift (rounded),
-// forward [2] scale, [3] beta; backward [2] scale, [3] k1, [4] k2.
+// forward [2] scale, [3] beta; backward [2] scale, [3] k1, [4] k2, [5] beta.
 struct FShared {
   uint64_t full[kFMaxStages];
   uint64_t empty[kFMaxStages];
@@ -98,7 +100,7 @@ struct FShared {
   int seg_len[kFMaxSegs];     // vectors
   int seg_klo[kFMaxSegs];     // first CTA of the channel
   int seg_khi[kFMaxSegs];     // last CTA of the channel
-  float seg_par[kFMaxSegs][5];
+  float seg_par[kFMaxSegs][6];
   float2 red[2][kFConsumerWarps];
 };
 static_assert(sizeof(FShared) <= kFStaticSmem, "static shared memory bound");
@@ -310,8 +312,17 @@ __device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, DF2& a1, DF2& a2) {
   df2_add(a2, l2);
 }
 
-template <typename T>
-__device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, DF2& a0, DF2& a1) {
+// With an activation (ACT), dy is first gated by d act / d pre with
+// pre = ((x - shift) - mean_d)*scale + beta, the forward's expression.
+struct ActPar {
+  f2 md2, sc2, be2;
+  int act;
+  float slope;
+};
+
+template <typename T, bool ACT>
+__device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, const ActPar& ap,
+                                        DF2& a0, DF2& a1) {
   constexpr int NP = Pairs16<T>::NP;
   f2 px[NP], pd[NP];
   Pairs16<T>::get(rx, px);
@@ -319,6 +330,11 @@ __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, DF2
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     const f2 d = f2_sub(px[k], sh2);
+    if constexpr (ACT) {
+      const float2 pre = f2_unpack(f2_fma(f2_sub(d, ap.md2), ap.sc2, ap.be2));
+      pd[k] = f2_mul_rounded(pd[k], f2_pack(act_gate(pre.x, ap.act, ap.slope),
+                                            act_gate(pre.y, ap.act, ap.slope)));
+    }
     df2_add(a0, pd[k]);
     const f2 prod = f2_mul_rounded(pd[k], d);
     df2_add(a1, prod);
@@ -364,6 +380,12 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
   for (int s = 0; s < sh.nseg; ++s) {
     const float shift = sh.seg_par[s][0];
     const f2 sh2 = f2_splat(shift), nsh2 = f2_splat(-shift);
+    ActPar ap;
+    ap.md2 = f2_splat(sh.seg_par[s][1]);
+    ap.sc2 = f2_splat(sh.seg_par[s][2]);
+    ap.be2 = f2_splat(sh.seg_par[s][5]);
+    ap.act = a.act;
+    ap.slope = a.slope;
     DF2 a0{0ull, 0ull}, a1{0ull, 0ull};
     const int nq = stages_in(sh, a, s);
     for (int q = 0; q < nq; ++q, ++i) {
@@ -375,11 +397,16 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
       if constexpr (!BWD) {
         for (int v = ct; v < len; v += kFConsumers)
           fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, a0, a1);
+      } else if (a.act == GBN_ACT_NONE) {
+        for (int v = ct; v < len; v += kFConsumers)
+          bwd_acc<T, false>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
+                            *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2,
+                            nsh2, ap, a0, a1);
       } else {
         for (int v = ct; v < len; v += kFConsumers)
-          bwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
-                     *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2, nsh2,
-                     a0, a1);
+          bwd_acc<T, true>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
+                           *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2,
+                           nsh2, ap, a0, a1);
       }
       // Release the slot only if phase 1 refills it; the last NS stages stay
       // resident for phase 2.
@@ -479,7 +506,9 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
   for (int s = sh.nseg - 1; s >= 0; --s) {
     const int c = sh.seg_c[s];
     const float shift = sh.seg_par[s][0], mean_d = sh.seg_par[s][1], scale = sh.seg_par[s][2];
-    const float p3 = sh.seg_par[s][3], p4 = sh.seg_par[s][4];
+    const float p3 = sh.seg_par[s][3], p4 = sh.seg_par[s][4], beta = sh.seg_par[s][5];
+    const int act = a.act;
+    const float slope = a.slope;
     const int nq = stages_in(sh, a, s);
     for (int q = nq - 1; q >= 0; --q, ++q2) {
       const int slot = (N1 - 1 - q2) % NS;
@@ -501,14 +530,18 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
         V::cvt(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), e);
         if constexpr (!BWD) {
 #pragma unroll
-          for (int k = 0; k < VEC; ++k) e[k] = fmaf((e[k] - shift) - mean_d, scale, p3);
+          for (int k = 0; k < VEC; ++k)
+            e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), act, slope);
         } else {
           float g[VEC];
           V::cvt(*reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), g);
 #pragma unroll
           for (int k = 0; k < VEC; ++k) {
             const float xc = (e[k] - shift) - mean_d;
-            e[k] = fmaf(g[k], scale, fmaf(xc, p3, p4));
+            const float gk = act == GBN_ACT_NONE
+                                 ? g[k]
+                                 : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), act, slope));
+            e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
           }
         }
         store16_cs(out + gvo * VEC, e);
@@ -579,6 +612,7 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
         sh.seg_par[s][0] = a.stats[4 * a.C + c];
         sh.seg_par[s][1] = a.stats[5 * a.C + c];
         sh.seg_par[s][2] = a.stats[3 * a.C + c];
+        sh.seg_par[s][5] = a.beta ? a.beta[c] : 0.f;
       }
     }
     consumers_sync();
@@ -720,8 +754,10 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
 cudaError_t bn_fused_forward(const BnFusedPlan& p, int dtype, const void* x, void* y,
                              const float* gamma, const float* beta, float* stats,
                              float* running_mean, float* running_var, float momentum, float eps,
-                             void* ws, int* status, cudaStream_t st) {
+                             int act, float slope, void* ws, int* status, cudaStream_t st) {
   FArgs a = make_args(p, ws);
+  a.act = act;
+  a.slope = slope;
   a.x = x;
   a.out = y;
   a.gamma = gamma;
@@ -737,9 +773,13 @@ cudaError_t bn_fused_forward(const BnFusedPlan& p, int dtype, const void* x, voi
 }
 
 cudaError_t bn_fused_backward(const BnFusedPlan& p, int dtype, const void* x, const void* dy,
-                              void* dx, const float* stats, float* grads, void* ws, int* status,
+                              void* dx, const float* stats, const float* beta, int act,
+                              float slope, float* grads, void* ws, int* status,
                               cudaStream_t st) {
   FArgs a = make_args(p, ws);
+  a.beta = beta;
+  a.act = act;
+  a.slope = slope;
   a.x = x;
   a.dy = dy;
   a.out = dx;

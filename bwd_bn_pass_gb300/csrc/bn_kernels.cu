@@ -216,6 +216,8 @@ struct ApplyArgs {
   float eps;
   const float* mean;
   const float* scale;
+  int act;      // GBN_ACT_*
+  float slope;
 };
 
 // Warp 0 computes (shift, mean - shift, scale, beta) for channel c; in
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
         float e[VEC];
         V::cvt(r[u], e);
 #pragma unroll
-        for (int k = 0; k < VEC; ++k) e[k] = fmaf((e[k] - shift) - mean_d, scale, beta);
+        for (int k = 0; k < VEC; ++k)
+          e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, beta), a.act, a.slope);
         V::store(y + (size_t)off[u] * VEC, e);
       }
     }
@@ -298,10 +301,11 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
 
 // --------------------------------------------------------- grad_sums --
 
-template <typename T, int VEC, typename I>
+template <typename T, int VEC, typename I, bool GATE>
 __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
     bn_grad_sums_kernel(const T* __restrict__ x, const T* __restrict__ dy, BnGeom g,
-                        const float* __restrict__ stats, float2* __restrict__ part) {
+                        const float* __restrict__ stats, float2* __restrict__ part,
+                        const float* __restrict__ beta, int act, float slope) {
   using V = Vec<T, VEC>;
   __shared__ float2 red[64];
   pdl_launch_dependents();
@@ -309,6 +313,21 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   int32_t v0, cnt;
   slice(g, j, v0, cnt);
   const float shift = stats[4 * (int64_t)g.C + c];
+  // With an activation, dy is gated by d act / d pre, pre recomputed as in
+  // the forward apply.
+  float mean_d = 0.f, scale = 0.f, bta = 0.f;
+  if constexpr (GATE) {
+    mean_d = stats[5 * (int64_t)g.C + c];
+    scale = stats[3 * (int64_t)g.C + c];
+    bta = beta ? beta[c] : 0.f;
+  }
+  auto gate = [&](const float (&ex)[VEC], float (&ed)[VEC]) {
+    if constexpr (GATE) {
+#pragma unroll
+      for (int k = 0; k < VEC; ++k)
+        ed[k] = __fmul_rn(ed[k], act_gate(fmaf((ex[k] - shift) - mean_d, scale, bta), act, slope));
+    }
+  };
 
   DF s0, s1;
   Cursor<I> q = cursor_at<I>(g, c, v0 + (int32_t)threadIdx.x);
@@ -335,6 +354,7 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
           float ex[VEC], ed[VEC];
           V::cvt(rx[u], ex);
           V::cvt(rd[u], ed);
+          gate(ex, ed);
 #pragma unroll
           for (int k = 0; k < VEC / 2; ++k) {
             const f2 x2 = f2_pack(ex[2 * k], ex[2 * k + 1]);
@@ -375,6 +395,7 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
           float ex[VEC], ed[VEC];
           V::cvt(rx[u], ex);
           V::cvt(rd[u], ed);
+          gate(ex, ed);
           float d, d_lo;
           x_minus_shift<T>(ex[0], shift, d, d_lo);
           df_add(s0, ed[0]);
@@ -398,7 +419,7 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
 // double-fp32 with the forward's (mean - shift) pair.
 __device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
                                          const float2* part, float* grads, int c, int j,
-                                         float* fin) {
+                                         const float* beta, float* fin) {
   DF p0, p1;
   reduce_partials(part, g, c, p0, p1);
   const int64_t C = g.C;
@@ -419,6 +440,7 @@ __device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
     fin[2] = scale;
     fin[3] = k1;
     fin[4] = k2;
+    fin[5] = beta ? beta[c] : 0.f;
   }
 }
 
@@ -426,9 +448,10 @@ template <typename T, int VEC, typename I>
 __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
     bn_dx_kernel(const T* __restrict__ x, const T* dy, T* dx, BnGeom g,
                  const float* __restrict__ stats, const float2* __restrict__ part,
-                 float* __restrict__ grads) {
+                 float* __restrict__ grads, const float* __restrict__ beta, int act,
+                 float slope) {
   using V = Vec<T, VEC>;
-  __shared__ float fin[5];  // shift, mean_d, scale, k1, k2
+  __shared__ float fin[6];  // shift, mean_d, scale, k1, k2, beta
   const int c = blockIdx.x, j = blockIdx.y;
   int32_t v0, cnt;
   slice(g, j, v0, cnt);
@@ -448,9 +471,10 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   }
 
   pdl_wait();
-  if (threadIdx.x < 32) dx_prologue(g, stats, part, grads, c, j, fin);
+  if (threadIdx.x < 32) dx_prologue(g, stats, part, grads, c, j, beta, fin);
   __syncthreads();
   const float shift = fin[0], mean_d = fin[1], scale = fin[2], k1 = fin[3], k2 = fin[4];
+  const float bta = fin[5];
 
   for (int32_t i = 0; i < cnt; i += kUDx) {
 #pragma unroll
@@ -462,7 +486,10 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
 #pragma unroll
         for (int k = 0; k < VEC; ++k) {
           const float xc = (ex[k] - shift) - mean_d;
-          ex[k] = fmaf(ed[k], scale, fmaf(xc, k1, k2));
+          const float gk = act == GBN_ACT_NONE
+                               ? ed[k]
+                               : __fmul_rn(ed[k], act_gate(fmaf(xc, scale, bta), act, slope));
+          ex[k] = fmaf(gk, scale, fmaf(xc, k1, k2));
         }
         V::store(dx + (size_t)off[u] * VEC, ex);
       }
@@ -537,18 +564,26 @@ template <typename T, int VEC, typename I> struct ApplyL {
 };
 template <typename T, int VEC, typename I> struct GradSumsL {
   static cudaError_t run(const void* x, const void* dy, const BnPlan& p, const float* stats,
-                         float2* part, cudaStream_t st) {
-    return launch(bn_grad_sums_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, false,
-                  static_cast<const T*>(x), static_cast<const T*>(dy), make_geom(p), stats, part);
+                         float2* part, const float* beta, int act, float slope,
+                         cudaStream_t st) {
+    // The gate is a template switch: the ungated kernel keeps the register
+    // budget it has without an activation.
+    return act == GBN_ACT_NONE
+               ? launch(bn_grad_sums_kernel<T, VEC, I, false>, bn_grid(p), dim3(kBnThreads), 0,
+                        st, false, static_cast<const T*>(x), static_cast<const T*>(dy),
+                        make_geom(p), stats, part, beta, act, slope)
+               : launch(bn_grad_sums_kernel<T, VEC, I, true>, bn_grid(p), dim3(kBnThreads), 0,
+                        st, false, static_cast<const T*>(x), static_cast<const T*>(dy),
+                        make_geom(p), stats, part, beta, act, slope);
   }
 };
 template <typename T, int VEC, typename I> struct DxL {
   static cudaError_t run(const void* x, const void* dy, void* dx, const BnPlan& p,
-                         const float* stats, const float2* part, float* grads, cudaStream_t st,
-                         bool pdl) {
+                         const float* stats, const float2* part, float* grads, const float* beta,
+                         int act, float slope, cudaStream_t st, bool pdl) {
     return launch(bn_dx_kernel<T, VEC, I>, bn_grid(p), dim3(kBnThreads), 0, st, pdl,
                   static_cast<const T*>(x), static_cast<const T*>(dy), static_cast<T*>(dx),
-                  make_geom(p), stats, part, grads);
+                  make_geom(p), stats, part, grads, beta, act, slope);
   }
 };
 
@@ -605,8 +640,10 @@ cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, 
                             const float2* part, const float* gamma, const float* beta,
                             float* stats, float* running_mean, float* running_var,
                             float momentum, float eps, const float* mean, const float* scale,
-                            cudaStream_t st, bool pdl) {
+                            int act, float slope, cudaStream_t st, bool pdl) {
   ApplyArgs a;
+  a.act = act;
+  a.slope = slope;
   a.mode = mode;
   a.part = part;
   a.gamma = gamma;
@@ -622,14 +659,15 @@ cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, 
 }
 
 cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const BnPlan& p,
-                                const float* stats, float2* part, cudaStream_t st) {
-  return dispatch<GradSumsL>(p, dtype, x, dy, p, stats, part, st);
+                                const float* stats, float2* part, const float* beta, int act,
+                                float slope, cudaStream_t st) {
+  return dispatch<GradSumsL>(p, dtype, x, dy, p, stats, part, beta, act, slope, st);
 }
 
 cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
-                         const float* stats, const float2* part, float* grads, cudaStream_t st,
-                         bool pdl) {
-  return dispatch<DxL>(p, dtype, x, dy, dx, p, stats, part, grads, st, pdl);
+                         const float* stats, const float2* part, float* grads, const float* beta,
+                         int act, float slope, cudaStream_t st, bool pdl) {
+  return dispatch<DxL>(p, dtype, x, dy, dx, p, stats, part, grads, beta, act, slope, st, pdl);
 }
 
 }  // namespace gbn

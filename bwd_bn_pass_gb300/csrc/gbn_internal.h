@@ -77,12 +77,15 @@ cudaError_t bn_launch_apply(const void* x, void* y, int dtype, const BnPlan& p, 
                             const float2* part, const float* gamma, const float* beta,
                             float* stats, float* running_mean, float* running_var,
                             float momentum, float eps, const float* mean, const float* scale,
-                            cudaStream_t st, bool pdl);
+                            int act, float slope, cudaStream_t st, bool pdl);
+// With act != GBN_ACT_NONE the backward kernels gate dy by d act / d pre,
+// pre recomputed from x, the stats rows and beta (may be null: 0).
 cudaError_t bn_launch_grad_sums(const void* x, const void* dy, int dtype, const BnPlan& p,
-                                const float* stats, float2* part, cudaStream_t st);
+                                const float* stats, float2* part, const float* beta, int act,
+                                float slope, cudaStream_t st);
 cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, const BnPlan& p,
-                         const float* stats, const float2* part, float* grads, cudaStream_t st,
-                         bool pdl);
+                         const float* stats, const float2* part, float* grads, const float* beta,
+                         int act, float slope, cudaStream_t st, bool pdl);
 
 // Persistent single-launch BatchNorm (bn_fused.cu): one CTA per SM owns a
 // contiguous range of the channel-major view; see that file.
@@ -111,9 +114,10 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
 cudaError_t bn_fused_forward(const BnFusedPlan& p, int dtype, const void* x, void* y,
                              const float* gamma, const float* beta, float* stats,
                              float* running_mean, float* running_var, float momentum, float eps,
-                             void* ws, int* status, cudaStream_t st);
+                             int act, float slope, void* ws, int* status, cudaStream_t st);
 cudaError_t bn_fused_backward(const BnFusedPlan& p, int dtype, const void* x, const void* dy,
-                              void* dx, const float* stats, float* grads, void* ws, int* status,
+                              void* dx, const float* stats, const float* beta, int act,
+                              float slope, float* grads, void* ws, int* status,
                               cudaStream_t st);
 // Shared-memory limits and the one-CTA-per-SM check (called from device_info).
 cudaError_t bn_fused_configure(int smem_optin, bool* ok);

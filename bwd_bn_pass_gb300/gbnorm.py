@@ -23,6 +23,11 @@ GBN_ROW_RMS = 0
 GBN_ROW_LN = 1
 GBN_ROW_LN_FUSED = 2
 GBN_DEV_WAIT_TIMEOUT = 1
+GBN_ACT_NONE = 0
+GBN_ACT_RELU = 1
+GBN_ACT_LEAKY_RELU = 2
+_ACTS = {None: GBN_ACT_NONE, "none": GBN_ACT_NONE, "relu": GBN_ACT_RELU,
+         "leaky_relu": GBN_ACT_LEAKY_RELU}
 
 _DTYPE_CODE = {torch.float32: GBN_F32, torch.bfloat16: GBN_BF16}
 
@@ -58,11 +63,16 @@ _SIGNATURES = {
                                     _P, _P, _P, _SZ, _P]),
     "gbn_bn_forward_train_noalloc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F,
                                             _F, _P, _P, _P]),
+    "gbn_bn_forward_train_act": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
+                                        _INT, _F, _P, _P, _P, _SZ, _P]),
     "gbn_bn_stats": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _SZ, _P]),
     "gbn_bn_finalize_apply": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                      _P, _P, _P, _SZ, _P]),
     "gbn_bn_apply": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P]),
+    "gbn_bn_apply_act": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _INT, _F, _P, _P]),
     "gbn_bn_backward": (_INT, [_P, _P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "gbn_bn_backward_act": (_INT, [_P, _P, _INT, _I64, _I64, _I64, _P, _P, _INT, _F, _P, _P,
+                                   _P, _SZ, _P]),
     "gbn_bn_grad_sums": (_INT, [_P, _P, _INT, _I64, _I64, _I64, _P, _P, _SZ, _P]),
     "gbn_bn_finalize_dx": (_INT, [_P, _P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "gbn_rowwise_workspace_bytes": (_SZ, [_I64, _I64, _INT, _INT, _INT]),
@@ -190,11 +200,21 @@ def bn_workspace(x):
     return torch.empty(max(n, 256), dtype=torch.uint8, device=x.device)
 
 
+def _act_code(act):
+    if act not in _ACTS:
+        raise ValueError(f"act must be one of {sorted(k for k in _ACTS if k)} or None")
+    return _ACTS[act]
+
+
 def bn_forward_train(x, gamma=None, beta=None, running_mean=None, running_var=None,
-                     momentum=0.1, eps=1e-5, *, y=None, stats=None, ws=None):
+                     momentum=0.1, eps=1e-5, *, y=None, stats=None, ws=None, act=None,
+                     slope=0.01):
     """Training forward.  Returns (y, stats); running stats updated in place.
 
-    ``stats[:4*C].view(4, C)`` = (mean, var, inv_std, gamma*inv_std)."""
+    ``stats[:4*C].view(4, C)`` = (mean, var, inv_std, gamma*inv_std).  With
+    ``act`` ("relu" / "leaky_relu", negative slope ``slope``) y is the
+    activation of the BatchNorm output (gbn_bn_forward_train_act)."""
+    code = _act_code(act)
     _cuda(x, "x")
     B, C, HW = _bn_dims(x)
     for name, t in (("gamma", gamma), ("beta", beta), ("running_mean", running_mean),
@@ -205,12 +225,16 @@ def bn_forward_train(x, gamma=None, beta=None, running_mean=None, running_var=No
     ws = bn_workspace(x) if ws is None else _cuda(ws, "ws")
     _same_device(x, ("y", y), ("stats", stats), ("ws", ws), ("gamma", gamma), ("beta", beta),
                  ("running_mean", running_mean), ("running_var", running_var))
+    args = (_ptr(x), _code(x.dtype), B, C, HW, _ptr(gamma), _ptr(beta), _ptr(running_mean),
+            _ptr(running_var), float(momentum), float(eps))
+    tail = (_ptr(y), _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(x.device))
     with torch.cuda.device(x.device):
-        st = lib().gbn_bn_forward_train(
-            _ptr(x), _code(x.dtype), B, C, HW, _ptr(gamma), _ptr(beta), _ptr(running_mean),
-            _ptr(running_var), float(momentum), float(eps), _ptr(y), _ptr(stats), _ptr(ws),
-            ws.numel() * ws.element_size(), _stream(x.device))
-    _check("gbn_bn_forward_train", st)
+        if code == GBN_ACT_NONE:
+            name, st = "gbn_bn_forward_train", lib().gbn_bn_forward_train(*args, *tail)
+        else:
+            name = "gbn_bn_forward_train_act"
+            st = lib().gbn_bn_forward_train_act(*args, code, float(slope), *tail)
+    _check(name, st)
     return y, stats
 
 
@@ -254,24 +278,34 @@ def bn_finalize_apply(x, gamma, beta, running_mean, running_var, momentum, eps, 
     _check("gbn_bn_finalize_apply", st)
 
 
-def bn_apply(x, beta=None, *, stats=None, mean=None, scale=None, y=None):
+def bn_apply(x, beta=None, *, stats=None, mean=None, scale=None, y=None, act=None,
+             slope=0.01):
     """Centred apply (x - mean)*scale + beta from a training stats buffer or
-    from per-channel mean/scale (inference)."""
+    from per-channel mean/scale (inference), optionally through ``act``."""
+    code = _act_code(act)
     _cuda(x, "x")
     B, C, HW = _bn_dims(x)
     for name, t in (("beta", beta), ("mean", mean), ("scale", scale)):
         _fp32_vec(t, name, C)
     y = torch.empty_like(x) if y is None else _cuda(y, "y")
+    args = (_ptr(x), _code(x.dtype), B, C, HW, _ptr(stats), _ptr(mean), _ptr(scale), _ptr(beta))
     with torch.cuda.device(x.device):
-        st = lib().gbn_bn_apply(_ptr(x), _code(x.dtype), B, C, HW, _ptr(stats), _ptr(mean),
-                                _ptr(scale), _ptr(beta), _ptr(y), _stream(x.device))
-    _check("gbn_bn_apply", st)
+        if code == GBN_ACT_NONE:
+            name, st = "gbn_bn_apply", lib().gbn_bn_apply(*args, _ptr(y), _stream(x.device))
+        else:
+            name = "gbn_bn_apply_act"
+            st = lib().gbn_bn_apply_act(*args, code, float(slope), _ptr(y), _stream(x.device))
+    _check(name, st)
     return y
 
 
-def bn_backward(x, dy, stats, *, dx=None, grads=None, ws=None):
+def bn_backward(x, dy, stats, *, dx=None, grads=None, ws=None, beta=None, act=None,
+                slope=0.01):
     """Training backward.  Returns (dx, grads) with grads.view(4, C) =
-    (dgamma, dbeta, k1, k2)."""
+    (dgamma, dbeta, k1, k2).  With ``act`` it is the backward of
+    ``bn_forward_train(..., act=act, slope=slope)`` given that forward's
+    ``beta`` (gbn_bn_backward_act)."""
+    code = _act_code(act)
     _cuda(x, "x")
     _cuda(dy, "dy")
     if dy.shape != x.shape or dy.dtype != x.dtype:
@@ -281,12 +315,20 @@ def bn_backward(x, dy, stats, *, dx=None, grads=None, ws=None):
     grads = (torch.empty(4 * C, dtype=torch.float32, device=x.device) if grads is None
              else _cuda(grads, "grads"))
     ws = bn_workspace(x) if ws is None else _cuda(ws, "ws")
-    _same_device(x, ("dy", dy), ("stats", stats), ("dx", dx), ("grads", grads), ("ws", ws))
+    _fp32_vec(beta, "beta", C)
+    _same_device(x, ("dy", dy), ("stats", stats), ("dx", dx), ("grads", grads), ("ws", ws),
+                 ("beta", beta))
+    tail = (_ptr(dx), _ptr(grads), _ptr(ws), ws.numel() * ws.element_size(), _stream(x.device))
     with torch.cuda.device(x.device):
-        st = lib().gbn_bn_backward(_ptr(x), _ptr(dy), _code(x.dtype), B, C, HW, _ptr(stats),
-                                   _ptr(dx), _ptr(grads), _ptr(ws),
-                                   ws.numel() * ws.element_size(), _stream(x.device))
-    _check("gbn_bn_backward", st)
+        if code == GBN_ACT_NONE:
+            name = "gbn_bn_backward"
+            st = lib().gbn_bn_backward(_ptr(x), _ptr(dy), _code(x.dtype), B, C, HW,
+                                       _ptr(stats), *tail)
+        else:
+            name = "gbn_bn_backward_act"
+            st = lib().gbn_bn_backward_act(_ptr(x), _ptr(dy), _code(x.dtype), B, C, HW,
+                                           _ptr(stats), _ptr(beta), code, float(slope), *tail)
+    _check(name, st)
     return dx, grads
 
 

@@ -85,6 +85,16 @@ extern "C" {
 /* grads: fp32 [4, C] = (dgamma, dbeta, k1, k2), [P4] "Backward finalize".  */
 #define GBN_BN_GRADS_FLOATS(C) (4 * (int64_t)(C))
 
+/* ---- activations fused into BatchNorm (gbn_bn_*_act) ------------------- */
+/* [P4] "Part 2": the BatchNorm output pre = (x - mean)*scale + beta goes
+ * through act in the same pass.  RELU: max(pre, 0).  LEAKY_RELU: pre where
+ * pre > 0, else slope*pre.  The backward gates dy by d act / d pre (1 where
+ * pre > 0, else 0 or slope), recomputing pre from x, stats and beta, so no
+ * mask or pre-activation tensor is stored.                                  */
+#define GBN_ACT_NONE 0
+#define GBN_ACT_RELU 1
+#define GBN_ACT_LEAKY_RELU 2
+
 /* ---- row-wise workspace kinds ------------------------------------------ */
 #define GBN_ROW_RMS 0      /* rmsnorm_backward: dweight partials           */
 #define GBN_ROW_LN 1       /* layernorm_backward, plain: dgamma, dbeta     */
@@ -166,6 +176,17 @@ GBN_API int gbn_bn_forward_train_noalloc(const void* x, int dtype, int64_t B, in
                                          float momentum, float eps, void* y, float* stats,
                                          void* stream);
 
+/* gbn_bn_forward_train followed by the activation `act` (GBN_ACT_*) in the
+ * same kernels: y = act((x - mean)*scale + beta).  slope is LeakyReLU's
+ * negative slope (finite; ignored for the others).  stats and the running
+ * update are those of gbn_bn_forward_train.  GBN_EINVAL for an unknown act
+ * or a non-finite LeakyReLU slope.                                          */
+GBN_API int gbn_bn_forward_train_act(const void* x, int dtype, int64_t B, int64_t C,
+                                     int64_t HW, const float* gamma, const float* beta,
+                                     float* running_mean, float* running_var, float momentum,
+                                     float eps, int act, float slope, void* y, float* stats,
+                                     void* ws, size_t ws_bytes, void* stream);
+
 /* Phase 1 of the forward alone: writes the stats partials into ws.        */
 GBN_API int gbn_bn_stats(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                  void* ws, size_t ws_bytes, void* stream);
@@ -188,6 +209,12 @@ GBN_API int gbn_bn_apply(const void* x, int dtype, int64_t B, int64_t C, int64_t
                  const float* stats, const float* mean, const float* scale,
                  const float* beta, void* y, void* stream);
 
+/* gbn_bn_apply followed by the activation `act` (arguments as
+ * gbn_bn_forward_train_act).                                                */
+GBN_API int gbn_bn_apply_act(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                             const float* stats, const float* mean, const float* scale,
+                             const float* beta, int act, float slope, void* y, void* stream);
+
 /* Full training backward: grad_sums pass + finalize/dx.  `stats` is the
  * buffer written by the matching training forward of the same x.  Writes
  * dx and grads (fp32 [4, C] = dgamma, dbeta, k1, k2; [P4] "Backward
@@ -196,6 +223,17 @@ GBN_API int gbn_bn_apply(const void* x, int dtype, int64_t B, int64_t C, int64_t
 GBN_API int gbn_bn_backward(const void* x, const void* dy, int dtype, int64_t B,
                     int64_t C, int64_t HW, const float* stats, void* dx,
                     float* grads, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of gbn_bn_forward_train_act: dy is first multiplied by
+ * d act / d pre, with pre = (x - mean)*scale + beta recomputed from x, the
+ * forward's stats and the forward's beta (fp32 [C], NULL if the forward had
+ * none), evaluated exactly as the forward did; then as gbn_bn_backward,
+ * grads' dbeta and dgamma being those of the gated gradient.  act and slope
+ * must be the forward's.                                                    */
+GBN_API int gbn_bn_backward_act(const void* x, const void* dy, int dtype, int64_t B,
+                                int64_t C, int64_t HW, const float* stats, const float* beta,
+                                int act, float slope, void* dx, float* grads, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* Phase 1 of the backward alone: grad_sums partials into ws.              */
 GBN_API int gbn_bn_grad_sums(const void* x, const void* dy, int dtype, int64_t B,

@@ -21,6 +21,11 @@ from .bn import (
     batch_norm_backward,
     batch_norm_act_forward_train,
     batch_norm_act_backward,
+    activation,
+    activation_gate,
+    ACT_NONE,
+    ACT_RELU,
+    ACT_LEAKY_RELU,
 )
 from .rmsnorm import rms_norm_rstd, rms_norm_forward, rms_norm_backward
 from .layernorm import (
@@ -39,6 +44,8 @@ __all__ = [
     "batch_norm_backward",
     "batch_norm_act_forward_train",
     "batch_norm_act_backward",
+    "activation",
+    "activation_gate",
     "rms_norm_rstd",
     "rms_norm_forward",
     "rms_norm_backward",

@@ -94,6 +94,33 @@ def test_bn_other_entry_points_argument_errors(gbn):
     assert L.gbn_bn_workspace_bytes(-1, 2, 2, -1) == 0
 
 
+def test_bn_act_argument_errors(gbn):
+    """Unknown activations and non-finite LeakyReLU slopes are rejected
+    before anything touches a device."""
+    L = gbn.lib()
+
+    def fwd(act, slope, C=3):
+        return L.gbn_bn_forward_train_act(A16, 0, 4, C, 5, NULL, NULL, NULL, NULL, 0.1, 1e-5,
+                                          act, slope, A16, A16, A16, 1 << 20, NULL)
+
+    def bwd(act, slope, C=3):
+        return L.gbn_bn_backward_act(A16, A16, 0, 4, C, 5, A16, NULL, act, slope, A16, A16, A16,
+                                     1 << 20, NULL)
+
+    def app(act, slope, C=3):
+        return L.gbn_bn_apply_act(A16, 0, 4, C, 5, A16, NULL, NULL, NULL, act, slope, A16, NULL)
+
+    for f in (fwd, bwd, app):
+        assert f(3, 0.0) == EINVAL
+        assert f(-1, 0.0) == EINVAL
+        assert f(2, float("nan")) == EINVAL
+        assert f(2, float("inf")) == EINVAL
+        assert f(1, float("nan"), C=0) == OK     # ReLU ignores the slope
+        assert f(2, -0.5, C=0) == OK             # any finite slope
+    assert L.gbn_bn_forward_train_act(A16, 7, 4, 3, 5, NULL, NULL, NULL, NULL, 0.1, 1e-5, 1,
+                                      0.0, A16, A16, A16, 1 << 20, NULL) == EDTYPE
+
+
 def _rms(L, dtype=1, R=4, H=64, dy=A16, x=A16, w=A16, rstd=A16, dx=A16, dw=A16, ws=A16):
     return L.gbn_rmsnorm_backward(dy, x, w, dtype, rstd, R, H, dx, dw, ws, 1 << 20, NULL)
 

@@ -34,8 +34,6 @@ struct DeviceGuard {
   }
 };
 
-inline int esize_of(int dtype) { return dtype == GBN_F32 ? 4 : 2; }
-
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

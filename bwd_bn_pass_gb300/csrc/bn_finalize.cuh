@@ -68,7 +68,8 @@ struct BnBwdFinal {
 };
 
 // From p0 = sum dy and p1 = sum dy*(x - shift); S = sum dy*(x - mean) =
-// p1 - (mean - shift)*p0 in double-fp32 with the forward's (mean - shift).
+// p1 - (mean - shift)*p0 in double-fp32 with the forward's (mean - shift),
+// whose channel sum is exact, so a constant dy gives S = 0 to that precision.
 __device__ __forceinline__ BnBwdFinal bn_bwd_final(DF p0, DF p1, DF md, float inv_std,
                                                    float scale, float M) {
   const float S = df_round(df_sum(p1, df_neg(df_mul_df(md, p0))));

@@ -291,24 +291,33 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
 
 // ------------------------------------------------------------ consumers --
 
-// Phase-1 accumulation of one 16-byte vector.  Forward: sum d and sum d^2
-// (d = x - shift) over the vector's lanes in fp32, then one double-fp32 add
-// per vector (as in the two-launch stats kernel).  Backward: sum dy and
-// sum dy*d per element in double-fp32 with each product's exact residual and,
-// for fp32 input, the rounding error of x - shift.
+// Phase-1 accumulation of one 16-byte vector.  Forward: sum d (d = x - shift)
+// per element in double-fp32 with, for fp32 input, the rounding error of
+// x - shift, so that the channel's sum d is exact to double-fp32 precision
+// (the backward's sum dy*(x - mean) relies on it: a constant dy must give 0);
+// sum d^2 over the vector's lanes in fp32, then one double-fp32 add per
+// vector (its rounding enters the variance only relatively).  Backward: sum
+// dy*d per element in double-fp32 with each product's exact residual and,
+// for fp32 input, the rounding error of x - shift; sum dy likewise for fp32,
+// while ungated bf16 dy is first summed over the vector's four elements per
+// lane in fp32 -- exact for 8-bit significands within 14 binades of each
+// other -- and then added in double-fp32 once per vector.
 template <typename T>
-__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, DF2& a1, DF2& a2) {
+__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2& a1, DF2& a2) {
   constexpr int NP = Pairs16<T>::NP;
   f2 p[NP];
   Pairs16<T>::get(r, p);
-  f2 l1 = 0ull, l2 = 0ull;
+  f2 l2 = 0ull;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     const f2 d = f2_sub(p[k], sh2);
-    l1 = f2_add(l1, d);
+    df2_add(a1, d);
+    if constexpr (sizeof(T) == 4) {
+      const f2 bb = f2_sub(d, p[k]);
+      a1.lo = f2_add(a1.lo, f2_add(f2_sub(p[k], f2_sub(d, bb)), f2_sub(nsh2, bb)));
+    }
     l2 = f2_fma(d, d, l2);
   }
-  df2_add(a1, l1);
   df2_add(a2, l2);
 }
 
@@ -327,6 +336,8 @@ __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, con
   f2 px[NP], pd[NP];
   Pairs16<T>::get(rx, px);
   Pairs16<T>::get(rd, pd);
+  constexpr bool kLocalDy = sizeof(T) == 2 && !ACT;
+  f2 l0 = 0ull;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     const f2 d = f2_sub(px[k], sh2);
@@ -335,7 +346,10 @@ __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, con
       pd[k] = f2_mul_rounded(pd[k], f2_pack(act_gate(pre.x, ap.act, ap.slope),
                                             act_gate(pre.y, ap.act, ap.slope)));
     }
-    df2_add(a0, pd[k]);
+    if constexpr (kLocalDy)
+      l0 = f2_add(l0, pd[k]);
+    else
+      df2_add(a0, pd[k]);
     const f2 prod = f2_mul_rounded(pd[k], d);
     df2_add(a1, prod);
     // exact residual dy*d - prod (the negation flips the sign of both lanes)
@@ -346,6 +360,7 @@ __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, con
       a1.lo = f2_fma(pd[k], d_lo, a1.lo);
     }
   }
+  if constexpr (kLocalDy) df2_add(a0, l0);
 }
 
 // Sum two (hi, lo) pairs over the consumer warps in a fixed tree; the result
@@ -396,7 +411,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
       const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
       if constexpr (!BWD) {
         for (int v = ct; v < len; v += kFConsumers)
-          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, a0, a1);
+          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a0, a1);
       } else if (a.act == GBN_ACT_NONE) {
         for (int v = ct; v < len; v += kFConsumers)
           bwd_acc<T, false>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
@@ -489,7 +504,9 @@ __device__ void finalize_segment(const FArgs& a, FShared& sh, int s) {
   __syncwarp();
 }
 
-template <typename T, bool BWD>
+// ACT is the activation (GBN_ACT_*) as a compile-time switch, so that the
+// plain pass carries no per-element test.
+template <typename T, bool BWD, int ACT>
 __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char* ring,
                                 uint32_t& fpar) {
   constexpr int VEC = 16 / sizeof(T);
@@ -507,7 +524,6 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
     const int c = sh.seg_c[s];
     const float shift = sh.seg_par[s][0], mean_d = sh.seg_par[s][1], scale = sh.seg_par[s][2];
     const float p3 = sh.seg_par[s][3], p4 = sh.seg_par[s][4], beta = sh.seg_par[s][5];
-    const int act = a.act;
     const float slope = a.slope;
     const int nq = stages_in(sh, a, s);
     for (int q = nq - 1; q >= 0; --q, ++q2) {
@@ -531,16 +547,16 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
         if constexpr (!BWD) {
 #pragma unroll
           for (int k = 0; k < VEC; ++k)
-            e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), act, slope);
+            e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), ACT, slope);
         } else {
           float g[VEC];
           V::cvt(*reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), g);
 #pragma unroll
           for (int k = 0; k < VEC; ++k) {
             const float xc = (e[k] - shift) - mean_d;
-            const float gk = act == GBN_ACT_NONE
+            const float gk = ACT == GBN_ACT_NONE
                                  ? g[k]
-                                 : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), act, slope));
+                                 : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), ACT, slope));
             e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
           }
         }
@@ -618,7 +634,12 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
     consumers_sync();
     uint32_t fpar = 0;
     consumer_phase1<T, BWD>(a, sh, ring, fpar);
-    consumer_phase2<T, BWD>(a, sh, ring, fpar);
+    if (a.act == GBN_ACT_RELU)
+      consumer_phase2<T, BWD, GBN_ACT_RELU>(a, sh, ring, fpar);
+    else if (a.act == GBN_ACT_LEAKY_RELU)
+      consumer_phase2<T, BWD, GBN_ACT_LEAKY_RELU>(a, sh, ring, fpar);
+    else
+      consumer_phase2<T, BWD, GBN_ACT_NONE>(a, sh, ring, fpar);
   }
   __syncthreads();
 

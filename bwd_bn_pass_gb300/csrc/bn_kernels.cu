@@ -144,8 +144,11 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   DF s1, s2;
   Cursor<I> q = cursor_at<I>(g, c, v0 + (int32_t)threadIdx.x);
   if constexpr (VEC >= 2) {
-    // Two packed lanes: pairs of elements per fp32x2 instruction.
+    // Two packed lanes: pairs of elements per fp32x2 instruction.  sum d per
+    // element in double-fp32 (plus, for fp32 input, the rounding error of
+    // x - shift); sum d^2 per vector in fp32, then double-fp32.
     const f2 sh2 = f2_pack(shift, shift);
+    const f2 nsh2 = f2_pack(-shift, -shift);
     DF2 a1{0ull, 0ull}, a2{0ull, 0ull};
     for (int32_t i = 0; i < cnt; i += kUStats) {
       typename V::raw r[kUStats];
@@ -159,14 +162,18 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
         if (i + u < cnt) {
           float e[VEC];
           V::cvt(r[u], e);
-          f2 l1 = 0ull, l2 = 0ull;  // +0.0f in both lanes
+          f2 l2 = 0ull;  // +0.0f in both lanes
 #pragma unroll
           for (int k = 0; k < VEC / 2; ++k) {
-            const f2 d = f2_sub(f2_pack(e[2 * k], e[2 * k + 1]), sh2);
-            l1 = f2_add(l1, d);
+            const f2 x2 = f2_pack(e[2 * k], e[2 * k + 1]);
+            const f2 d = f2_sub(x2, sh2);
+            df2_add(a1, d);
+            if constexpr (sizeof(T) == 4) {
+              const f2 bb = f2_sub(d, x2);
+              a1.lo = f2_add(a1.lo, f2_add(f2_sub(x2, f2_sub(d, bb)), f2_sub(nsh2, bb)));
+            }
             l2 = f2_fma(d, d, l2);
           }
-          df2_add(a1, l1);
           df2_add(a2, l2);
         }
       }
@@ -188,8 +195,10 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
         if (i + u < cnt) {
           float e[VEC];
           V::cvt(r[u], e);
-          const float d = e[0] - shift;
+          float d, d_lo;
+          x_minus_shift<T>(e[0], shift, d, d_lo);
           df_add(s1, d);
+          if constexpr (sizeof(T) == 4) s1.lo = __fadd_rn(s1.lo, d_lo);
           df_add(s2, d * d);
         }
       }
@@ -612,8 +621,9 @@ bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan)
   // The same workspace also serves the persistent path of either dtype.
   BnFusedPlan fp;
   for (int dtype : {GBN_F32, GBN_BF16})
-    if (bn_fused_plan(dtype, false, B, C, HW, dev, &fp) && fp.ws_bytes > plan->ws_bytes)
-      plan->ws_bytes = fp.ws_bytes;
+    for (bool backward : {false, true})
+      if (bn_fused_plan(dtype, backward, B, C, HW, dev, &fp) && fp.ws_bytes > plan->ws_bytes)
+        plan->ws_bytes = fp.ws_bytes;
   return true;
 }
 

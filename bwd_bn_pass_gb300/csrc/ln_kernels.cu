@@ -93,15 +93,16 @@ __device__ __forceinline__ float sum_warp_slots(const float* slot, int nwarps) {
     const float v5 = nwarps > 5 ? q.y : 0.f, v6 = nwarps > 6 ? q.z : 0.f;
     const float v7 = nwarps > 7 ? q.w : 0.f;
     return ((v0 + v1) + (v2 + v3)) + ((v4 + v5) + (v6 + v7));
+  } else {
+    float v[16];
+#pragma unroll
+    for (int w = 0; w < 16; ++w) v[w] = w < nwarps ? slot[w] : 0.f;
+#pragma unroll
+    for (int step = 1; step < 16; step *= 2)
+#pragma unroll
+      for (int w = 0; w < 16; w += 2 * step) v[w] += v[w + step];
+    return v[0];
   }
-  float v[16];
-#pragma unroll
-  for (int w = 0; w < 16; ++w) v[w] = w < nwarps ? slot[w] : 0.f;
-#pragma unroll
-  for (int step = 1; step < 16; step *= 2)
-#pragma unroll
-    for (int w = 0; w < 16; w += 2 * step) v[w] += v[w + step];
-  return v[0];
 }
 
 // One element's LayerNorm input z from the stage (fused: residual +

@@ -238,6 +238,60 @@ def test_bn_phase_entry_points(gbn, name):
     compare(run_gpu(gbn, inp), run_oracle(inp), case.dtype, what=f"{name} composite")
 
 
+def _constant_dy_inputs(dtype, centred):
+    """dy constant per channel (the gradient of a plain sum of the outputs):
+    sum dy*(x - mean) is then exactly 0, so dgamma and k1 are 0 and only the
+    fp32 tolerance's absolute floor remains.  The constants are exact in
+    bf16; 0.30078125 has a full 8-bit significand.  Channels with a large
+    offset have few significant bits in x - shift; zero-mean channels span
+    many binades, where a channel sum of x - shift rounded in plain fp32
+    would miss that floor."""
+    mu = None if centred else ((-1000.0, 1000.0) if dtype == "f32" else (-100.0, 100.0))
+    sigma = None if dtype == "f32" else (0.01, 10.0)
+    case = synth.BNCase(f"const_dy_{dtype}", (64, 8, 56, 56), dtype, mu_range=mu,
+                        sigma_range=sigma, seed=881 + 2 * centred + (dtype == "bf16"))
+    inp = synth.bn_inputs(case)
+    c = torch.tensor([1.0, 0.30078125, -2.5, 7.0, -0.0078125, 1.0, 3.0, -1.0])
+    inp["dy"] = c.view(1, 8, 1, 1).expand(inp["x"].shape).to(inp["x"].dtype).contiguous()
+    return case, inp
+
+
+@pytest.mark.parametrize("centred", [False, True], ids=["offset", "centred"])
+@pytest.mark.parametrize("path", ["composite", "phases", "misaligned"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bn_constant_dy_cancels(gbn, dtype, path, centred):
+    """The channel sums cancel to the last bit: dgamma, dbeta, k1, k2 within
+    the fp32 tolerance of the oracle (dgamma = 0 exactly there), on the
+    single-launch kernel, the two-launch kernels and their scalar form.  dx
+    is dy*scale + k2 plus rounding: within a few fp32 ulps of dy*scale."""
+    case, inp = _constant_dy_inputs(dtype, centred)
+    if path == "composite":
+        got = run_gpu(gbn, inp)
+    elif path == "phases":
+        got = _run_phases(gbn, inp)
+    else:
+        def misaligned(t):
+            buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+            buf[1:] = t.to(DEV).reshape(-1)
+            return buf[1:].view(t.shape)
+        xm, dym = misaligned(inp["x"]), misaligned(inp["dy"])
+        y, stats = gbn.bn_forward_train(xm, inp["gamma"].to(DEV), inp["beta"].to(DEV), None,
+                                        None, inp["momentum"], inp["eps"])
+        dx, grads = gbn.bn_backward(xm, dym, stats)
+        C = xm.shape[1]
+        gr = grads.cpu()
+        got = {"dx": dx.cpu(), "dgamma": gr[:C], "dbeta": gr[C:2 * C], "k1": gr[2 * C:3 * C],
+               "k2": gr[3 * C:]}
+    ref = run_oracle(inp)
+    assert np.max(np.abs(ref["dgamma"])) < 1e-7   # 0 up to the oracle's own float64 rounding
+    for k in ("dgamma", "dbeta", "k1", "k2"):
+        tol.check_f32(got[k], ref[k], f"constant dy {dtype} {path} {k}")
+    C = inp["x"].shape[1]
+    term = np.abs(_f64(inp["dy"][0, :, 0, 0]) * ref["scale"]).reshape(1, C, 1, 1)
+    err = np.abs(_f64(got["dx"]) - ref["dx"])
+    assert np.all(err <= 2.0 ** -20 * term + 1e-30), f"dx off by {err.max()}"
+
+
 def test_bn_apply_modes(gbn):
     case = synth.CASES["bn_ragged_f32"]
     inp = synth.bn_inputs(case)

@@ -367,6 +367,67 @@ int gbn_bn_finalize_dx(const void* x, const void* dy, int dtype, int64_t B, int6
                           true);
 }
 
+// ------------------------------------------------- BatchNorm, NHWC --
+
+static int nhwc_check(int dtype, int64_t M, int64_t C, bool training) {
+  if (dtype != GBN_F32 && dtype != GBN_BF16) return GBN_EDTYPE;
+  if (M < 0 || C < 0 || C > INT32_MAX || M > INT32_MAX) return GBN_EINVAL;
+  int64_t n;
+  if (!mul_ok(M, C, &n) || n > (LLONG_MAX >> 3)) return GBN_EINVAL;
+  if (training && C > 0 && M < 2) return GBN_EINVAL;
+  return GBN_OK;
+}
+
+size_t gbn_bn_nhwc_workspace_bytes(int64_t M, int64_t C, int device) {
+  if (nhwc_check(GBN_F32, M, C, false) != GBN_OK) return 0;
+  if (C == 0) return 256;
+  const DevInfo* dev = device_info(device);
+  if (!dev) return 0;
+  return nhwc_ws_bound(M, C, *dev);
+}
+
+int gbn_bn_nhwc_forward_train(const void* x, int dtype, int64_t M, int64_t C, const float* gamma,
+                              const float* beta, float* running_mean, float* running_var,
+                              float momentum, float eps, int act, float slope, void* y,
+                              float* stats, void* ws, size_t ws_bytes, void* stream) {
+  int rc = nhwc_check(dtype, M, C, true);
+  if (rc != GBN_OK) return rc;
+  if (!act_ok(act, slope)) return GBN_EINVAL;
+  if (C == 0) return GBN_OK;
+  if (x == nullptr || y == nullptr || stats == nullptr || ws == nullptr) return GBN_EINVAL;
+  if (!aligned(ws, 16) || !aligned(stats, 4)) return GBN_EALIGN;
+  if (!(eps >= 0.f) || momentum != momentum) return GBN_EINVAL;
+  const DevInfo* dev = device_info(-1);
+  if (!dev) return GBN_ECUDA;
+  const void* ptrs[2] = {x, y};
+  NhwcPlan p;
+  if (!nhwc_plan(M, C, bn_vec_width(dtype, C, ptrs, 2), *dev, &p)) return GBN_EINVAL;
+  if (ws_bytes < p.ws_bytes) return GBN_EWORKSPACE;
+  return to_status(nhwc_forward(p, dtype, x, y, gamma, beta, stats, running_mean, running_var,
+                                momentum, eps, act, slope, ws, static_cast<cudaStream_t>(stream)));
+}
+
+int gbn_bn_nhwc_backward(const void* x, const void* dy, int dtype, int64_t M, int64_t C,
+                         const float* stats, const float* beta, int act, float slope, void* dx,
+                         float* grads, void* ws, size_t ws_bytes, void* stream) {
+  int rc = nhwc_check(dtype, M, C, true);
+  if (rc != GBN_OK) return rc;
+  if (!act_ok(act, slope)) return GBN_EINVAL;
+  if (C == 0) return GBN_OK;
+  if (x == nullptr || dy == nullptr || dx == nullptr || stats == nullptr || grads == nullptr ||
+      ws == nullptr)
+    return GBN_EINVAL;
+  if (!aligned(ws, 16) || !aligned(stats, 4)) return GBN_EALIGN;
+  const DevInfo* dev = device_info(-1);
+  if (!dev) return GBN_ECUDA;
+  const void* ptrs[3] = {x, dy, dx};
+  NhwcPlan p;
+  if (!nhwc_plan(M, C, bn_vec_width(dtype, C, ptrs, 3), *dev, &p)) return GBN_EINVAL;
+  if (ws_bytes < p.ws_bytes) return GBN_EWORKSPACE;
+  return to_status(nhwc_backward(p, dtype, x, dy, dx, stats, beta, act, slope, grads, ws,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------ row-wise --
 
 static int row_check(int dtype, int64_t R, int64_t H) {

@@ -218,4 +218,23 @@ cudaError_t colsum_launch(const float* part, int nout, int nplanes, int G, int64
 // Set the kernels' dynamic shared memory limits (called from device_info).
 cudaError_t row_kernels_configure(int smem_optin);
 
+// -------------------------------------------- BatchNorm, channels last --
+
+struct NhwcPlan {
+  int64_t M = 0, C = 0;  // rows (N*H*W) and channels
+  int vec = 1;           // channels per vector (divides C)
+  int TX = 1;            // vectors per block row
+  int grid_y = 1;        // row slices
+  size_t ws_bytes = 0;   // partials [2][grid_y][C] float2
+};
+bool nhwc_plan(int64_t M, int64_t C, int vec, const DevInfo& dev, NhwcPlan* p);
+size_t nhwc_ws_bound(int64_t M, int64_t C, const DevInfo& dev);
+cudaError_t nhwc_forward(const NhwcPlan& p, int dtype, const void* x, void* y,
+                         const float* gamma, const float* beta, float* stats,
+                         float* running_mean, float* running_var, float momentum, float eps,
+                         int act, float slope, void* ws, cudaStream_t st);
+cudaError_t nhwc_backward(const NhwcPlan& p, int dtype, const void* x, const void* dy, void* dx,
+                          const float* stats, const float* beta, int act, float slope,
+                          float* grads, void* ws, cudaStream_t st);
+
 }  // namespace gbn

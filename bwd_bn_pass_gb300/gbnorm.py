@@ -75,6 +75,11 @@ _SIGNATURES = {
                                    _P, _SZ, _P]),
     "gbn_bn_grad_sums": (_INT, [_P, _P, _INT, _I64, _I64, _I64, _P, _P, _SZ, _P]),
     "gbn_bn_finalize_dx": (_INT, [_P, _P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
+    "gbn_bn_nhwc_workspace_bytes": (_SZ, [_I64, _I64, _INT]),
+    "gbn_bn_nhwc_forward_train": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _P, _F, _F, _INT, _F,
+                                         _P, _P, _P, _SZ, _P]),
+    "gbn_bn_nhwc_backward": (_INT, [_P, _P, _INT, _I64, _I64, _P, _P, _INT, _F, _P, _P, _P, _SZ,
+                                    _P]),
     "gbn_rowwise_workspace_bytes": (_SZ, [_I64, _I64, _INT, _INT, _INT]),
     "gbn_rmsnorm_backward": (_INT, [_P, _P, _P, _INT, _P, _I64, _I64, _P, _P, _P, _SZ, _P]),
     "gbn_layernorm_backward": (_INT, [_P, _P, _INT, _P, _P, _P, _I64, _I64, _P, _P, _P, _F,
@@ -350,6 +355,73 @@ def bn_finalize_dx(x, dy, stats, dx, grads, ws):
 
 
 # ------------------------------------------------------------ row-wise --
+
+def _nhwc_dims(x):
+    if x.dim() < 2 or not x.is_contiguous():
+        raise ValueError("channels-last BatchNorm wants a contiguous [..., C] tensor")
+    C = x.shape[-1]
+    return x.numel() // C if C else 0, C
+
+
+def bn_nhwc_workspace(x):
+    M, C = _nhwc_dims(x)
+    with torch.cuda.device(x.device):
+        n = lib().gbn_bn_nhwc_workspace_bytes(M, C, -1)
+    if n == 0:
+        raise ValueError(f"bad channels-last BatchNorm shape {tuple(x.shape)}")
+    return torch.empty(n, dtype=torch.uint8, device=x.device)
+
+
+def bn_nhwc_forward_train(x, gamma=None, beta=None, running_mean=None, running_var=None,
+                          momentum=0.1, eps=1e-5, *, y=None, stats=None, ws=None, act=None,
+                          slope=0.01):
+    """Channels-last training forward: x is a contiguous [..., C] tensor (e.g.
+    [N, H, W, C]); the channel is the last dimension.  Returns (y, stats)."""
+    code = _act_code(act)
+    _cuda(x, "x")
+    M, C = _nhwc_dims(x)
+    for name, t in (("gamma", gamma), ("beta", beta), ("running_mean", running_mean),
+                    ("running_var", running_var)):
+        _fp32_vec(t, name, C)
+    y = torch.empty_like(x) if y is None else _cuda(y, "y")
+    stats = bn_stats_tensor(C, x.device) if stats is None else _cuda(stats, "stats")
+    ws = bn_nhwc_workspace(x) if ws is None else _cuda(ws, "ws")
+    _same_device(x, ("y", y), ("stats", stats), ("ws", ws), ("gamma", gamma), ("beta", beta),
+                 ("running_mean", running_mean), ("running_var", running_var))
+    with torch.cuda.device(x.device):
+        st = lib().gbn_bn_nhwc_forward_train(
+            _ptr(x), _code(x.dtype), M, C, _ptr(gamma), _ptr(beta), _ptr(running_mean),
+            _ptr(running_var), float(momentum), float(eps), code, float(slope), _ptr(y),
+            _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(x.device))
+    _check("gbn_bn_nhwc_forward_train", st)
+    return y, stats
+
+
+def bn_nhwc_backward(x, dy, stats, *, dx=None, grads=None, ws=None, beta=None, act=None,
+                     slope=0.01):
+    """Channels-last training backward.  Returns (dx, grads) with
+    grads.view(4, C) = (dgamma, dbeta, k1, k2)."""
+    code = _act_code(act)
+    _cuda(x, "x")
+    _cuda(dy, "dy")
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    M, C = _nhwc_dims(x)
+    _fp32_vec(beta, "beta", C)
+    dx = torch.empty_like(x) if dx is None else _cuda(dx, "dx")
+    grads = (torch.empty(4 * C, dtype=torch.float32, device=x.device) if grads is None
+             else _cuda(grads, "grads"))
+    ws = bn_nhwc_workspace(x) if ws is None else _cuda(ws, "ws")
+    _same_device(x, ("dy", dy), ("stats", stats), ("dx", dx), ("grads", grads), ("ws", ws),
+                 ("beta", beta))
+    with torch.cuda.device(x.device):
+        st = lib().gbn_bn_nhwc_backward(
+            _ptr(x), _ptr(dy), _code(x.dtype), M, C, _ptr(stats), _ptr(beta), code,
+            float(slope), _ptr(dx), _ptr(grads), _ptr(ws), ws.numel() * ws.element_size(),
+            _stream(x.device))
+    _check("gbn_bn_nhwc_backward", st)
+    return dx, grads
+
 
 def rowwise_workspace_bytes(R, H, kind, dtype, device=None):
     dev = -1 if device is None else int(device)

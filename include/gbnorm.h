@@ -248,6 +248,40 @@ GBN_API int gbn_bn_finalize_dx(const void* x, const void* dy, int dtype, int64_t
                        void* stream);
 
 /* =========================================================================
+ * BatchNorm2d, training mode, channels last (NHWC)  ([P4]; "Part 2" act)
+ *
+ * x, y, dy, dx: [M, C] row-major in `dtype` with M = N*H*W and the channel
+ * innermost (a channels-last [N, H, W, C] tensor).  The statistics, the
+ * finalize, the centred apply, the backward finalize and the activation are
+ * those of the NCHW entry points, and stats / grads have the same layout
+ * (GBN_BN_STATS_FLOATS, GBN_BN_GRADS_FLOATS) with shift = x[0, c].  Three
+ * launches per direction: a row-streaming sum kernel writing per-block
+ * (hi, lo) partials for every channel, a finalize kernel (one warp per
+ * channel, fixed order), and the apply / dx kernel.  act / slope as for
+ * gbn_bn_forward_train_act (GBN_ACT_NONE for plain BatchNorm).  Requires
+ * M >= 2 and M < 2^31.  ws must be 16-byte aligned.                       */
+
+/* Workspace bytes for an NHWC forward or backward of this shape on `device`
+ * (-1: current): the partials, 16 * grid_y * C rounded up to 256.  Returns
+ * 0 on a bad shape or a CUDA error.                                        */
+GBN_API size_t gbn_bn_nhwc_workspace_bytes(int64_t M, int64_t C, int device);
+
+/* Training forward: writes y, stats (8*C floats) and the running update as
+ * gbn_bn_forward_train does.  y may alias x.                               */
+GBN_API int gbn_bn_nhwc_forward_train(const void* x, int dtype, int64_t M, int64_t C,
+                                      const float* gamma, const float* beta,
+                                      float* running_mean, float* running_var, float momentum,
+                                      float eps, int act, float slope, void* y, float* stats,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/* Training backward from the matching forward's stats (and its beta when an
+ * activation is fused): writes dx and grads (fp32 [4, C]).  dx may alias dy. */
+GBN_API int gbn_bn_nhwc_backward(const void* x, const void* dy, int dtype, int64_t M,
+                                 int64_t C, const float* stats, const float* beta, int act,
+                                 float slope, void* dx, float* grads, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* =========================================================================
  * Row-wise backward passes: RMSNorm ([P3]) and LayerNorm ([P2]).
  *
  * Tensors are [R, H] row-major in `dtype` unless stated.  One persistent

@@ -21,6 +21,8 @@ from .bn import (
     batch_norm_backward,
     batch_norm_act_forward_train,
     batch_norm_act_backward,
+    batch_norm_nhwc_forward_train,
+    batch_norm_nhwc_backward,
     activation,
     activation_gate,
     ACT_NONE,
@@ -44,6 +46,8 @@ __all__ = [
     "batch_norm_backward",
     "batch_norm_act_forward_train",
     "batch_norm_act_backward",
+    "batch_norm_nhwc_forward_train",
+    "batch_norm_nhwc_backward",
     "activation",
     "activation_gate",
     "rms_norm_rstd",

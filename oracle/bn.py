@@ -169,3 +169,34 @@ def batch_norm_act_backward(x, dy, gamma, beta, eps, act, slope=0.0):
     out = batch_norm_backward(x, gated, gamma, eps)
     out["pre"] = pre
     return out
+
+
+# Channels-last (NHWC) BatchNorm: the same definition with the channel as the
+# last axis.  x is [..., C]; the channel axis is moved to position 1 and back.
+
+def _to_channel_first(a):
+    return np.moveaxis(np.asarray(a, dtype=np.float64), -1, 1)
+
+
+def _to_channel_last(a):
+    return np.moveaxis(a, 1, -1)
+
+
+def batch_norm_nhwc_forward_train(x, gamma, beta, running_mean, running_var, momentum, eps,
+                                  act=ACT_NONE, slope=0.0):
+    """Training forward of act(BatchNorm(x)) for a channels-last x [..., C].
+    Returns the dict of batch_norm_forward_train (y channels-last)."""
+    out = batch_norm_act_forward_train(_to_channel_first(x), gamma, beta, running_mean,
+                                       running_var, momentum, eps, act, slope)
+    out["y"] = _to_channel_last(out["y"])
+    out["pre"] = _to_channel_last(out["pre"])
+    return out
+
+
+def batch_norm_nhwc_backward(x, dy, gamma, beta, eps, act=ACT_NONE, slope=0.0):
+    """Backward of act(BatchNorm(x)) for channels-last x, dy [..., C]."""
+    out = batch_norm_act_backward(_to_channel_first(x), _to_channel_first(dy), gamma, beta, eps,
+                                  act, slope)
+    out["dx"] = _to_channel_last(out["dx"])
+    out["pre"] = _to_channel_last(out["pre"])
+    return out

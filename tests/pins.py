@@ -214,9 +214,35 @@ def pin_bn_act_vs_torch(bn):
         _close(b["dbeta"], tb.grad.numpy(), what=f"act {act} dbeta")
 
 
+def pin_bn_nhwc_vs_torch(bn):
+    """Channels-last BatchNorm (x [N, H, W, C]) against torch float64 autograd
+    of F.batch_norm on the same data permuted by torch to [N, C, H, W]; all
+    four sizes differ, so a wrong axis fails on shape or values."""
+    r = _rng(41)
+    N, H, W, C = 3, 4, 5, 6
+    x = r.standard_normal((N, H, W, C)) * r.uniform(0.5, 2.0, C) + r.uniform(-5, 5, C)
+    dy = r.standard_normal((N, H, W, C))
+    gamma, beta = r.uniform(0.5, 1.5, C), r.uniform(-0.5, 0.5, C)
+    eps = 1e-5
+    for act, slope, fn in ((bn.ACT_NONE, 0.0, lambda t: t),
+                           (bn.ACT_RELU, 0.0, lambda t: F.relu(t))):
+        tx = torch.tensor(x, requires_grad=True)
+        tg = torch.tensor(gamma, requires_grad=True)
+        tb = torch.tensor(beta, requires_grad=True)
+        y = fn(F.batch_norm(tx.permute(0, 3, 1, 2), None, None, tg, tb, training=True, eps=eps))
+        y.permute(0, 2, 3, 1).backward(torch.tensor(dy))
+        f = bn.batch_norm_nhwc_forward_train(x, gamma, beta, np.zeros(C), np.ones(C), 0.1, eps,
+                                             act, slope)
+        _close(f["y"], y.permute(0, 2, 3, 1).detach().numpy(), what=f"nhwc {act} y")
+        b = bn.batch_norm_nhwc_backward(x, dy, gamma, beta, eps, act, slope)
+        _close(b["dx"], tx.grad.numpy(), what=f"nhwc {act} dx")
+        _close(b["dgamma"], tg.grad.numpy(), what=f"nhwc {act} dgamma")
+        _close(b["dbeta"], tb.grad.numpy(), what=f"nhwc {act} dbeta")
+
+
 BN_PINS = [pin_bn_forward_vs_torch, pin_bn_backward_vs_torch,
            pin_bn_finite_differences, pin_bn_invariants, pin_bn_running_ema,
-           pin_bn_exact_rational, pin_bn_act_vs_torch]
+           pin_bn_exact_rational, pin_bn_act_vs_torch, pin_bn_nhwc_vs_torch]
 
 
 # ------------------------------------------------------------------ RMSNorm

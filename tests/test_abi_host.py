@@ -121,6 +121,35 @@ def test_bn_act_argument_errors(gbn):
                                       0.0, A16, A16, A16, 1 << 20, NULL) == EDTYPE
 
 
+def test_bn_nhwc_argument_errors(gbn):
+    L = gbn.lib()
+
+    def fwd(x=A16, dtype=0, M=8, C=4, act=0, slope=0.0, y=A16, stats=A16, ws=A16, n=1 << 20,
+            eps=1e-5):
+        return L.gbn_bn_nhwc_forward_train(x, dtype, M, C, NULL, NULL, NULL, NULL, 0.1, eps, act,
+                                           slope, y, stats, ws, n, NULL)
+
+    def bwd(x=A16, dy=A16, dtype=0, M=8, C=4, stats=A16, dx=A16, grads=A16, ws=A16):
+        return L.gbn_bn_nhwc_backward(x, dy, dtype, M, C, stats, NULL, 0, 0.0, dx, grads, ws,
+                                      1 << 20, NULL)
+
+    assert fwd(dtype=5) == EDTYPE
+    assert fwd(M=-1) == EINVAL
+    assert fwd(M=1) == EINVAL                      # one row: no unbiased running var
+    assert fwd(M=1 << 31) == EINVAL                # per-channel count >= 2^31
+    assert fwd(act=9) == EINVAL
+    assert fwd(x=NULL) == EINVAL
+    assert fwd(stats=NULL) == EINVAL
+    assert fwd(ws=A4) == EALIGN
+    assert fwd(eps=float("nan")) == EINVAL
+    assert fwd(C=0) == OK                          # nothing to do
+    assert bwd(dy=NULL) == EINVAL
+    assert bwd(grads=NULL) == EINVAL
+    assert bwd(dtype=3) == EDTYPE
+    assert bwd(C=0) == OK
+    assert L.gbn_bn_nhwc_workspace_bytes(-1, 4, -1) == 0
+
+
 def _rms(L, dtype=1, R=4, H=64, dy=A16, x=A16, w=A16, rstd=A16, dx=A16, dw=A16, ws=A16):
     return L.gbn_rmsnorm_backward(dy, x, w, dtype, rstd, R, H, dx, dw, ws, 1 << 20, NULL)
 

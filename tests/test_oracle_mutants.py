@@ -39,6 +39,10 @@ MUTATIONS = [
      "gated = np.asarray(dy, dtype=np.float64)"),
     (obn, pins.BN_PINS, "return np.where(pre > 0, pre, float(slope) * pre)",
      "return np.where(pre > 0, pre, 0.0)"),
+    (obn, pins.BN_PINS, "return np.moveaxis(np.asarray(a, dtype=np.float64), -1, 1)",
+     "return np.asarray(a, dtype=np.float64).reshape(np.shape(a)[0], np.shape(a)[-1], -1)"),
+    (obn, pins.BN_PINS, 'out["dx"] = _to_channel_last(out["dx"])',
+     'out["dx"] = out["dx"].reshape(np.shape(x))'),
     # RMSNorm
     (orms, pins.RMS_PINS, "x * (rstd3 * row_sum / H)", "x * (rstd3 * row_sum)"),
     (orms, pins.RMS_PINS, "rstd3 = rstd * rstd * rstd", "rstd3 = rstd * rstd"),

@@ -12,8 +12,11 @@ One step = one pass of every hot-path operation over its workload:
 
 Also available through --ops (not part of the default step, whose
 operations are the configured workloads): rms_bf16_fwd, rms_f32_fwd
-(RMSNorm training forward [2048, 8192]) and ln_bf16_fwd (bias+dropout+add
-LayerNorm training forward [16*512, 1600]).
+(RMSNorm training forward [2048, 8192]), ln_bf16_fwd (bias+dropout+add
+LayerNorm training forward [16*512, 1600]), and the BatchNorm variants
+bn_relu_{f32,bf16}_{fwd,bwd} (fused ReLU), bn_nhwc_{f32,bf16}_{fwd,bwd}
+(channels-last, the same data permuted to [N,H,W,C]) and
+bn_relu_nhwc_{f32,bf16}_{fwd,bwd}.
 
 Every call goes through the C ABI (ctypes binding).  Each operation is timed
 with CUDA events on the stream it runs on, after an L2 flush (a 256 MB write
@@ -184,45 +187,55 @@ def build_ops(names, dev):
     ops = []
     for name in names:
         if name.startswith("bn_"):
+            # bn[_relu][_nhwc]_{f32,bf16}_{fwd,bwd}
             case = synth.CASES["bn_offset_f32" if "f32" in name else "bn_offset_bf16"]
+            act = "relu" if "_relu_" in name else None
+            nhwc = "_nhwc_" in name
             inp = synth.bn_inputs(case)
+            if nhwc:  # the same data, channels last
+                inp["x"] = inp["x"].permute(0, 2, 3, 1).contiguous()
+                inp["dy"] = inp["dy"].permute(0, 2, 3, 1).contiguous()
             hx, hdy = _pin(inp["x"]), _pin(inp["dy"])
             x, dy = hx.to(dev), hdy.to(dev)
             g, b = inp["gamma"].to(dev), inp["beta"].to(dev)
             rm, rv = inp["running_mean"].to(dev), inp["running_var"].to(dev)
-            C = x.shape[1]
+            C = x.shape[-1] if nhwc else x.shape[1]
             y = torch.empty_like(x)
             stats = G.bn_stats_tensor(C, dev)
-            ws = G.bn_workspace(x)
+            fwd_fn = G.bn_nhwc_forward_train if nhwc else G.bn_forward_train
+            bwd_fn = G.bn_nhwc_backward if nhwc else G.bn_backward
+            ws = G.bn_nhwc_workspace(x) if nhwc else G.bn_workspace(x)
             # a forward once so the backward has valid stats
-            G.bn_forward_train(x, g, b, rm, rv, case.momentum, case.eps, y=y, stats=stats,
-                               ws=ws)
+            fwd_fn(x, g, b, rm, rv, case.momentum, case.eps, y=y, stats=stats, ws=ws, act=act)
             T = _nbytes(x)
             small = _nbytes(g, b, rm, rv) + 4 * C * 4
-            shape = "x".join(map(str, case.shape))
+            shape = "x".join(map(str, x.shape))
+            kind = ("BatchNorm2d" + ("+ReLU" if act else "")
+                    + (" channels-last" if nhwc else ""))
+            key = "bn_forward_train" if name.endswith("fwd") else "bn_backward"
             if name.endswith("fwd"):
                 # the composite call a user makes: statistics, finalize and apply
                 phases = [
-                    ("bn_forward_train",
-                     lambda x=x, g=g, b=b, rm=rm, rv=rv, y=y, stats=stats, ws=ws, c=case:
-                     G.bn_forward_train(x, g, b, rm, rv, c.momentum, c.eps, y=y, stats=stats,
-                                        ws=ws)),
+                    (key,
+                     lambda x=x, g=g, b=b, rm=rm, rv=rv, y=y, stats=stats, ws=ws, c=case,
+                     f=fwd_fn, a=act:
+                     f(x, g, b, rm, rv, c.momentum, c.eps, y=y, stats=stats, ws=ws, act=a)),
                 ]
                 hy = torch.empty_like(hx).pin_memory()
-                ops.append(Op(name, f"BatchNorm2d fwd {case.dtype} [{shape}]", phases,
-                              2 * T + small, {"bn_forward_train": 2 * T + small}, 1,
+                ops.append(Op(name, f"{kind} fwd {case.dtype} [{shape}]", phases,
+                              2 * T + small, {key: 2 * T + small}, 3 if nhwc else 1,
                               [(hx, x)], [(y, hy)], None))
             else:
                 dx = torch.empty_like(x)
                 grads = torch.empty(4 * C, dtype=torch.float32, device=dev)
                 phases = [
-                    ("bn_backward", lambda x=x, dy=dy, s=stats, dx=dx, gr=grads, ws=ws:
-                     G.bn_backward(x, dy, s, dx=dx, grads=gr, ws=ws)),
+                    (key, lambda x=x, dy=dy, s=stats, dx=dx, gr=grads, ws=ws, b=b, f=bwd_fn,
+                     a=act: f(x, dy, s, dx=dx, grads=gr, ws=ws, beta=b if a else None, act=a)),
                 ]
                 hdx = torch.empty_like(hx).pin_memory()
                 ub = 3 * T + 8 * C * 4 + 4 * C * 4
-                ops.append(Op(name, f"BatchNorm2d bwd {case.dtype} [{shape}]", phases,
-                              ub, {"bn_backward": ub}, 1,
+                ops.append(Op(name, f"{kind} bwd {case.dtype} [{shape}]", phases,
+                              ub, {key: ub}, 3 if nhwc else 1,
                               [(hx, x), (hdy, dy)], [(dx, hdx)], None))
         elif name in ("rms_bf16_fwd", "rms_f32_fwd"):
             case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]

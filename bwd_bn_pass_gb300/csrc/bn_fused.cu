@@ -329,22 +329,24 @@ struct ActPar {
   float slope;
 };
 
-template <typename T, bool ACT>
+// ACT: GBN_ACT_* at compile time.  A ReLU gate (0 or 1) keeps bf16 dy
+// exact, so its per-vector sum stays exact too; a LeakyReLU gate rounds.
+template <typename T, int ACT>
 __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, const ActPar& ap,
                                         DF2& a0, DF2& a1) {
   constexpr int NP = Pairs16<T>::NP;
   f2 px[NP], pd[NP];
   Pairs16<T>::get(rx, px);
   Pairs16<T>::get(rd, pd);
-  constexpr bool kLocalDy = sizeof(T) == 2 && !ACT;
+  constexpr bool kLocalDy = sizeof(T) == 2 && ACT != GBN_ACT_LEAKY_RELU;
   f2 l0 = 0ull;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     const f2 d = f2_sub(px[k], sh2);
-    if constexpr (ACT) {
+    if constexpr (ACT != GBN_ACT_NONE) {
       const float2 pre = f2_unpack(f2_fma(f2_sub(d, ap.md2), ap.sc2, ap.be2));
-      pd[k] = f2_mul_rounded(pd[k], f2_pack(act_gate(pre.x, ap.act, ap.slope),
-                                            act_gate(pre.y, ap.act, ap.slope)));
+      pd[k] = f2_mul_rounded(pd[k], f2_pack(act_gate(pre.x, ACT, ap.slope),
+                                            act_gate(pre.y, ACT, ap.slope)));
     }
     if constexpr (kLocalDy)
       l0 = f2_add(l0, pd[k]);
@@ -414,14 +416,20 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
           fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a0, a1);
       } else if (a.act == GBN_ACT_NONE) {
         for (int v = ct; v < len; v += kFConsumers)
-          bwd_acc<T, false>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
-                            *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2,
-                            nsh2, ap, a0, a1);
+          bwd_acc<T, GBN_ACT_NONE>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
+                                   *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16),
+                                   sh2, nsh2, ap, a0, a1);
+      } else if (a.act == GBN_ACT_RELU) {
+        for (int v = ct; v < len; v += kFConsumers)
+          bwd_acc<T, GBN_ACT_RELU>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
+                                   *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16),
+                                   sh2, nsh2, ap, a0, a1);
       } else {
         for (int v = ct; v < len; v += kFConsumers)
-          bwd_acc<T, true>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),
-                           *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2,
-                           nsh2, ap, a0, a1);
+          bwd_acc<T, GBN_ACT_LEAKY_RELU>(
+              *reinterpret_cast<const uint4*>(st + (size_t)v * 16),
+              *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), sh2, nsh2, ap,
+              a0, a1);
       }
       // Release the slot only if phase 1 refills it; the last NS stages stay
       // resident for phase 2.

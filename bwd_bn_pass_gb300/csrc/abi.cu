@@ -3,6 +3,7 @@
 // Every entry point validates its arguments before touching CUDA, so an
 // argument error launches nothing and writes nothing; then it plans the
 // launch from cached device attributes and launches on the caller's stream.
+#include <atomic>
 #include <climits>
 #include <cstring>
 #include <mutex>
@@ -162,6 +163,13 @@ static int bn_prepare(int dtype, int64_t B, int64_t C, int64_t HW, bool training
 
 static bool bn_empty(int64_t B, int64_t C, int64_t HW) { return C == 0 || B == 0 || HW == 0; }
 
+// Inputs (x, and dy backward) below this many bytes per call run the
+// two-launch kernels even when the persistent kernel could take them: the
+// cooperative launch and its flag handshake cost more than the re-read they
+// save on small tensors (GB300: two-launch ahead up to ~100 MB, behind from
+// ~200 MB).
+static std::atomic<int64_t> g_fused_min_bytes{128ll << 20};
+
 // act one of GBN_ACT_*; LeakyReLU's slope finite.
 static bool act_ok(int act, float slope) {
   if (act == GBN_ACT_NONE || act == GBN_ACT_RELU) return true;
@@ -206,8 +214,10 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float2* part = static_cast<float2*>(const_cast<void*>(ws));
   BnFusedPlan fp;
-  if (with_stats_pass && aligned(x, 16) && aligned(y, 16) &&
-      bn_fused_plan(dtype, false, B, C, HW, *dev, &fp) && ws_bytes >= fp.ws_bytes)
+  const int64_t in_bytes = B * C * HW * (dtype == GBN_F32 ? 4 : 2);
+  if (with_stats_pass && in_bytes >= g_fused_min_bytes.load() && aligned(x, 16) &&
+      aligned(y, 16) && bn_fused_plan(dtype, false, B, C, HW, *dev, &fp) &&
+      ws_bytes >= fp.ws_bytes)
     return to_status(bn_fused_forward(fp, dtype, x, y, gamma, beta, stats, running_mean,
                                       running_var, momentum, eps, act, slope,
                                       const_cast<void*>(ws), dev->status, st));
@@ -244,6 +254,12 @@ int bn_forward_train_scratch(const void* x, int dtype, int64_t B, int64_t C, int
 }  // namespace gbn
 
 extern "C" {
+
+int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes) {
+  return g_fused_min_bytes.exchange(bytes < 0 ? 0 : bytes);
+}
+
+int64_t gbn_bn_persistent_min_bytes(void) { return g_fused_min_bytes.load(); }
 
 int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                          const float* gamma, const float* beta, float* running_mean,
@@ -326,8 +342,10 @@ static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float2* part = static_cast<float2*>(const_cast<void*>(ws));
   BnFusedPlan fp;
-  if (sums && finalize && aligned(x, 16) && aligned(dy, 16) && aligned(dx, 16) &&
-      bn_fused_plan(dtype, true, B, C, HW, *dev, &fp) && ws_bytes >= fp.ws_bytes)
+  const int64_t in_bytes = 2 * B * C * HW * (dtype == GBN_F32 ? 4 : 2);
+  if (sums && finalize && in_bytes >= g_fused_min_bytes.load() && aligned(x, 16) &&
+      aligned(dy, 16) && aligned(dx, 16) && bn_fused_plan(dtype, true, B, C, HW, *dev, &fp) &&
+      ws_bytes >= fp.ws_bytes)
     return to_status(bn_fused_backward(fp, dtype, x, dy, dx, stats, beta, act, slope, grads,
                                        const_cast<void*>(ws), dev->status, st));
   if (sums) {

@@ -13,8 +13,9 @@
 //   * every thread keeps double-fp32 sums for its VEC channels (two channels
 //     per packed fp32x2 register): sum d per element with TwoSum (and, for
 //     fp32, the rounding error of x - shift) so that sum d is exact; sum d^2
-//     over four rows in fp32 before its double-fp32 add; backward sum dy and
-//     sum dy*d per element with each product's FMA residual;
+//     over eight rows in fp32 before its double-fp32 add; backward sum dy*d
+//     per element with each product's FMA residual, and sum dy per element
+//     (fp32) or over four rows first (bf16, exact for 8-bit significands);
 //   * the TY thread rows are added in a fixed tree in shared memory and
 //     the block writes one (hi, lo) pair per channel and sum to
 //     partials[2][grid_y][C] -- no atomics;
@@ -34,7 +35,10 @@ namespace {
 
 constexpr int kNThreads = 256;
 constexpr int kNSumBlocksPerSm = 2;  // the sum kernels hold ~100 registers
-constexpr int kNRowsUnroll = 4;
+// Rows each thread loads before using them: 8 for the one-input kernels, 4
+// for the two-input ones (more ran slower there: register pressure).
+constexpr int kNRowsUnroll1 = 8;
+constexpr int kNRowsUnroll2 = 4;
 
 struct NhwcGeom {
   int64_t M;       // rows
@@ -144,10 +148,10 @@ __global__ void __launch_bounds__(kNThreads, kNSumBlocksPerSm)
       sh2[k] = pair_of<VEC>(sh, k);
       nsh2[k] = f2_sub(0ull, sh2[k]);
     }
-    for (int64_t r = r0 + ty; r < r1; r += (int64_t)kNRowsUnroll * g.TY) {
-      typename V::raw raw[kNRowsUnroll];
+    for (int64_t r = r0 + ty; r < r1; r += (int64_t)kNRowsUnroll1 * g.TY) {
+      typename V::raw raw[kNRowsUnroll1];
 #pragma unroll
-      for (int u = 0; u < kNRowsUnroll; ++u) {
+      for (int u = 0; u < kNRowsUnroll1; ++u) {
         const int64_t ru = r + (int64_t)u * g.TY;
         if (ru < r1) raw[u] = V::ld(x + ru * g.C + (int64_t)cv * VEC);
       }
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kNThreads, kNSumBlocksPerSm)
 #pragma unroll
       for (int k = 0; k < NP; ++k) l2[k] = 0ull;
 #pragma unroll
-      for (int u = 0; u < kNRowsUnroll; ++u) {
+      for (int u = 0; u < kNRowsUnroll1; ++u) {
         if (r + (int64_t)u * g.TY < r1) {
           float e[VEC];
           V::cvt(raw[u], e);
@@ -218,18 +222,25 @@ __global__ void __launch_bounds__(kNThreads, kNSumBlocksPerSm)
       sc2[k] = pair_of<VEC>(sc, k);
       be2[k] = pair_of<VEC>(be, k);
     }
-    for (int64_t r = r0 + ty; r < r1; r += (int64_t)kNRowsUnroll * g.TY) {
-      typename V::raw rx[kNRowsUnroll], rd[kNRowsUnroll];
+    for (int64_t r = r0 + ty; r < r1; r += (int64_t)kNRowsUnroll2 * g.TY) {
+      typename V::raw rx[kNRowsUnroll2], rd[kNRowsUnroll2];
 #pragma unroll
-      for (int u = 0; u < kNRowsUnroll; ++u) {
+      for (int u = 0; u < kNRowsUnroll2; ++u) {
         const int64_t ru = r + (int64_t)u * g.TY;
         if (ru < r1) {
           rx[u] = V::ld(x + ru * g.C + (int64_t)cv * VEC);
           rd[u] = V::ld(dy + ru * g.C + (int64_t)cv * VEC);
         }
       }
+      // bf16 dy (plain or ReLU-gated, so still bf16 values) is summed over
+      // the row group in fp32 first: exact for 8-bit significands within
+      // 2^14 of each other.
+      constexpr bool kLocalDy = sizeof(T) == 2 && ACT != GBN_ACT_LEAKY_RELU;
+      f2 l0[NP];
 #pragma unroll
-      for (int u = 0; u < kNRowsUnroll; ++u) {
+      for (int k = 0; k < NP; ++k) l0[k] = 0ull;
+#pragma unroll
+      for (int u = 0; u < kNRowsUnroll2; ++u) {
         if (r + (int64_t)u * g.TY < r1) {
           float ex[VEC], ed[VEC];
           V::cvt(rx[u], ex);
@@ -245,7 +256,10 @@ __global__ void __launch_bounds__(kNThreads, kNSumBlocksPerSm)
               dy2 = f2_mul_rounded(dy2, f2_pack(act_gate(pre.x, ACT, slope),
                                                 act_gate(pre.y, ACT, slope)));
             }
-            df2_add(p0[k], dy2);
+            if constexpr (kLocalDy)
+              l0[k] = f2_add(l0[k], dy2);
+            else
+              df2_add(p0[k], dy2);
             const f2 prod = f2_mul_rounded(dy2, d);
             df2_add(p1[k], prod);
             p1[k].lo = f2_add(p1[k].lo, f2_fma(dy2, d, prod ^ 0x8000000080000000ull));
@@ -256,6 +270,10 @@ __global__ void __launch_bounds__(kNThreads, kNSumBlocksPerSm)
             }
           }
         }
+      }
+      if constexpr (kLocalDy) {
+#pragma unroll
+        for (int k = 0; k < NP; ++k) df2_add(p0[k], l0[k]);
       }
     }
   }
@@ -326,6 +344,7 @@ __global__ void __launch_bounds__(kNThreads)
                     const float* __restrict__ stats, const float* __restrict__ grads,
                     const float* __restrict__ beta, float slope) {
   using V = Vec<T, VEC>;
+  constexpr int U = BWD ? kNRowsUnroll2 : kNRowsUnroll1;
   const int tx = threadIdx.x % g.TX, ty = threadIdx.x / g.TX;
   const int cv = blockIdx.x * g.TX + tx;
   if (cv >= g.Cv) return;
@@ -346,10 +365,10 @@ __global__ void __launch_bounds__(kNThreads)
       k2[k] = grads[3 * C + c];
     }
   }
-  for (int64_t r = r0 + ty; r < r1; r += (int64_t)kNRowsUnroll * g.TY) {
-    typename V::raw rx[kNRowsUnroll], rd[kNRowsUnroll];
+  for (int64_t r = r0 + ty; r < r1; r += (int64_t)U * g.TY) {
+    typename V::raw rx[U], rd[U];
 #pragma unroll
-    for (int u = 0; u < kNRowsUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t ru = r + (int64_t)u * g.TY;
       if (ru < r1) {
         rx[u] = V::ld(x + ru * C + (int64_t)cv * VEC);
@@ -357,7 +376,7 @@ __global__ void __launch_bounds__(kNThreads)
       }
     }
 #pragma unroll
-    for (int u = 0; u < kNRowsUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t ru = r + (int64_t)u * g.TY;
       if (ru < r1) {
         float e[VEC];

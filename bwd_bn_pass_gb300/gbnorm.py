@@ -59,6 +59,8 @@ _SIGNATURES = {
     "gbn_init": (_INT, [_INT]),
     "gbn_get_device_status": (_INT, [_INT, ctypes.POINTER(_INT), _INT]),
     "gbn_bn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
+    "gbn_bn_set_persistent_min_bytes": (_I64, [_I64]),
+    "gbn_bn_persistent_min_bytes": (_I64, []),
     "gbn_bn_forward_train": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                     _P, _P, _P, _SZ, _P]),
     "gbn_bn_forward_train_noalloc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F,
@@ -187,6 +189,17 @@ def get_device_status(device=None, clear=False):
 
 
 # ----------------------------------------------------------- BatchNorm --
+
+def bn_set_persistent_min_bytes(nbytes):
+    """Input bytes from which the composite BatchNorm calls take the
+    single-launch persistent kernel (process-wide); returns the previous
+    value."""
+    return lib().gbn_bn_set_persistent_min_bytes(int(nbytes))
+
+
+def bn_persistent_min_bytes():
+    return lib().gbn_bn_persistent_min_bytes()
+
 
 def bn_workspace_bytes(B, C, HW, device=None):
     dev = -1 if device is None else int(device)

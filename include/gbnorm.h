@@ -141,6 +141,19 @@ GBN_API int gbn_get_device_status(int device, int* status, int clear);
  * block slot once).  Returns 0 on a bad shape or a CUDA error.              */
 GBN_API size_t gbn_bn_workspace_bytes(int64_t B, int64_t C, int64_t HW, int device);
 
+/* The composite calls below (gbn_bn_forward_train[_act], gbn_bn_backward[_act],
+ * gbn_bn_forward_train_noalloc) run the single-launch persistent kernel
+ * only when the input bytes of the call (x forward; x and dy backward) are
+ * at least this threshold, and the two-launch kernels otherwise; both give
+ * results within the parity tolerance.  Default 128 MiB: on GB300 the
+ * cooperative launch and its flag handshake cost more than the re-read the
+ * persistent kernel saves on smaller tensors.  Sets the process-wide value
+ * (negative: 0, i.e. always when eligible) and returns the previous one.
+ * The pages have no counterpart: it is a tuning knob of this library.     */
+GBN_API int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes);
+/* The current threshold (bytes).                                           */
+GBN_API int64_t gbn_bn_persistent_min_bytes(void);
+
 /* Full training forward: stats pass + finalize/apply.  Writes y, stats
  * (8*C floats, see GBN_BN_STATS_FLOATS), and updates the running stats in
  * place: running_mean = (1-momentum)*running_mean + momentum*mean,

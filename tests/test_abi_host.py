@@ -150,6 +150,14 @@ def test_bn_nhwc_argument_errors(gbn):
     assert L.gbn_bn_nhwc_workspace_bytes(-1, 4, -1) == 0
 
 
+def test_bn_persistent_threshold(gbn):
+    L = gbn.lib()
+    prev = L.gbn_bn_set_persistent_min_bytes(12345)
+    assert prev >= 0
+    assert L.gbn_bn_set_persistent_min_bytes(-7) == 12345
+    assert L.gbn_bn_set_persistent_min_bytes(prev) == 0     # negative stored as 0
+
+
 def _rms(L, dtype=1, R=4, H=64, dy=A16, x=A16, w=A16, rstd=A16, dx=A16, dw=A16, ws=A16):
     return L.gbn_rmsnorm_backward(dy, x, w, dtype, rstd, R, H, dx, dw, ws, 1 << 20, NULL)
 

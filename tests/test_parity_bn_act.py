@@ -22,6 +22,20 @@ from . import tolerances as tol
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(autouse=True, params=["auto", "persistent"])
+def _bn_path(request, gbn):
+    """Every test runs twice: with the library's default size threshold for
+    the single-launch persistent kernel, and with the threshold at 0 so that
+    the persistent kernel takes every eligible shape, small ones included."""
+    if request.param == "persistent":
+        prev = gbn.bn_set_persistent_min_bytes(0)
+        yield
+        gbn.bn_set_persistent_min_bytes(prev)
+    else:
+        yield
+
+
 DEV = "cuda:0"
 ACTS = {"relu": (oracle.ACT_RELU, 0.0), "leaky_relu": (oracle.ACT_LEAKY_RELU, 0.1)}
 

@@ -283,13 +283,15 @@ cudaError_t launch_fast(const RowPlan& p, const RmsArgs& a, cudaStream_t st) {
 }
 
 // Instances: (KV, RB, min blocks per SM).  The plan picks RB = 2 for short
-// rows and 2 blocks per SM whenever the columns a thread owns fit.
+// rows and for two-vector rows (then one block per SM), and 2 blocks per SM
+// whenever the columns a thread owns fit.
 template <typename T>
 cudaError_t launch_typed(const RowPlan& p, const RmsArgs& a, cudaStream_t st) {
   if (!p.fast) {
     constexpr bool COMP = sizeof(T) == 4;
     return launch(rms_bwd_generic_kernel<T, COMP>, dim3(p.G), dim3(p.threads), 0, st, false, a);
   }
+  if (p.rb == 2 && p.kv == 2) return launch_fast<T, 2, 2, 1>(p, a, st);
   if (p.rb == 2) return launch_fast<T, 1, 2, 2>(p, a, st);
   switch (p.kv) {
     case 1: return launch_fast<T, 1, 1, 2>(p, a, st);
@@ -310,6 +312,7 @@ template <typename T>
 cudaError_t set_smem_all(int bytes) {
   cudaError_t e = cudaSuccess, r;
   if ((r = set_smem<T, 1, 2, 2>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 2, 2, 1>(bytes)) != cudaSuccess) e = r;
   if ((r = set_smem<T, 1, 1, 2>(bytes)) != cudaSuccess) e = r;
   if ((r = set_smem<T, 2, 1, 2>(bytes)) != cudaSuccess) e = r;
   if ((r = set_smem<T, 3, 1, 1>(bytes)) != cudaSuccess) e = r;

@@ -111,6 +111,10 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
     int cand[3][2];
     int ncand = 0;
     if (kind == GBN_ROW_RMS) {
+      // Two-vector rows (e.g. 8192 bf16): two rows per stage at one block
+      // per SM amortise the per-row barrier and bookkeeping over twice the
+      // elements (29.3 vs 32.4 us at [2048, 8192] bf16).
+      if (kv == 2) cand[ncand][0] = 2, cand[ncand++][1] = 1;
       cand[ncand][0] = kv == 1 ? 2 : 1;
       cand[ncand++][1] = kv <= 2 ? 2 : 1;
     } else if (kv == 1 && threads <= 256) {

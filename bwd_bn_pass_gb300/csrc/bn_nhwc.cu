@@ -23,7 +23,8 @@
 //     launch) adds the grid_y partials in a fixed order and writes stats /
 //     grads and the running statistics with the NCHW path's formulas;
 //   * the apply / dx kernel (programmatic dependent launch) reads the
-//     per-channel parameters once per thread and streams the rows again.
+//     per-channel parameters once per thread and streams the rows again,
+//     each slice from its end (the part the sum kernel read last).
 // Three launches per direction; x (and dy) are read twice.
 #include "bn_finalize.cuh"
 #include "gbn_common.cuh"
@@ -365,20 +366,24 @@ __global__ void __launch_bounds__(kNThreads)
       k2[k] = grads[3 * C + c];
     }
   }
-  for (int64_t r = r0 + ty; r < r1; r += (int64_t)U * g.TY) {
+  // This thread's rows r0 + ty + j*TY, j < n, walked from the last: the
+  // sum kernel read every slice front to back, so the slice tails are the
+  // likeliest to still be in L2.
+  const int64_t n = r1 - r0 > ty ? (r1 - r0 - ty + g.TY - 1) / g.TY : 0;
+  for (int64_t jb = n - 1; jb >= 0; jb -= U) {
     typename V::raw rx[U], rd[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t ru = r + (int64_t)u * g.TY;
-      if (ru < r1) {
+      const int64_t ru = r0 + ty + (jb - u) * g.TY;
+      if (jb - u >= 0) {
         rx[u] = V::ld(x + ru * C + (int64_t)cv * VEC);
         if constexpr (BWD) rd[u] = V::ld(dy + ru * C + (int64_t)cv * VEC);
       }
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int64_t ru = r + (int64_t)u * g.TY;
-      if (ru < r1) {
+      const int64_t ru = r0 + ty + (jb - u) * g.TY;
+      if (jb - u >= 0) {
         float e[VEC];
         V::cvt(rx[u], e);
         if constexpr (!BWD) {

@@ -425,6 +425,24 @@ int gbn_bn_nhwc_forward_train(const void* x, int dtype, int64_t M, int64_t C, co
                                 momentum, eps, act, slope, ws, static_cast<cudaStream_t>(stream)));
 }
 
+int gbn_bn_nhwc_apply(const void* x, int dtype, int64_t M, int64_t C, const float* stats,
+                      const float* mean, const float* scale, const float* beta, int act,
+                      float slope, void* y, void* stream) {
+  int rc = nhwc_check(dtype, M, C, false);
+  if (rc != GBN_OK) return rc;
+  if (!act_ok(act, slope)) return GBN_EINVAL;
+  if (C == 0 || M == 0) return GBN_OK;
+  if (x == nullptr || y == nullptr) return GBN_EINVAL;
+  if (stats == nullptr && (mean == nullptr || scale == nullptr)) return GBN_EINVAL;
+  const DevInfo* dev = device_info(-1);
+  if (!dev) return GBN_ECUDA;
+  const void* ptrs[2] = {x, y};
+  NhwcPlan p;
+  if (!nhwc_plan(M, C, bn_vec_width(dtype, C, ptrs, 2), *dev, &p)) return GBN_EINVAL;
+  return to_status(nhwc_apply(p, dtype, x, y, stats, mean, scale, beta, act, slope,
+                              static_cast<cudaStream_t>(stream)));
+}
+
 int gbn_bn_nhwc_backward(const void* x, const void* dy, int dtype, int64_t M, int64_t C,
                          const float* stats, const float* beta, int act, float slope, void* dx,
                          float* grads, void* ws, size_t ws_bytes, void* stream) {

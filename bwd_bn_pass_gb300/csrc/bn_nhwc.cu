@@ -343,7 +343,8 @@ template <typename T, int VEC, int ACT, bool BWD>
 __global__ void __launch_bounds__(kNThreads)
     nhwc_out_kernel(const T* __restrict__ x, const T* dy, T* out, NhwcGeom g,
                     const float* __restrict__ stats, const float* __restrict__ grads,
-                    const float* __restrict__ beta, float slope) {
+                    const float* __restrict__ beta, float slope, const float* __restrict__ imean,
+                    const float* __restrict__ iscale) {
   using V = Vec<T, VEC>;
   constexpr int U = BWD ? kNRowsUnroll2 : kNRowsUnroll1;
   const int tx = threadIdx.x % g.TX, ty = threadIdx.x / g.TX;
@@ -357,9 +358,15 @@ __global__ void __launch_bounds__(kNThreads)
 #pragma unroll
   for (int k = 0; k < VEC; ++k) {
     const int64_t c = (int64_t)cv * VEC + k;
-    sh[k] = stats[4 * C + c];
-    md[k] = stats[5 * C + c];
-    sc[k] = stats[3 * C + c];
+    if (stats != nullptr) {
+      sh[k] = stats[4 * C + c];
+      md[k] = stats[5 * C + c];
+      sc[k] = stats[3 * C + c];
+    } else {  // inference: (x - mean)*scale + beta from the given vectors
+      sh[k] = imean[c];
+      md[k] = 0.f;
+      sc[k] = iscale[c];
+    }
     be[k] = beta ? beta[c] : 0.f;
     if constexpr (BWD) {
       k1[k] = grads[2 * C + c];
@@ -456,25 +463,26 @@ template <typename T, int VEC> struct NOut {
   template <bool BWD>
   static cudaError_t go(const NhwcPlan& p, const void* x, const void* dy, void* out,
                         const float* stats, const float* grads, const float* beta, int act,
-                        float slope, cudaStream_t st) {
+                        float slope, const float* imean, const float* iscale, cudaStream_t st) {
     const T* xt = static_cast<const T*>(x);
     const T* dt = static_cast<const T*>(dy);
     T* ot = static_cast<T*>(out);
     if (act == GBN_ACT_RELU)
       return launch(nhwc_out_kernel<T, VEC, GBN_ACT_RELU, BWD>, sum_grid(p), dim3(kNThreads), 0,
-                    st, true, xt, dt, ot, make_geom(p), stats, grads, beta, slope);
+                    st, true, xt, dt, ot, make_geom(p), stats, grads, beta, slope, imean,
+                    iscale);
     if (act == GBN_ACT_LEAKY_RELU)
       return launch(nhwc_out_kernel<T, VEC, GBN_ACT_LEAKY_RELU, BWD>, sum_grid(p),
                     dim3(kNThreads), 0, st, true, xt, dt, ot, make_geom(p), stats, grads, beta,
-                    slope);
+                    slope, imean, iscale);
     return launch(nhwc_out_kernel<T, VEC, GBN_ACT_NONE, BWD>, sum_grid(p), dim3(kNThreads), 0,
-                  st, true, xt, dt, ot, make_geom(p), stats, grads, beta, slope);
+                  st, true, xt, dt, ot, make_geom(p), stats, grads, beta, slope, imean, iscale);
   }
   static cudaError_t run(const NhwcPlan& p, bool bwd, const void* x, const void* dy, void* out,
                          const float* stats, const float* grads, const float* beta, int act,
-                         float slope, cudaStream_t st) {
-    return bwd ? go<true>(p, x, dy, out, stats, grads, beta, act, slope, st)
-               : go<false>(p, x, dy, out, stats, grads, beta, act, slope, st);
+                         float slope, const float* imean, const float* iscale, cudaStream_t st) {
+    return bwd ? go<true>(p, x, dy, out, stats, grads, beta, act, slope, imean, iscale, st)
+               : go<false>(p, x, dy, out, stats, grads, beta, act, slope, imean, iscale, st);
   }
 };
 
@@ -551,7 +559,15 @@ cudaError_t nhwc_forward(const NhwcPlan& p, int dtype, const void* x, void* y,
   if (e != cudaSuccess) return e;
   return ndispatch<NOut>(p, dtype, false, x, static_cast<const void*>(nullptr), y,
                          static_cast<const float*>(stats), static_cast<const float*>(nullptr),
-                         beta, act, slope, st);
+                         beta, act, slope, static_cast<const float*>(nullptr),
+                         static_cast<const float*>(nullptr), st);
+}
+
+cudaError_t nhwc_apply(const NhwcPlan& p, int dtype, const void* x, void* y, const float* stats,
+                       const float* mean, const float* scale, const float* beta, int act,
+                       float slope, cudaStream_t st) {
+  return ndispatch<NOut>(p, dtype, false, x, static_cast<const void*>(nullptr), y, stats,
+                         static_cast<const float*>(nullptr), beta, act, slope, mean, scale, st);
 }
 
 cudaError_t nhwc_backward(const NhwcPlan& p, int dtype, const void* x, const void* dy, void* dx,
@@ -566,7 +582,8 @@ cudaError_t nhwc_backward(const NhwcPlan& p, int dtype, const void* x, const voi
              static_cast<const float2*>(part), stats, grads);
   if (e != cudaSuccess) return e;
   return ndispatch<NOut>(p, dtype, true, x, dy, dx, stats, static_cast<const float*>(grads),
-                         beta, act, slope, st);
+                         beta, act, slope, static_cast<const float*>(nullptr),
+                         static_cast<const float*>(nullptr), st);
 }
 
 }  // namespace gbn

@@ -233,6 +233,12 @@ cudaError_t nhwc_forward(const NhwcPlan& p, int dtype, const void* x, void* y,
                          const float* gamma, const float* beta, float* stats,
                          float* running_mean, float* running_var, float momentum, float eps,
                          int act, float slope, void* ws, cudaStream_t st);
+// y = act(((x - shift) - (mean - shift))*scale + beta) from a training
+// stats buffer, or (stats NULL) act((x - mean)*scale + beta) from
+// per-channel mean and scale.
+cudaError_t nhwc_apply(const NhwcPlan& p, int dtype, const void* x, void* y, const float* stats,
+                       const float* mean, const float* scale, const float* beta, int act,
+                       float slope, cudaStream_t st);
 cudaError_t nhwc_backward(const NhwcPlan& p, int dtype, const void* x, const void* dy, void* dx,
                           const float* stats, const float* beta, int act, float slope,
                           float* grads, void* ws, cudaStream_t st);

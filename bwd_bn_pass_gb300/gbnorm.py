@@ -80,6 +80,7 @@ _SIGNATURES = {
     "gbn_bn_nhwc_workspace_bytes": (_SZ, [_I64, _I64, _INT]),
     "gbn_bn_nhwc_forward_train": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _P, _F, _F, _INT, _F,
                                          _P, _P, _P, _SZ, _P]),
+    "gbn_bn_nhwc_apply": (_INT, [_P, _INT, _I64, _I64, _P, _P, _P, _P, _INT, _F, _P, _P]),
     "gbn_bn_nhwc_backward": (_INT, [_P, _P, _INT, _I64, _I64, _P, _P, _INT, _F, _P, _P, _P, _SZ,
                                     _P]),
     "gbn_rowwise_workspace_bytes": (_SZ, [_I64, _I64, _INT, _INT, _INT]),
@@ -408,6 +409,24 @@ def bn_nhwc_forward_train(x, gamma=None, beta=None, running_mean=None, running_v
             _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(), _stream(x.device))
     _check("gbn_bn_nhwc_forward_train", st)
     return y, stats
+
+
+def bn_nhwc_apply(x, beta=None, *, stats=None, mean=None, scale=None, y=None, act=None,
+                  slope=0.01):
+    """Channels-last centred apply from a training stats buffer or from
+    per-channel mean / scale (inference), optionally through ``act``."""
+    code = _act_code(act)
+    _cuda(x, "x")
+    M, C = _nhwc_dims(x)
+    for name, t in (("beta", beta), ("mean", mean), ("scale", scale)):
+        _fp32_vec(t, name, C)
+    y = torch.empty_like(x) if y is None else _cuda(y, "y")
+    with torch.cuda.device(x.device):
+        st = lib().gbn_bn_nhwc_apply(_ptr(x), _code(x.dtype), M, C, _ptr(stats), _ptr(mean),
+                                     _ptr(scale), _ptr(beta), code, float(slope), _ptr(y),
+                                     _stream(x.device))
+    _check("gbn_bn_nhwc_apply", st)
+    return y
 
 
 def bn_nhwc_backward(x, dy, stats, *, dx=None, grads=None, ws=None, beta=None, act=None,

@@ -287,6 +287,14 @@ GBN_API int gbn_bn_nhwc_forward_train(const void* x, int dtype, int64_t M, int64
                                       float eps, int act, float slope, void* y, float* stats,
                                       void* ws, size_t ws_bytes, void* stream);
 
+/* Centred apply (optionally through act) for channels-last x, as
+ * gbn_bn_apply_act: from a training stats buffer when `stats` is non-NULL,
+ * else from per-channel mean and scale (fp32 [C], e.g. the running mean and
+ * gamma/sqrt(running_var + eps)).  No workspace.  y may alias x.          */
+GBN_API int gbn_bn_nhwc_apply(const void* x, int dtype, int64_t M, int64_t C,
+                              const float* stats, const float* mean, const float* scale,
+                              const float* beta, int act, float slope, void* y, void* stream);
+
 /* Training backward from the matching forward's stats (and its beta when an
  * activation is fused): writes dx and grads (fp32 [4, C]).  dx may alias dy. */
 GBN_API int gbn_bn_nhwc_backward(const void* x, const void* dy, int dtype, int64_t M,

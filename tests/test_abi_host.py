@@ -148,6 +148,9 @@ def test_bn_nhwc_argument_errors(gbn):
     assert bwd(dtype=3) == EDTYPE
     assert bwd(C=0) == OK
     assert L.gbn_bn_nhwc_workspace_bytes(-1, 4, -1) == 0
+    assert L.gbn_bn_nhwc_apply(A16, 0, 8, 4, NULL, NULL, NULL, NULL, 0, 0.0, A16, NULL) == EINVAL
+    assert L.gbn_bn_nhwc_apply(A16, 0, 8, 4, A16, NULL, NULL, NULL, 5, 0.0, A16, NULL) == EINVAL
+    assert L.gbn_bn_nhwc_apply(A16, 0, 0, 4, NULL, NULL, NULL, NULL, 0, 0.0, A16, NULL) == OK
 
 
 def test_bn_persistent_threshold(gbn):

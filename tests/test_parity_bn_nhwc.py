@@ -206,3 +206,38 @@ def test_nhwc_matches_nchw_statistics(gbn):
     _, s2 = gbn.bn_nhwc_forward_train(_nhwc(x), None, None, None, None, 0.1, inp["eps"])
     C = x.shape[1]
     tol.check_f32(s2[:4 * C].cpu(), _f64(s1[:4 * C]), "nhwc vs nchw stats")
+
+
+@pytest.mark.parametrize("act", [None, "relu", "leaky_relu"])
+def test_nhwc_apply_modes(gbn, act):
+    """Apply from a training stats buffer equals the training forward's y
+    bit for bit; the inference form matches the oracle's apply."""
+    case = synth.BNCase("nhwc_apply", (6, 48, 9, 11), "f32", mu_range=(-100.0, 100.0),
+                        seed=1009)
+    inp = nhwc_inputs(case)
+    slope = ACTS[act][1]
+    x = inp["x"].to(DEV)
+    g, b = inp["gamma"].to(DEV), inp["beta"].to(DEV)
+    y, stats = gbn.bn_nhwc_forward_train(x, g, b, None, None, 0.1, 1e-5, act=act, slope=slope)
+    y2 = gbn.bn_nhwc_apply(x, b, stats=stats, act=act, slope=slope)
+    assert torch.equal(y, y2)
+    r = np.random.default_rng(9)
+    C = x.shape[-1]
+    rmean = torch.tensor(r.uniform(-100, 100, C), dtype=torch.float32)
+    rvar = torch.tensor(r.uniform(0.5, 2.0, C), dtype=torch.float32)
+    scale = (inp["gamma"].double() / torch.sqrt(rvar.double() + 1e-5)).float()
+    yi = gbn.bn_nhwc_apply(x, b, mean=rmean.to(DEV), scale=scale.to(DEV), act=act, slope=slope)
+    x64 = np.moveaxis(_f64(inp["x"]), -1, 1)
+    pre = oracle.batch_norm_apply(x64, _f64(rmean), _f64(scale), _f64(inp["beta"]))
+    ref = np.moveaxis(oracle.activation(pre, ACTS[act][0], slope), 1, -1)
+    tol.check_f32(yi, ref, f"nhwc inference apply {act}")
+
+
+@pytest.mark.parametrize("dtype,shape", [("f32", (2, 1, 1, 1)), ("bf16", (1, 1, 2, 3)),
+                                         ("bf16", (3, 5000, 1, 2)), ("f32", (2, 7, 1, 1))])
+def test_nhwc_edge_shapes(gbn, dtype, shape):
+    """Two rows only, one channel, 5000 channels (20 column tiles of 32
+    vectors), a 1x1 image."""
+    case = synth.BNCase(f"nhwc_edge_{shape}", shape, dtype, seed=1013 + shape[1])
+    inp = nhwc_inputs(case)
+    compare(run_gpu(gbn, inp), run_oracle(inp), dtype, what=f"nhwc edge {shape}")

@@ -130,6 +130,14 @@ int gbn_get_device_status(int device, int* status, int clear) {
   return GBN_OK;
 }
 
+int gbn_selftest_bounded_wait(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > 2000000000ll) return GBN_EINVAL;
+  const DevInfo* dev = device_info(-1);
+  if (!dev) return GBN_ECUDA;
+  return to_status(selftest_bounded_wait(dev->status, (uint64_t)limit_ns,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 // ----------------------------------------------------------- BatchNorm --
 
 size_t gbn_bn_workspace_bytes(int64_t B, int64_t C, int64_t HW, int device) {

@@ -218,6 +218,11 @@ cudaError_t colsum_launch(const float* part, int nout, int nplanes, int G, int64
 // Set the kernels' dynamic shared memory limits (called from device_info).
 cudaError_t row_kernels_configure(int smem_optin);
 
+// Launches one block that waits on an mbarrier nothing completes, through
+// the library's bounded wait, for at most limit_ns; the expired wait sets
+// GBN_DEV_WAIT_TIMEOUT in *status.
+cudaError_t selftest_bounded_wait(int* status, uint64_t limit_ns, cudaStream_t st);
+
 // -------------------------------------------- BatchNorm, channels last --
 
 struct NhwcPlan {

@@ -58,6 +58,7 @@ _SIGNATURES = {
     "gbn_status_string": (ctypes.c_char_p, [_INT]),
     "gbn_init": (_INT, [_INT]),
     "gbn_get_device_status": (_INT, [_INT, ctypes.POINTER(_INT), _INT]),
+    "gbn_selftest_bounded_wait": (_INT, [_I64, _P]),
     "gbn_bn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "gbn_bn_set_persistent_min_bytes": (_I64, [_I64]),
     "gbn_bn_persistent_min_bytes": (_I64, []),
@@ -187,6 +188,15 @@ def get_device_status(device=None, clear=False):
     v = ctypes.c_int(0)
     _check("gbn_get_device_status", lib().gbn_get_device_status(dev, ctypes.byref(v), int(clear)))
     return v.value
+
+
+def selftest_bounded_wait(limit_ns=50_000_000, device=None):
+    """Launch the bounded-wait self-test (a wait nothing satisfies, given up
+    after `limit_ns`) on the current stream of `device`."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    with torch.cuda.device(dev):
+        _check("gbn_selftest_bounded_wait",
+               lib().gbn_selftest_bounded_wait(int(limit_ns), _stream(dev)))
 
 
 # ----------------------------------------------------------- BatchNorm --

@@ -112,6 +112,15 @@ GBN_API const char* gbn_status_string(int status);
  * capturing a CUDA graph.  Returns GBN_OK or GBN_ECUDA.                     */
 GBN_API int gbn_init(int device);
 
+/* The pages have no counterpart: a self-test of the failure detection.  It
+ * launches one block on `stream` that waits, through the bounded wait every
+ * ring and flag wait of the library uses, on a barrier nothing completes;
+ * after about limit_ns nanoseconds (0 < limit_ns <= 2e9) the wait gives up
+ * and sets GBN_DEV_WAIT_TIMEOUT in the current device's status word, and
+ * the kernel returns.  Read and clear the word with gbn_get_device_status.
+ * Nothing faults, traps or hangs; the context stays usable.               */
+GBN_API int gbn_selftest_bounded_wait(int64_t limit_ns, void* stream);
+
 /* Read the device status word of `device` (-1: current) into *status, a
  * HOST pointer (bit set of GBN_DEV_*; 0 = no device-side error), and clear it
  * when `clear` is nonzero.  Synchronises with the device (it is a copy).     */

@@ -528,9 +528,16 @@ def run_graph(ops, stream, dev, steps, world, flush_l2):
             if it > 0:
                 times.append(a.elapsed_time(b) * 1e-3)
     except Exception as exc:  # reported, never fatal: `value` stands alone
-        return {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
+        failure = f"{type(exc).__name__}: {exc}"[:200]
+        times = [math.inf]
+    else:
+        failure = None
+    # every rank takes part in the aggregation, a failed one with an
+    # infinite time, so that no rank waits on a collective the others skip
     t = statistics.mean(times)
     job_s, job_bytes = aggregate(t, sum(op.unique_bytes for op in ops), world)
+    if failure is not None or not math.isfinite(job_s):
+        return {"unavailable": failure or "graph replay failed on another rank"}
     return {"value": round(job_bytes / job_s / 1e9, 1), "unit": UNIT,
             "ms_per_step": round(job_s * 1e3, 4),
             "note": "whole step in one CUDA graph replay; L2 flushed before each replay"}

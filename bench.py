@@ -25,7 +25,9 @@ through the composite calls (bn_forward_train, bn_backward): one launch of the
 persistent kernel for inputs of 128 MiB and more, two launches below.
 value = unique bytes of every input and
 output tensor of the step / summed device time (the effective-bandwidth
-convention), in GB/s, over all ranks.
+convention), in GB/s, over all ranks.  Each op also gets a warm-L2 time
+(the same calls back to back, no flush; labelled, not used in value), and
+the oracle baseline is reported on one thread and on every host core.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--ops a,b,...] [--no-e2e] [--no-cpu-baseline]
@@ -446,6 +448,25 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": dbytes,
                 "traffic": recorded_traffic(f"{dop}:{dphase}")}
 
+    # Warm-L2 figures, labelled as such and not part of `value`: each op
+    # called back to back without the flush, so whatever fits in L2 stays.
+    warm = {}
+    for op in ops:
+        for _ in range(2):
+            for _, fn in op.phases:
+                fn()
+        evs = []
+        for _ in range(max(args.steps, 5)):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _, fn in op.phases:
+                fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        warm[op.name] = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e-3
+
     ops_out = {}
     for op in ops:
         t = statistics.mean(per_op[op.name])
@@ -457,6 +478,8 @@ def run_ours(args, rank, world, local_rank):
             "frac_of_measured_peak": round(op.unique_bytes / t / 1e9 / peak, 4),
             "phases_us": {p: round(statistics.mean(per_phase[(op.name, p)]) * 1e6, 2)
                           for p, _ in op.phases},
+            "us_warm_l2": round(warm[op.name] * 1e6, 2),
+            "eff_gbs_warm_l2": round(op.unique_bytes / warm[op.name] / 1e9, 1),
         }
 
     graph = run_graph(ops, stream, dev, args.steps, world, flush_l2)
@@ -476,6 +499,8 @@ def run_ours(args, rank, world, local_rank):
             "l2": "before every operation: 256 MB write + 256 MB read of another buffer "
                   "(outside the timed events; L2 left clean)",
             "timing": "CUDA events per operation on the launching stream; sum over ops",
+            "warm_l2": "ops.*.us_warm_l2: the same calls back to back without the flush "
+                       "(labelled, not used in value)",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },
         "pct_of_measured_peak": round(100 * value / world / peak, 2),
@@ -593,34 +618,43 @@ def run_e2e(ops, stream, dev, steps, world):
 class OracleSample:
     """A bounded sample of every op's workload, prepared once as float64
     arrays for the oracle: BatchNorm on the first `bn_channels` channels (all
-    batches and pixels), RMSNorm / LayerNorm on the first rows.  `time_pass`
-    runs the oracle once over all ops and returns (unique storage bytes of
-    the sample, seconds of oracle time)."""
+    batches and pixels), RMSNorm / LayerNorm on the first rows.  Each op is
+    split into independent units (BatchNorm channels, rows), so the sample
+    can also be cut into shards for several host threads.  `time_pass` runs
+    the oracle once over all ops on one thread and returns (unique storage
+    bytes of the sample, seconds of oracle time)."""
 
     def __init__(self, bn_f32_channels, bn_bf16_channels, rms_rows, ln_rows):
         import numpy as np
         import oracle
         from bwd_bn_pass_gb300 import synth
 
-        self.items = []
+        self.items = []  # (name, units, storage bytes per unit, make(lo, hi) -> callable)
         self.desc = {}
         for name in OPS_ALL:
             if name.startswith("bn_"):
                 case = synth.CASES["bn_offset_f32" if "f32" in name else "bn_offset_bf16"]
                 k = bn_f32_channels if "f32" in name else bn_bf16_channels
                 inp = synth.bn_inputs(case)
-                x = inp["x"][:, :k].double().numpy()
-                dy = inp["dy"][:, :k].double().numpy()
+                x = np.ascontiguousarray(inp["x"][:, :k].double().numpy())
+                dy = np.ascontiguousarray(inp["dy"][:, :k].double().numpy())
                 g = inp["gamma"][:k].double().numpy()
                 b = inp["beta"][:k].double().numpy()
-                esz = inp["x"].element_size()
+                plane = x.shape[0] * x.shape[2] * x.shape[3] * inp["x"].element_size()
                 if name.endswith("fwd"):
-                    fn = (lambda x=x, g=g, b=b, k=k, c=case: oracle.batch_norm_forward_train(
-                        x, g, b, np.zeros(k), np.ones(k), c.momentum, c.eps))
-                    nb = 2 * x.size * esz
+                    def make(lo, hi, x=x, g=g, b=b, c=case):
+                        xs = np.ascontiguousarray(x[:, lo:hi])
+                        return lambda: oracle.batch_norm_forward_train(
+                            xs, g[lo:hi], b[lo:hi], np.zeros(hi - lo), np.ones(hi - lo),
+                            c.momentum, c.eps)
+                    per = 2 * plane
                 else:
-                    fn = lambda x=x, dy=dy, g=g, c=case: oracle.batch_norm_backward(x, dy, g, c.eps)
-                    nb = 3 * x.size * esz
+                    def make(lo, hi, x=x, dy=dy, g=g, c=case):
+                        xs = np.ascontiguousarray(x[:, lo:hi])
+                        ds = np.ascontiguousarray(dy[:, lo:hi])
+                        return lambda: oracle.batch_norm_backward(xs, ds, g[lo:hi], c.eps)
+                    per = 3 * plane
+                self.items.append((name, k, per, make))
                 self.desc[name] = f"{k}/{case.shape[1]} channels"
             elif name.startswith("rms_"):
                 case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]
@@ -629,8 +663,12 @@ class OracleSample:
                 dy = inp["dy"][:rms_rows].double().numpy()
                 w = inp["w"].double().numpy()
                 rstd = oracle.rms_norm_rstd(x, case.eps)
-                fn = lambda x=x, dy=dy, w=w, r=rstd: oracle.rms_norm_backward(x, dy, w, r)
-                nb = 3 * x.size * inp["x"].element_size()
+
+                def make(lo, hi, x=x, dy=dy, w=w, r=rstd):
+                    xs, ds, rs = x[lo:hi], dy[lo:hi], r[lo:hi]
+                    return lambda: oracle.rms_norm_backward(xs, ds, w, rs)
+                self.items.append((name, rms_rows, 3 * case.hidden * inp["x"].element_size(),
+                                   make))
                 self.desc[name] = f"{rms_rows}/{case.rows} rows"
             else:
                 case = synth.CASES["ln_fused_bf16"]
@@ -639,32 +677,90 @@ class OracleSample:
                      for n in ("inp", "residual", "dy", "mask")}
                 bias = inp["bias"].double().numpy()
                 gamma = inp["gamma"].double().numpy()
-                s = inp["dropout_scale"]
-                z = oracle.dropout_add(f["inp"], f["residual"], bias, f["mask"], s)
+                sc = inp["dropout_scale"]
+                z = oracle.dropout_add(f["inp"], f["residual"], bias, f["mask"], sc)
                 mu, rs = oracle.layer_norm_saved_stats(z, case.eps)
-                fn = (lambda f=f, bias=bias, gamma=gamma, s=s, mu=mu, rs=rs:
-                      oracle.fused_bias_dropout_add_layer_norm_backward(
-                          f["dy"], f["inp"], f["residual"], bias, f["mask"], s, mu, rs, gamma))
-                nb = ln_rows * case.hidden * (5 * 2 + 1)
+
+                def make(lo, hi, f=f, bias=bias, gamma=gamma, sc=sc, mu=mu, rs=rs):
+                    p = {n: v[lo:hi] for n, v in f.items()}
+                    m, r = mu[lo:hi], rs[lo:hi]
+                    return lambda: oracle.fused_bias_dropout_add_layer_norm_backward(
+                        p["dy"], p["inp"], p["residual"], bias, p["mask"], sc, m, r, gamma)
+                self.items.append((name, ln_rows, case.hidden * (5 * 2 + 1), make))
                 self.desc[name] = f"{ln_rows}/{case.rows} rows"
-            self.items.append((name, fn, nb))
+        self.whole = [make(0, units) for _, units, _, make in self.items]
+        self.nbytes = sum(units * per for _, units, per, _ in self.items)
 
     def time_pass(self):
-        nb, secs = 0, 0.0
-        for _, fn, b in self.items:
+        secs = 0.0
+        for fn in self.whole:
             t0 = time.perf_counter()
             fn()
             secs += time.perf_counter() - t0
-            nb += b
-        return nb, secs
+        return self.nbytes, secs
+
+    def shards(self, n):
+        """n lists of calls that together cover the sample once (each op's
+        units split into n contiguous ranges)."""
+        out = [[] for _ in range(n)]
+        for _, units, _, make in self.items:
+            for s in range(n):
+                lo, hi = units * s // n, units * (s + 1) // n
+                if hi > lo:
+                    out[s].append(make(lo, hi))
+        return out
 
     def describe(self):
         return ", ".join(f"{k} {v}" for k, v in self.desc.items())
 
 
+def cpu_model():
+    """One line naming the host CPU (/proc/cpuinfo), else the machine type."""
+    import platform
+    try:
+        lines = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        lines = []
+    kv = {}
+    for ln in lines:
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            kv.setdefault(k.strip(), v.strip())
+    if "model name" in kv:
+        return kv["model name"]
+    if "CPU implementer" in kv:
+        return (f"{platform.machine()}, CPU implementer {kv['CPU implementer']} "
+                f"part {kv.get('CPU part', '?')}")
+    return platform.machine()
+
+
+def cpu_parallel(sample, budget_s):
+    """The same oracle sample cut into one shard per host core and run on
+    that many threads (numpy releases the interpreter lock inside its array
+    loops); wall-clock time per pass."""
+    from concurrent.futures import ThreadPoolExecutor
+    n = os.cpu_count() or 1
+    lists = sample.shards(n)
+    run = lambda fns: [fn() for fn in fns]
+    nb, secs, passes = 0, 0.0, 0
+    with ThreadPoolExecutor(max_workers=n) as pool:
+        list(pool.map(run, lists))  # warm-up pass
+        while secs < budget_s and passes < 8:
+            t0 = time.perf_counter()
+            list(pool.map(run, lists))
+            secs += time.perf_counter() - t0
+            nb += sample.nbytes
+            passes += 1
+    return {"value": round(nb / secs / 1e9, 4), "unit": UNIT, "cores": n,
+            "sample": f"the same sample in {n} shards (BatchNorm channels, rows) on {n} "
+                      f"threads; {passes} pass(es)",
+            "seconds": round(secs, 2)}
+
+
 def cpu_baseline(budget_s):
     """The oracle as it stands, single-threaded, on a bounded sample of the
-    step (about `budget_s` seconds of oracle time)."""
+    step (about `budget_s` seconds of oracle time); beside it the same
+    sample spread over every host core."""
     sample = OracleSample(bn_f32_channels=32, bn_bf16_channels=32, rms_rows=2048,
                           ln_rows=8192)
     nb, secs, passes = 0, 0.0, 0
@@ -675,7 +771,9 @@ def cpu_baseline(budget_s):
         passes += 1
     return {"value": round(nb / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "float64 numpy oracle, one thread; per op: " + sample.describe()
-            + f"; {passes} pass(es)", "seconds": round(secs, 2)}
+            + f"; {passes} pass(es)", "seconds": round(secs, 2),
+            "nproc": os.cpu_count(), "cpu_model": cpu_model(),
+            "all_cores": cpu_parallel(sample, budget_s / 4)}
 
 
 def run_reference(args, rank, world):

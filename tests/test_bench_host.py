@@ -67,3 +67,17 @@ def test_reference_arm_json_line(capsys):
     assert line["metric"] == bench.METRIC and line["unit"] == "GB/s"
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_oracle_sample_shards_cover_every_unit_once():
+    s = bench.OracleSample(bn_f32_channels=3, bn_bf16_channels=2, rms_rows=10, ln_rows=7)
+    for n in (1, 4, 16):
+        lists = s.shards(n)
+        assert len(lists) == n
+        # every op's units are split into contiguous ranges; ops with fewer
+        # units than shards leave some shards without a call for that op
+        expect = sum(min(units, n) for _, units, _, _ in s.items)
+        assert sum(len(fns) for fns in lists) == expect
+    par = bench.cpu_parallel(s, 0.05)
+    assert par["value"] > 0 and par["cores"] == (os.cpu_count() or 1)
+    assert bench.cpu_model()

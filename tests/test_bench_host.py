@@ -81,3 +81,30 @@ def test_oracle_sample_shards_cover_every_unit_once():
     par = bench.cpu_parallel(s, 0.05)
     assert par["value"] > 0 and par["cores"] == (os.cpu_count() or 1)
     assert bench.cpu_model()
+
+
+def test_johnson_order_minimises_two_stage_makespan():
+    """The end-to-end pipeline order: for random upload / download sizes the
+    order must reach the smallest two-stage flow-shop makespan found by
+    trying every permutation."""
+    import itertools
+    import random
+    import types
+    import torch
+
+    def makespan(seq):
+        t_up = t_down = 0
+        for up, down in seq:
+            t_up += up
+            t_down = max(t_down, t_up) + down
+        return t_down
+
+    rng = random.Random(7)
+    for _ in range(20):
+        jobs = [(rng.randint(1, 40), rng.randint(1, 40)) for _ in range(6)]
+        ops = [types.SimpleNamespace(name=str(i), h2d=[(torch.empty(u, dtype=torch.uint8), None)],
+                                     d2h=[(None, torch.empty(d, dtype=torch.uint8))])
+               for i, (u, d) in enumerate(jobs)]
+        got = [jobs[int(op.name)] for op in bench.johnson_order(ops)]
+        assert sorted(got) == sorted(jobs)
+        assert makespan(got) == min(makespan(p) for p in itertools.permutations(jobs))

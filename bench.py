@@ -447,6 +447,11 @@ def run_ours(args, rank, world, local_rank):
                 if peak_kind == "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": dbytes,
                 "traffic": recorded_traffic(f"{dop}:{dphase}")}
+    if roofline["traffic"]:
+        # what DRAM actually moved (the recorded ncu bytes) over the live time
+        dram = roofline["traffic"] / dmean / 1e9
+        roofline["dram_achieved"] = round(dram, 1)
+        roofline["dram_frac"] = round(dram / peak, 4)
 
     # Warm-L2 figures, labelled as such and not part of `value`: each op
     # called back to back without the flush, so whatever fits in L2 stays.

@@ -477,6 +477,7 @@ def run_ours(args, rank, world, local_rank):
         t = statistics.mean(per_op[op.name])
         ops_out[op.name] = {
             "desc": op.desc, "us": round(t * 1e6, 2),
+            "us_median": round(statistics.median(per_op[op.name]) * 1e6, 2),
             "us_min": round(min(per_op[op.name]) * 1e6, 2),
             "unique_bytes": op.unique_bytes,
             "eff_gbs": round(op.unique_bytes / t / 1e9, 1),

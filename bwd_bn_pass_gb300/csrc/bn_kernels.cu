@@ -29,6 +29,8 @@
 //     double-fp32 from the forward's (mean - shift) pair.
 //   * The consumer walks its slice in reverse, so the tail that the producer
 //     read last (still in L2) is read first.
+#include <atomic>
+
 #include "bn_finalize.cuh"
 #include "gbn_common.cuh"
 #include "gbn_internal.h"
@@ -551,10 +553,13 @@ cudaError_t dispatch_t(int dtype, int vec, A&&... args) {
   }
 }
 
+std::atomic<int> g_force_wide{0};
+
 template <template <typename, int, typename> class F, typename... A>
 cudaError_t dispatch(const BnPlan& p, int dtype, A&&... args) {
   const uint64_t vectors = (uint64_t)p.B * (uint64_t)p.C * (uint64_t)(p.P / p.vec);
-  if (vectors < (1ull << 32)) return dispatch_t<F, uint32_t>(dtype, p.vec, args...);
+  if (vectors < (1ull << 32) && g_force_wide.load(std::memory_order_relaxed) == 0)
+    return dispatch_t<F, uint32_t>(dtype, p.vec, args...);
   return dispatch_t<F, uint64_t>(dtype, p.vec, args...);
 }
 
@@ -597,6 +602,8 @@ template <typename T, int VEC, typename I> struct DxL {
 };
 
 }  // namespace
+
+int bn_set_wide_offsets(int force) { return g_force_wide.exchange(force != 0 ? 1 : 0); }
 
 bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan) {
   if (B < 0 || C < 0 || HW < 0) return false;

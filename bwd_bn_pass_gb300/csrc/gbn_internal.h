@@ -64,6 +64,7 @@ struct BnPlan {
 };
 
 // Fills grid_y / ws_bytes (device-dependent) for a shape; false on error.
+int bn_set_wide_offsets(int force);  // 64-bit offsets in the two-launch kernels
 bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan);
 
 // Largest power-of-two vector width (<= 16 bytes) valid for all pointers.

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "gbn_bn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "gbn_bn_set_persistent_min_bytes": (_I64, [_I64]),
     "gbn_bn_persistent_min_bytes": (_I64, []),
+    "gbn_bn_set_wide_offsets": (_INT, [_INT]),
     "gbn_bn_forward_train": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                     _P, _P, _P, _SZ, _P]),
     "gbn_bn_forward_train_noalloc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F,
@@ -210,6 +211,13 @@ def bn_set_persistent_min_bytes(nbytes):
 
 def bn_persistent_min_bytes():
     return lib().gbn_bn_persistent_min_bytes()
+
+
+def bn_set_wide_offsets(force):
+    """Make the two-launch BatchNorm kernels use 64-bit vector offsets even
+    for tensors that do not need them (a test hook; results are identical).
+    Process-wide; returns the previous setting."""
+    return bool(lib().gbn_bn_set_wide_offsets(1 if force else 0))
 
 
 def bn_workspace_bytes(B, C, HW, device=None):

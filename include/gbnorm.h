@@ -163,6 +163,14 @@ GBN_API int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes);
 /* The current threshold (bytes).                                           */
 GBN_API int64_t gbn_bn_persistent_min_bytes(void);
 
+/* The two-launch BatchNorm kernels (NCHW) address vectors with 32-bit
+ * offsets while the tensor holds fewer than 2^32 16-byte-or-smaller vectors,
+ * and with 64-bit offsets beyond.  A nonzero `force` makes every later call
+ * take the 64-bit form (results are identical; it exists so that the wide
+ * form can be tested on small tensors).  Process-wide; returns the previous
+ * setting.  The pages have no counterpart.                                 */
+GBN_API int gbn_bn_set_wide_offsets(int force);
+
 /* Full training forward: stats pass + finalize/apply.  Writes y, stats
  * (8*C floats, see GBN_BN_STATS_FLOATS), and updates the running stats in
  * place: running_mean = (1-momentum)*running_mean + momentum*mean,

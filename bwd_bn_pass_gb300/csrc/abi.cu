@@ -251,6 +251,17 @@ size_t bn_partials_bytes(int64_t B, int64_t C, int64_t HW) {
   return p.ws_partials;
 }
 
+int bn_forward_check_args(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                          const void* y, const float* stats, float momentum, float eps) {
+  int64_t M;
+  const int rc = bn_check(dtype, B, C, HW, true, &M);
+  if (rc != GBN_OK || C == 0) return rc;
+  if (x == nullptr || y == nullptr || stats == nullptr) return GBN_EINVAL;
+  if (!aligned(stats, 8)) return GBN_EALIGN;
+  if (!(eps >= 0.f) || momentum != momentum) return GBN_EINVAL;
+  return GBN_OK;
+}
+
 int bn_forward_train_scratch(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                              const float* gamma, const float* beta, float* running_mean,
                              float* running_var, float momentum, float eps, void* y,

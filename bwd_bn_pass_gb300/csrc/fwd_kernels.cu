@@ -5,7 +5,8 @@
 // `rmsnorm_prims` / F.rms_norm section: y = w*x*rstd with
 // rstd = 1/sqrt(mean(x^2) + eps), the statistic the backward takes.
 // nvFuser issue #1473 "Why is LayerNorm Backward Segmenting?" -- the forward
-// whose saved statistics (mean T5, rstd T7) the backward repros take:
+// whose saved statistics (the fp32 per-row mean and rstd) the backward
+// repros take:
 // y = (z - mean)*rstd*gamma + beta with the biased variance, and in the fused
 // form z = residual + mask*scale*(input + bias), the residual-stream output
 // (written when requested).

@@ -128,6 +128,11 @@ cudaError_t bn_fused_configure(int smem_optin, bool* ok);
 // the persistent kernel is used when `ws_bytes` also fits its workspace,
 // else the two-launch kernels.  Same status codes as gbn_bn_forward_train.
 size_t bn_partials_bytes(int64_t B, int64_t C, int64_t HW);
+// The argument checks of the training forward that need no CUDA call (dtype,
+// sizes, null pointers, stats alignment, eps / momentum): GBN_OK or the
+// status the forward would return for them.
+int bn_forward_check_args(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
+                          const void* y, const float* stats, float momentum, float eps);
 int bn_forward_train_scratch(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                              const float* gamma, const float* beta, float* running_mean,
                              float* running_var, float momentum, float eps, void* y,

@@ -21,12 +21,17 @@
 
 namespace {
 
-// 64 KiB: the two-launch kernels' stats partials take 16 * grid_y * C bytes,
-// and grid_y * C is at most one resident block slot per SM (608 on GB300)
-// whenever C <= 608, so every shape with C <= 4096 channels fits on GB300.
+// 64 KiB.  The two-launch kernels need 16 * grid_y * C bytes of partials,
+// where grid_y (blocks per channel) fills the device's resident 256-thread
+// block slots (608 on GB300, 4 per SM) at least once:
+//   * C <= slots: grid_y * C stays within about one slot per channel-block,
+//     at most ~608 * 16 bytes = 9.5 KiB, far below the limit;
+//   * C > slots: grid_y = 1 and the partials are 16 * C bytes, so every
+//     C <= 4096 fits and larger C is rejected with GBN_EWORKSPACE.
 // The single-launch persistent kernel also needs its per-CTA flags (16 bytes
-// per SM) and its own partials; it runs whenever those fit too, otherwise
-// the two-launch kernels do.
+// per SM) and its own partials; it runs whenever those fit the array too
+// (and the call's size threshold selects it), otherwise the two-launch
+// kernels do.
 constexpr size_t kNoAllocScratchBytes = 64 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -57,9 +62,14 @@ extern "C" int gbn_bn_forward_train_noalloc(const void* x, int dtype, int64_t B,
                                             float* running_mean, float* running_var,
                                             float momentum, float eps, void* y, float* stats,
                                             void* stream) {
+  // Argument errors come back before any CUDA call, as for every entry point.
+  const int rc = gbn::bn_forward_check_args(x, dtype, B, C, HW, y, stats, momentum, eps);
+  if (rc != GBN_OK) return rc;
+  if (C == 0 || B == 0 || HW == 0) return GBN_OK;
   void* scratch = scratch_on_current_device();
   if (scratch == nullptr) return GBN_ECUDA;
   const size_t need = gbn::bn_partials_bytes(B, C, HW);
+  if (need == 0) return GBN_ECUDA;
   if (need > kNoAllocScratchBytes) return GBN_EWORKSPACE;
   return gbn::bn_forward_train_scratch(x, dtype, B, C, HW, gamma, beta, running_mean,
                                        running_var, momentum, eps, y, stats, scratch,

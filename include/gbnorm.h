@@ -109,7 +109,10 @@ GBN_API const char* gbn_status_string(int status);
 /* Prepare `device` (-1: current): cache its attributes, resolve the device
  * status word and raise the kernels' shared-memory limits.  Every entry
  * point does this on its first call on a device; call it explicitly before
- * capturing a CUDA graph.  Returns GBN_OK or GBN_ECUDA.                     */
+ * capturing a CUDA graph.  Returns GBN_OK or GBN_ECUDA.  The cached facts
+ * include device addresses (the status word, the allocation-free call's
+ * scratch array) that a cudaDeviceReset invalidates: do not use the library
+ * on a device after resetting it in the same process.                      */
 GBN_API int gbn_init(int device);
 
 /* The pages have no counterpart: a self-test of the failure detection.  It
@@ -199,7 +202,9 @@ GBN_API int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C,
  * so calls that overlap on the GPU (other streams, other threads) race; order
  * them on one stream.  The first call on a device resolves the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.                                          */
+ * call before any stream capture.  Argument errors (dtype, sizes, null x / y
+ * / stats, stats alignment, eps, momentum) return GBN_EINVAL / GBN_EDTYPE /
+ * GBN_EALIGN before any CUDA call, as for the other entry points.          */
 GBN_API int gbn_bn_forward_train_noalloc(const void* x, int dtype, int64_t B, int64_t C,
                                          int64_t HW, const float* gamma, const float* beta,
                                          float* running_mean, float* running_var,
@@ -374,10 +379,10 @@ GBN_API int gbn_layernorm_backward(const void* dy, const void* x_or_input, int d
 
 /* Flags of gbn_layernorm_backward_ex.                                       */
 #define GBN_LN_SAVED_Z  1  /* x_or_input is the saved LayerNorm input z        */
-#define GBN_LN_DRES_F32 2  /* dresidual is written as fp32 (T77 of [P2])       */
+#define GBN_LN_DRES_F32 2  /* dresidual is written as fp32 (as [P2] emits it)  */
 
 /* gbn_layernorm_backward with variants ([P2] nvfuser_fusion_id9, where the
- * LayerNorm input T6 and the residual gradient T77 are fp32):
+ * LayerNorm input and the residual gradient are fp32 tensors):
  *   GBN_LN_SAVED_Z: x_or_input is z itself (e.g. the z written by
  *     gbn_layernorm_forward) instead of the dropout input; residual and bias
  *     must be NULL.  The fused outputs are still produced from mask and
@@ -413,7 +418,7 @@ GBN_API int gbn_rmsnorm_forward(const void* x, const void* w, int dtype, int64_t
                                 int64_t H, float eps, void* y, float* rstd, void* stream);
 
 /* LayerNorm forward, plain or fused with bias+dropout+add ([P2]: the
- * forward whose saved mean (T5) and rstd (T7) the backward repros take).
+ * forward whose saved fp32 mean and rstd the backward repros take).
  * Plain (residual == NULL; bias, mask, z must be NULL): z = x_or_input.
  * Fused (residual != NULL): z = residual + mask*dropout_scale*(x_or_input +
  *   bias) in fp32, written to `z` (the residual-stream output) unless NULL.

@@ -10,23 +10,28 @@ Source: nvFuser issue #1473, "Why is LayerNorm Backward Segmenting?".
   (nvfuser_fusion_id9) is the same backward followed by the gradient of a
   bias+dropout+add that produced the LayerNorm input.
 
-Decoding of the fusion definitions, per row of length H with saved mean mu
-and saved rstd rho (T5/T7 in the repros):
+What is computed, per row of length H with the saved mean mu and saved
+rstd rho = 1/sqrt(var + eps) (both inputs of the repros), written out by the
+chain rule.  The forward is y = xhat * gamma + beta with xhat = (z - mu) * rho,
+where mu and var (biased) are functions of the whole row z.  With
+g = dL/dxhat = dy * gamma, the loss reaches z directly through xhat, and
+through mu and var:
 
-    xhat  = (z - mu) * rho                      (T15)
-    g     = dy * gamma                          (T20)
-    dvar  = -1/2 * sum_j g * (z - mu) * rho^3   (T43)
-    dmean = -sum_j g * rho                      (T33/T44)
-    dz    = g*rho + 2*dvar*(z - mu)/H + dmean/H (T76)
-    dz   += dz_extra                            (T77; the extra fp32 gradient T2)
-    dgamma = sum_rows dy * xhat                 (T22)
-    dbeta  = sum_rows dy                        (T18)
+    dL/dvar  = sum_j g_j * (z_j - mu) * d(rho)/d(var)
+             = -1/2 * rho^3 * sum_j g_j * (z_j - mu)
+    dL/dmu   = -rho * sum_j g_j          (the var path adds
+               dL/dvar * (-2/H) * sum_j (z_j - mu) = 0)
+    dz_j     = g_j * rho + dL/dvar * 2 * (z_j - mu) / H + dL/dmu / H
+    dz      += dz_extra                  (an optional fp32 gradient that
+                                          reaches z by another path)
+    dgamma   = sum_rows dy * xhat,   dbeta = sum_rows dy
 
-and, for the fused form where z = residual + dropout(input + bias):
+and, for the fused form where z = residual + dropout(input + bias), the
+derivative of that sum and of the dropout's elementwise scale:
 
-    dresidual = dz                              (T77)
-    dinput    = dz * scale * mask               (T78/T79)
-    dbias     = sum_rows dinput                 (T81)
+    dresidual = dz
+    dinput    = dz * scale * mask
+    dbias     = sum_rows dinput
 
 Readings where the pages are silent (the fusion definitions show the
 backward only): the forward is ``z = residual + mask * scale * (input +
@@ -62,7 +67,7 @@ def layer_norm_saved_stats(z, eps):
 
 
 def layer_norm_forward(z, gamma, beta, eps):
-    """Training forward whose saved statistics the backward takes (T5/T7):
+    """Training forward whose saved statistics (mean, rstd) the backward takes:
     ``y = (z - mean) * rstd * gamma + beta`` per row, with the biased
     variance.  gamma / beta may be None (ones / zeros).  Returns dict
     y [R, H], mean [R], rstd [R]."""
@@ -142,7 +147,8 @@ def layer_norm_backward_saved_z(dy, z, mask, scale, mean, rstd, gamma, dz_extra=
     """The fused backward given the saved LayerNorm input z (the
     residual-stream output of the forward) instead of the operands that
     produced it: the same dz, dresidual = dz, dx = dz * scale * mask and
-    dbias = sum_rows dx (nvfuser_fusion_id9 with T6 read, not recomputed).
+    dbias = sum_rows dx (nvfuser_fusion_id9 with the LayerNorm input read,
+    not recomputed).
     mask may be None (everything kept).  Returns dict dx, dresidual, dbias
     (None unless with_dbias), dgamma, dbeta."""
     dz, dgamma, dbeta = _ln_core(dy, z, mean, rstd, gamma, dz_extra)

@@ -78,6 +78,28 @@ def test_bn_forward_argument_errors(gbn):
     assert _fwd(L, C=0) == OK                    # nothing to do, nothing launched
 
 
+def test_bn_noalloc_argument_errors(gbn):
+    """The allocation-free forward rejects bad arguments before any CUDA call
+    (it resolves its fixed scratch array only afterwards), with the codes of
+    gbn_bn_forward_train."""
+    L = gbn.lib()
+
+    def na(x=A16, dtype=0, B=4, C=3, HW=5, y=A16, stats=A16, mom=0.1, eps=1e-5):
+        return L.gbn_bn_forward_train_noalloc(x, dtype, B, C, HW, NULL, NULL, NULL, NULL, mom,
+                                              eps, y, stats, NULL)
+
+    assert na(dtype=7) == EDTYPE
+    assert na(B=-1) == EINVAL
+    assert na(B=1, HW=1) == EINVAL
+    assert na(x=NULL) == EINVAL
+    assert na(y=NULL) == EINVAL
+    assert na(stats=NULL) == EINVAL
+    assert na(stats=A4) == EALIGN
+    assert na(eps=float("nan")) == EINVAL
+    assert na(mom=float("nan")) == EINVAL
+    assert na(C=0) == OK
+
+
 def test_bn_other_entry_points_argument_errors(gbn):
     L = gbn.lib()
     assert L.gbn_bn_stats(A16, 3, 2, 2, 2, A16, 4096, NULL) == EDTYPE

@@ -274,7 +274,8 @@ def test_ln_backward_saved_z_with_dz_extra_and_fp32_dresidual(gbn):
 
 @pytest.mark.parametrize("R,H", [(256, 1600), (23, 1000)])
 def test_ln_fused_backward_fp32_dresidual(gbn, R, H):
-    """dresidual in fp32 (the page's T77) from bf16 operands, on the bulk-copy
+    """dresidual in fp32 (the residual gradient the fused repro emits in fp32)
+    from bf16 operands, on the bulk-copy
     and the generic kernel; the other outputs are unchanged."""
     inp = ln_case(R, H, "bf16")
     d = {k: (v.to(DEV) if torch.is_tensor(v) else v) for k, v in inp.items()}

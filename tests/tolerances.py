@@ -75,10 +75,17 @@ def bf16_report(got, ref, tau):
             "err": err, "bound": bound, "g": g, "r": r, "badmask": bad}
 
 
+# (check name, elements whose bound came from the floor tau, elements
+# checked) of every bf16 comparison in this process; the test session prints
+# the totals at its end.
+TAU_FLOOR_LOG = []
+
+
 def check_bf16(got, ref, name, tau=None):
     if tau is None:
         tau = tau_of(ref)
     rep = bf16_report(got, ref, tau)
+    TAU_FLOOR_LOG.append((name, rep["tau_floor"], rep["g"].size))
     if rep["bad"]:
         bad = rep["badmask"]
         ratio = np.where(bad, rep["err"] / np.maximum(rep["bound"], 1e-300), 0)

@@ -521,7 +521,7 @@ int gbn_rmsnorm_backward(const void* dy, const void* x, const void* w, int dtype
   RowPlan p;
   if (!row_plan(R, H, GBN_ROW_RMS, dtype, fast_ok, false, false, *dev, &p)) return GBN_EINVAL;
   if (ws_bytes < p.ws_bytes) return GBN_EWORKSPACE;
-  return to_status(rms_launch(p, dy, x, w, rstd, dx, dw, static_cast<float*>(ws), dev->status,
+  return to_status(rms_launch(p, dy, x, w, rstd, dx, dw, ws, dev->status,
                               static_cast<cudaStream_t>(stream)));
 }
 
@@ -573,7 +573,7 @@ int gbn_layernorm_backward_ex(const void* dy, const void* x_or_input, int dtype,
   q.dbias = dbias;
   q.saved_z = saved_z;
   q.dres_f32 = (flags & GBN_LN_DRES_F32) != 0 && dtype != GBN_F32;
-  return to_status(ln_launch(p, q, static_cast<float*>(ws), dev->status,
+  return to_status(ln_launch(p, q, ws, dev->status,
                              static_cast<cudaStream_t>(stream)));
 }
 

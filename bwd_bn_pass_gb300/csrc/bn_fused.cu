@@ -109,42 +109,6 @@ __device__ __forceinline__ void consumers_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kFConsumers) : "memory");
 }
 
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
-  float a, b;
-  asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(a), "=f"(b) : "l"(p) : "memory");
-  return make_float2(a, b);
-}
-
-// Flag pair of CTA k: word 0 is stored last, with release semantics.
-__device__ __forceinline__ bool flag_ready(const unsigned long long* f, unsigned long long t) {
-  return ld_acquire_u64(f) == t && ld_relaxed_u64(f + 1) == ~t;
-}
-__device__ bool wait_flag(const unsigned long long* f, unsigned long long t) {
-  if (flag_ready(f, t)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    __nanosleep(100);
-    if (flag_ready(f, t)) return true;
-    if ((it & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // mbarrier wait that also gives up once another warp has aborted.
 __device__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -691,18 +655,6 @@ cudaError_t launch_fused(const FArgs& a, const BnFusedPlan& p, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, bn_fused_kernel<T, BWD>, a);
 }
 
-std::atomic<unsigned long long> g_nonce{0};
-
-// A fresh 64-bit value per call (splitmix64 of a process counter): the flag
-// epoch used when the workspace holds no valid epoch pair.
-unsigned long long next_nonce() {
-  unsigned long long z = g_nonce.fetch_add(0x9e3779b97f4a7c15ull) + 0x9e3779b97f4a7c15ull;
-  z ^= reinterpret_cast<uintptr_t>(&g_nonce);
-  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
-  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
-  return z ^ (z >> 31);
-}
-
 FArgs make_args(const BnFusedPlan& p, void* ws) {
   FArgs a = {};
   a.sync = static_cast<unsigned long long*>(ws);
@@ -726,6 +678,20 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<unsigned long long> g_nonce{0};
+}  // namespace
+
+// A fresh 64-bit value per call (splitmix64 of a process counter): the flag
+// epoch used when a workspace holds no valid epoch pair.
+unsigned long long next_nonce() {
+  unsigned long long z = g_nonce.fetch_add(0x9e3779b97f4a7c15ull) + 0x9e3779b97f4a7c15ull;
+  z ^= reinterpret_cast<uintptr_t>(&g_nonce);
+  z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+  z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+  return z ^ (z >> 31);
+}
 
 bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
                    const DevInfo& dev, BnFusedPlan* p) {

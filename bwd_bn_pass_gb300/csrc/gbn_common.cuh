@@ -474,4 +474,81 @@ __device__ __forceinline__ void report_status(int* status, int bits) {
   if (status != nullptr) atomicOr(status, bits);
 }
 
+// ------------------------------------------- flags between resident CTAs --
+//
+// Kernels whose CTAs are all resident (cooperative launch) hand results to
+// each other through a workspace of 64-bit words: an epoch pair (e, ~e) at
+// the start, then one flag pair per CTA.  A CTA publishes by storing
+// (t, ~t) with t = e + 1 (release); a reader acquires the pair and checks
+// both halves.  The epoch comes from the workspace when its pair is
+// self-consistent, else from a host nonce, and one CTA advances it after it
+// has seen every flag, so a reused or replayed workspace never matches a
+// stale flag.  No memset and no atomics.
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
+  float a, b;
+  asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(a), "=f"(b) : "l"(p) : "memory");
+  return make_float2(a, b);
+}
+
+// Flag pair of CTA k: word 0 is stored last, with release semantics.
+__device__ __forceinline__ bool flag_ready(const unsigned long long* f, unsigned long long t) {
+  return ld_acquire_u64(f) == t && ld_relaxed_u64(f + 1) == ~t;
+}
+__device__ __forceinline__ bool wait_flag(const unsigned long long* f, unsigned long long t) {
+  if (flag_ready(f, t)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(100);
+    if (flag_ready(f, t)) return true;
+    if ((it & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// The flag value of this launch: (epoch of the workspace's pair, or the
+// nonce when the pair is not self-consistent) + 1.
+__device__ __forceinline__ unsigned long long flag_target(const unsigned long long* sync,
+                                                          unsigned long long nonce) {
+  const unsigned long long ea = ld_relaxed_u64(sync), eb = ld_relaxed_u64(sync + 1);
+  return (eb == ~ea ? ea : nonce) + 1ull;
+}
+
+// Publish CTA k's flag after its earlier global writes (the caller makes
+// the writes of the other threads of the CTA visible to this one first,
+// e.g. with a barrier).
+__device__ __forceinline__ void flag_publish(unsigned long long* sync, int k,
+                                             unsigned long long t) {
+  unsigned long long* f = sync + 2 + 2 * (int64_t)k;
+  __threadfence();
+  st_relaxed_u64(f + 1, ~t);
+  st_release_u64(f, t);
+}
+
+// Store the next epoch (after every flag of this launch was seen).  After a
+// failure one epoch is skipped so that no flag of this launch can match the
+// next launch's target.
+__device__ __forceinline__ void epoch_advance(unsigned long long* sync, unsigned long long t,
+                                              bool all_seen) {
+  const unsigned long long next = all_seen ? t : t + 1ull;
+  st_relaxed_u64(sync + 1, ~next);
+  st_relaxed_u64(sync, next);
+}
+
+
 }  // namespace gbn

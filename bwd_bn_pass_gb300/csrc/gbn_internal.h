@@ -120,6 +120,9 @@ cudaError_t bn_fused_backward(const BnFusedPlan& p, int dtype, const void* x, co
                               void* dx, const float* stats, const float* beta, int act,
                               float slope, float* grads, void* ws, int* status,
                               cudaStream_t st);
+// A fresh 64-bit value per call: the epoch of a launch whose workspace holds
+// no valid epoch pair (kernels that hand results between resident CTAs).
+unsigned long long next_nonce();
 // Shared-memory limits and the one-CTA-per-SM check (called from device_info).
 cudaError_t bn_fused_configure(int smem_optin, bool* ok);
 
@@ -158,8 +161,16 @@ struct RowPlan {
   size_t smem = 0;     // dynamic shared memory per block
   uint32_t stage_bytes = 0;
   uint32_t off[5] = {0, 0, 0, 0, 0};  // per-stage offsets: dy, x, residual, mask, dz_extra
+  int tprw = 0;        // LayerNorm ring: consumer warps per row slot
+  int rs = 0;          // LayerNorm ring: row slots
+  size_t part_offset = 0;  // column partials' offset in the workspace (flags first)
   size_t ws_bytes = 0;
 };
+
+// Consumer warps of the LayerNorm ring kernel: at most 14 when a thread owns
+// one 16-byte vector of a row, 8 when it owns two (register budget).
+constexpr int kLnRingWarpsKV1 = 14;
+constexpr int kLnRingWarpsKVn = 8;
 
 struct LnPtrs {
   const void* dy = nullptr;
@@ -188,9 +199,9 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
               bool has_dzx, const DevInfo& dev, RowPlan* plan);
 
 cudaError_t rms_launch(const RowPlan& p, const void* dy, const void* x, const void* w,
-                       const float* rstd, void* dx, void* dw, float* part, int* status,
+                       const float* rstd, void* dx, void* dw, void* ws, int* status,
                        cudaStream_t st);
-cudaError_t ln_launch(const RowPlan& p, const LnPtrs& a, float* part, int* status,
+cudaError_t ln_launch(const RowPlan& p, const LnPtrs& a, void* ws, int* status,
                       cudaStream_t st);
 
 // Row-wise training forwards (fwd_kernels.cu).

@@ -14,14 +14,29 @@
 // separate passes over the [R, H] tensors -- is met by accumulating the
 // column sums while the rows stream through.
 //
-// GB300 design: the same persistent, bulk-copy-fed skeleton as the RMSNorm
-// kernel.  A pipeline stage holds RB consecutive rows of dy, input,
-// residual and mask (one bulk copy per tensor); each thread owns fixed
-// 16-byte column vectors (gamma, bias and the three column accumulators stay
-// in registers), computes both row sums for all RB rows of the stage before a
-// single block barrier, then writes dx / dresidual with 16-byte stores.
+// GB300 design: one launch, the ring engine of the RMSNorm kernel
+// (row_engine.cuh).  A stage holds RB consecutive rows of dy, input,
+// residual and mask (one bulk copy per tensor), filled by the producer warp.
+// The consumer warps form NGRP groups of TPRW warps each; group q takes
+// stages q, q + NGRP, ... and has its own named barrier, so that one group
+// computes while another waits (the producer warp serves them all).  Each
+// thread owns fixed 16-byte column vectors of a row (gamma, bias and the
+// three column accumulators stay in registers); it copies its vectors of the
+// stage's rows into registers and releases the stage at once, computes both
+// row sums, meets its group at one barrier per stage, then writes dx /
+// dresidual with 16-byte stores.  At the end the groups' column accumulators are added
+// in shared memory into one partial row per CTA, the CTAs hand the partials
+// to each other through the workspace's arrival counter, and every CTA sums
+// its share of the dgamma / dbeta / dbias columns over all partial rows in a
+// fixed order -- no second launch.  Shapes the ring does not take (rows that
+// are not whole 16-byte vectors, masks of rows that are not whole 16-byte
+// words, unaligned tensors, rows longer than the registers hold) run a plain
+// kernel followed by a separate fixed-order column-sum launch.
+#include <type_traits>
+
 #include "gbn_common.cuh"
 #include "gbn_internal.h"
+#include "row_engine.cuh"
 
 namespace gbn {
 
@@ -51,59 +66,14 @@ struct LnArgs {
   int32_t dres_f32;  // dresidual written as fp32
   uint32_t stage_bytes;
   uint32_t off_dy, off_x, off_res, off_mask;
+  void* dgamma;
+  void* dbeta;
+  void* dbias;
+  unsigned long long* sync;  // ring kernel: epoch pair, counter, flags
+  unsigned long long nonce;
+  int32_t tprw;              // ring kernel: consumer warps per row slot
+  int32_t rs;                // ring kernel: row slots
 };
-
-__host__ __device__ constexpr uint32_t ln_header(int rb) { return 64 + 2 * 2 * rb * 32 * 4; }
-
-template <typename T>
-__device__ __forceinline__ void ldg16(const T* p, float (&v)[16 / sizeof(T)]) {
-  Vec16<T>::load(p, v);
-}
-
-// Mask bits of VE consecutive bytes (nonzero = kept).
-template <int VE>
-__device__ __forceinline__ uint32_t mask_bits(const uint8_t* p) {
-  uint32_t bits = 0;
-  if constexpr (VE == 8) {
-    const uint2 w = *reinterpret_cast<const uint2*>(p);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      bits |= (((w.x >> (8 * e)) & 0xffu) != 0u) << e;
-      bits |= (((w.y >> (8 * e)) & 0xffu) != 0u) << (e + 4);
-    }
-  } else {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) bits |= (((w >> (8 * e)) & 0xffu) != 0u) << e;
-  }
-  return bits;
-}
-
-// Sum of the nwarps per-warp partials in slot[0..nwarps) as a fixed
-// pairwise tree (every thread computes the same bits).  Blocks of at most 8
-// warps read the 8 slots as two 16-byte words (slot is 16-byte aligned) and
-// add the same tree without its all-zero upper half.
-template <int MAXW>
-__device__ __forceinline__ float sum_warp_slots(const float* slot, int nwarps) {
-  if constexpr (MAXW <= 8) {
-    const float4 p = reinterpret_cast<const float4*>(slot)[0];
-    const float4 q = reinterpret_cast<const float4*>(slot)[1];
-    const float v0 = p.x, v1 = nwarps > 1 ? p.y : 0.f, v2 = nwarps > 2 ? p.z : 0.f;
-    const float v3 = nwarps > 3 ? p.w : 0.f, v4 = nwarps > 4 ? q.x : 0.f;
-    const float v5 = nwarps > 5 ? q.y : 0.f, v6 = nwarps > 6 ? q.z : 0.f;
-    const float v7 = nwarps > 7 ? q.w : 0.f;
-    return ((v0 + v1) + (v2 + v3)) + ((v4 + v5) + (v6 + v7));
-  } else {
-    float v[16];
-#pragma unroll
-    for (int w = 0; w < 16; ++w) v[w] = w < nwarps ? slot[w] : 0.f;
-#pragma unroll
-    for (int step = 1; step < 16; step *= 2)
-#pragma unroll
-      for (int w = 0; w < 16; w += 2 * step) v[w] += v[w + step];
-    return v[0];
-  }
-}
 
 // One element's LayerNorm input z from the stage (fused: residual +
 // keep*(input + bias), exact (hi, lo) for fp32 outputs).
@@ -130,325 +100,481 @@ __device__ __forceinline__ f2 keep_pair(uint2 m, int p, float s) {
   return f2_pack(lo, hi);
 }
 
-template <typename T, int KV, int RB, bool FUSED, int MAXT, int MINB>
-__global__ void __launch_bounds__(MAXT, MINB) ln_bwd_fast_kernel(LnArgs a) {
+constexpr int kLnMaxRedFloats = 16 * 2 * 2 * 2;  // [group, buffer, row, sum, warp] slots
+
+// Bit 7 of every byte of the result is set iff that byte of w is nonzero.
+__device__ __forceinline__ uint32_t bytes_nonzero(uint32_t w) {
+  return (((w & 0x7f7f7f7fu) + 0x7f7f7f7fu) | w) & 0x80808080u;
+}
+// All ones if byte E of nz has bit 7 set, else zero (a byte permute that
+// replicates the selected byte's top bit).
+template <int E>
+__device__ __forceinline__ uint32_t byte_select_mask(uint32_t nz) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(nz), "n"(0x8888 | (E * 0x1111)));
+  return r;
+}
+// keep factors (scale where the mask byte is nonzero, else 0) of the NP
+// pairs of a 16-byte vector whose mask bytes are in m (bf16: 8 bytes; fp32:
+// the 4 bytes of m.x).
+template <int NP>
+__device__ __forceinline__ void keep_pairs(uint2 m, float s, f2 (&keep2)[NP]) {
+  const uint32_t sb = __float_as_uint(s);
+  const uint32_t n0 = bytes_nonzero(m.x);
+  keep2[0] = f2_pack(__uint_as_float(sb & byte_select_mask<0>(n0)),
+                     __uint_as_float(sb & byte_select_mask<1>(n0)));
+  keep2[1] = f2_pack(__uint_as_float(sb & byte_select_mask<2>(n0)),
+                     __uint_as_float(sb & byte_select_mask<3>(n0)));
+  if constexpr (NP == 4) {
+    const uint32_t n1 = bytes_nonzero(m.y);
+    keep2[2] = f2_pack(__uint_as_float(sb & byte_select_mask<0>(n1)),
+                       __uint_as_float(sb & byte_select_mask<1>(n1)));
+    keep2[3] = f2_pack(__uint_as_float(sb & byte_select_mask<2>(n1)),
+                       __uint_as_float(sb & byte_select_mask<3>(n1)));
+  }
+}
+
+// Warp sums of four values at once (a transposed butterfly: 6 shuffles
+// instead of 20).  Lane l ends with the full sum of value ((l >> 4) & 1) * 2
+// + ((l >> 3) & 1); the addition order is fixed, so every lane holding a
+// value holds the same bits.
+__device__ __forceinline__ float warp_sum4_transposed(float v0, float v1, float v2, float v3) {
+  const int lane = threadIdx.x & 31;
+  const bool b = (lane & 16) != 0;
+  float a0 = b ? v2 : v0, a1 = b ? v3 : v1;
+  const float s0 = b ? v0 : v2, s1 = b ? v1 : v3;
+  a0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  a1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  const bool c = (lane & 8) != 0;
+  float m = c ? a1 : a0;
+  const float o = c ? a0 : a1;
+  m += __shfl_xor_sync(0xffffffffu, o, 8);
+  m += __shfl_xor_sync(0xffffffffu, m, 4);
+  m += __shfl_xor_sync(0xffffffffu, m, 2);
+  m += __shfl_xor_sync(0xffffffffu, m, 1);
+  return m;
+}
+// consumer warps of the ring instances, by KV (the plan's choices)
+constexpr int kLnRingWarps[3] = {0, kLnRingWarpsKV1, kLnRingWarpsKVn};
+
+// KV: 16-byte vectors per consumer thread and row; a stage holds RPS rows
+// (two for one-vector rows, else one).  MAXW: consumer warps at most (the
+// register budget of a thread follows from it).
+template <typename T, int KV, bool FUSED, int MAXW>
+__global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs a) {
   constexpr int VE = 16 / sizeof(T);
   constexpr bool COMP = sizeof(T) == 4;
   using PK = Pairs16<T>;
   constexpr int NP = PK::NP;
-  constexpr uint32_t HDR = ln_header(RB);
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + 64);  // [2][2*RB][32]
-  unsigned char* data = smem + HDR;
+  constexpr int RPS = KV == 1 ? 2 : 1;
+  using MaskRaw = typename std::conditional<VE == 8, uint2, uint32_t>::type;
+  extern __shared__ __align__(128) unsigned char data[];
+  __shared__ RowShared sh;
+  __shared__ __align__(16) float red[kLnMaxRedFloats];
+  static_assert(sizeof(RowShared) + sizeof(red) + 16 <= kRowStaticSmem, "static shared memory");
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
+  const int tid = threadIdx.x;
   const int g = blockIdx.x, G = gridDim.x;
+  const int TPRW = a.tprw, NGRP = a.rs, NCW = NGRP * TPRW, NC = NCW * 32, TPR = TPRW * 32;
+  constexpr int RB = RPS;
   const int64_t nblk = (a.R + RB - 1) / RB;
   const int64_t nmine = (nblk - g + G - 1) / G;
-  const int nst = a.nstage;
+  const int NS = a.nstage;
   const int64_t H = a.H;
   const uint32_t rowb = (uint32_t)(H * sizeof(T));
   const bool has_mask = FUSED && a.mask != nullptr;
-
-  auto issue = [&](int64_t i) {
-    const int s = (int)(i % nst);
-    const int64_t r0 = (g + i * G) * RB;
-    const int64_t nr = a.R - r0 < RB ? a.R - r0 : RB;
-    const uint32_t bt = (uint32_t)nr * rowb;
-    const uint32_t bm = (uint32_t)(nr * H);
-    unsigned char* st = data + (size_t)s * a.stage_bytes;
-    const bool with_res = FUSED && !a.zin;
-    mbar_arrive_expect_tx(&bar[s], bt * (with_res ? 3u : 2u) + (has_mask ? bm : 0u));
-    bulk_g2s(st + a.off_dy, static_cast<const char*>(a.dy) + r0 * rowb, bt, &bar[s]);
-    bulk_g2s(st + a.off_x, static_cast<const char*>(a.x) + r0 * rowb, bt, &bar[s]);
-    if (with_res) bulk_g2s(st + a.off_res, static_cast<const char*>(a.res) + r0 * rowb, bt, &bar[s]);
-    if (has_mask) bulk_g2s(st + a.off_mask, a.mask + r0 * H, bm, &bar[s]);
-  };
+  const bool with_res = FUSED && !a.zin;
 
   if (tid == 0) {
-    for (int s = 0; s < nst; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], TPRW);  // the warps of the stage's group
+      sh.issued[s] = 0;
+    }
+    sh.abort = 0;
+    sh.target = flag_target(a.sync, a.nonce);
     fence_mbarrier_init();
+    GBN_RING_TRACE(0);
   }
   __syncthreads();
-  if (tid == 0)
-    for (int64_t i = 0; i < nmine && i < nst; ++i) issue(i);
 
-  // Per-column constants and accumulators of this thread's columns.  fp32
-  // outputs use scalar double-fp32 sums; bf16 outputs packed fp32x2 sums.
-  float gam[KV][VE], bia[KV][VE];
-  f2 gam2[KV][NP], bia2[KV][NP];
-  DF acc_g[KV][VE], acc_b[KV][VE], acc_x[KV][VE];  // dgamma, dbeta, dbias (fp32 outputs)
-  f2 sg_g[KV][NP], sg_b[KV][NP], sg_x[KV][NP];     // the same, packed (bf16 outputs)
-#pragma unroll
-  for (int k = 0; k < KV; ++k) {
-    const int vi = tid + k * blockDim.x;
-    uint4 rg = make_uint4(0u, 0u, 0u, 0u), rbias = make_uint4(0u, 0u, 0u, 0u);
-    if (vi < a.Hv) {
-      rg = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.gamma) + (int64_t)vi * VE);
-      if (FUSED && a.bias != nullptr)
-        rbias = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.bias) + (int64_t)vi * VE);
-    }
-    PK::get(rg, gam2[k]);
-    PK::get(rbias, bia2[k]);
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      const float2 gg = f2_unpack(gam2[k][p]), bb = f2_unpack(bia2[k][p]);
-      gam[k][2 * p] = gg.x;
-      gam[k][2 * p + 1] = gg.y;
-      bia[k][2 * p] = bb.x;
-      bia[k][2 * p + 1] = bb.y;
-      sg_g[k][p] = sg_b[k][p] = sg_x[k][p] = 0ull;
-    }
-#pragma unroll
-    for (int e = 0; e < VE; ++e) { acc_g[k][e] = acc_b[k][e] = acc_x[k][e] = DF{0.f, 0.f}; }
-  }
+  if (tid < 32) {
+    if (tid == 0)
+      ring_produce(sh, NS, nmine, a.status, [&](int64_t i, int s) {
+        const int64_t r0 = (g + i * G) * RB;
+        const int64_t nr = a.R - r0 < RB ? a.R - r0 : RB;
+        const uint32_t bt = (uint32_t)nr * rowb;
+        const uint32_t bm = (uint32_t)(nr * H);
+        unsigned char* st = data + (size_t)s * a.stage_bytes;
+        mbar_arrive_expect_tx(&sh.full[s], bt * (with_res ? 3u : 2u) + (has_mask ? bm : 0u));
+        bulk_g2s(st + a.off_dy, static_cast<const char*>(a.dy) + r0 * rowb, bt, &sh.full[s]);
+        bulk_g2s(st + a.off_x, static_cast<const char*>(a.x) + r0 * rowb, bt, &sh.full[s]);
+        if (with_res)
+          bulk_g2s(st + a.off_res, static_cast<const char*>(a.res) + r0 * rowb, bt, &sh.full[s]);
+        if (has_mask) bulk_g2s(st + a.off_mask, a.mask + r0 * H, bm, &sh.full[s]);
+      });
+  } else if (tid - 32 < NC) {
+    const int ct = tid - 32, lane = ct & 31, cw = ct >> 5;
+    const int grp = cw / TPRW, wis = cw - grp * TPRW, lr = ct - grp * TPR;
+    const int gbar = 2 + grp;  // the group's named barrier
 
-  // One 16-byte column vector of row rr of the stage as packed pairs: dy, z
-  // (fused: residual + keep*(input + bias)) and keep.
-  auto load_pairs = [&](const unsigned char* st, int rr, int k, f2 (&dy2)[NP], f2 (&z2)[NP],
-                        f2 (&keep2)[NP]) {
-    const int vi = tid + k * blockDim.x;
-    const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
-    PK::get(*reinterpret_cast<const uint4*>(st + a.off_dy + o), dy2);
-    f2 x2[NP];
-    PK::get(*reinterpret_cast<const uint4*>(st + a.off_x + o), x2);
-    if constexpr (FUSED) {
-      f2 r2[NP];
-      if (!a.zin) PK::get(*reinterpret_cast<const uint4*>(st + a.off_res + o), r2);
-      uint2 m = make_uint2(0x01010101u, 0x01010101u);
-      if (has_mask) {
-        const unsigned char* mp = st + a.off_mask + (size_t)rr * H + (size_t)vi * VE;
-        if constexpr (VE == 8) m = *reinterpret_cast<const uint2*>(mp);
-        else m.x = *reinterpret_cast<const uint32_t*>(mp);
+    // Per-column constants and accumulators of this thread's columns.  fp32
+    // outputs use scalar double-fp32 sums; bf16 outputs packed fp32x2 sums.
+    float gam[KV][VE], bia[KV][VE];
+    f2 gam2[KV][NP], bia2[KV][NP];
+    DF acc_g[KV][VE], acc_b[KV][VE], acc_x[KV][VE];  // dgamma, dbeta, dbias (fp32 outputs)
+    f2 sg_g[KV][NP], sg_b[KV][NP], sg_x[KV][NP];     // the same, packed (bf16 outputs)
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int vi = lr + k * TPR;
+      uint4 rg = make_uint4(0u, 0u, 0u, 0u), rbias = make_uint4(0u, 0u, 0u, 0u);
+      if (vi < a.Hv) {
+        rg = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.gamma) + (int64_t)vi * VE);
+        if (FUSED && a.bias != nullptr)
+          rbias = *reinterpret_cast<const uint4*>(static_cast<const T*>(a.bias) + (int64_t)vi * VE);
       }
+      PK::get(rg, gam2[k]);
+      PK::get(rbias, bia2[k]);
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
-        keep2[p] = keep_pair(m, p, a.scale);
-        z2[p] = a.zin ? x2[p] : f2_fma(keep2[p], f2_add(x2[p], bia2[k][p]), r2[p]);
+        const float2 gg = f2_unpack(gam2[k][p]), bb = f2_unpack(bia2[k][p]);
+        gam[k][2 * p] = gg.x;
+        gam[k][2 * p + 1] = gg.y;
+        bia[k][2 * p] = bb.x;
+        bia[k][2 * p + 1] = bb.y;
+        sg_g[k][p] = sg_b[k][p] = sg_x[k][p] = 0ull;
       }
-    } else {
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        keep2[p] = f2_splat(1.f);
-        z2[p] = x2[p];
-      }
+      for (int e = 0; e < VE; ++e) { acc_g[k][e] = acc_b[k][e] = acc_x[k][e] = DF{0.f, 0.f}; }
     }
-  };
 
-  // Scalar form for fp32 outputs: dy, exact z (hi, lo), keep.
-  auto load_elem = [&](const unsigned char* st, int rr, int k, float (&dyv)[VE],
-                       DF (&z)[VE], float (&keep)[VE]) {
-    const int vi = tid + k * blockDim.x;
-    const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
-    float xv[VE];
-    Vec16<T>::load(st + a.off_dy + o, dyv);
-    Vec16<T>::load(st + a.off_x + o, xv);
-    if constexpr (FUSED) {
-      float rv[VE];
-      if (!a.zin) Vec16<T>::load(st + a.off_res + o, rv);
-      const uint32_t mk =
-          has_mask ? mask_bits<VE>(st + a.off_mask + (size_t)rr * H + (size_t)vi * VE) : 0xffu;
+    // One 16-byte column vector as packed pairs: dy, z (fused: residual +
+    // keep*(input + bias)) and keep, from the raw words.
+    auto pairs = [&](int k, uint4 rdy, uint4 rx, uint4 rres, MaskRaw rm, f2 (&dy2)[NP],
+                     f2 (&z2)[NP], f2 (&keep2)[NP]) {
+      PK::get(rdy, dy2);
+      f2 x2[NP];
+      PK::get(rx, x2);
+      if constexpr (FUSED) {
+        f2 r2[NP];
+        PK::get(rres, r2);
+        if (has_mask) {
+          uint2 m;
+          if constexpr (VE == 8) m = rm;
+          else m = make_uint2(rm, 0u);
+          keep_pairs<NP>(m, a.scale, keep2);
+        } else {
 #pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        keep[e] = ((mk >> e) & 1u) ? a.scale : 0.f;
-        z[e] = a.zin ? DF{xv[e], 0.f} : ln_z<FUSED, COMP>(xv[e], rv[e], bia[k][e], keep[e]);
+          for (int p = 0; p < NP; ++p) keep2[p] = f2_splat(a.scale);
+        }
+#pragma unroll
+        for (int p = 0; p < NP; ++p)
+          z2[p] = a.zin ? x2[p] : f2_fma(keep2[p], f2_add(x2[p], bia2[k][p]), r2[p]);
+      } else {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          keep2[p] = f2_splat(1.f);
+          z2[p] = x2[p];
+        }
       }
-    } else {
+    };
+    // Scalar form for fp32 outputs: dy, exact z (hi, lo), keep.
+    auto elems = [&](int k, uint4 rdy, uint4 rx, uint4 rres, MaskRaw rm, float (&dyv)[VE],
+                     DF (&z)[VE], float (&keep)[VE]) {
+      float xv[VE];
+      Vec<T, VE>::cvt(rdy, dyv);
+      Vec<T, VE>::cvt(rx, xv);
+      if constexpr (FUSED) {
+        float rv[VE];
+        Vec<T, VE>::cvt(rres, rv);
+        uint32_t mk = 0xffu;
+        if (has_mask) {
+          uint32_t bits = 0;
+          if constexpr (VE == 8) {
 #pragma unroll
-      for (int e = 0; e < VE; ++e) {
-        keep[e] = 1.f;
-        z[e] = DF{xv[e], 0.f};
+            for (int e = 0; e < 4; ++e) {
+              bits |= (((rm.x >> (8 * e)) & 0xffu) != 0u) << e;
+              bits |= (((rm.y >> (8 * e)) & 0xffu) != 0u) << (e + 4);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) bits |= (((rm >> (8 * e)) & 0xffu) != 0u) << e;
+          }
+          mk = bits;
+        }
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          keep[e] = ((mk >> e) & 1u) ? a.scale : 0.f;
+          z[e] = a.zin ? DF{xv[e], 0.f} : ln_z<FUSED, COMP>(xv[e], rv[e], bia[k][e], keep[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          keep[e] = 1.f;
+          z[e] = DF{xv[e], 0.f};
+        }
       }
-    }
-  };
+    };
 
-  const float inv_H = 1.f / (float)H;
-  bool failed = false;
-  int64_t i = 0;
-  for (; i < nmine; ++i) {
-    const int s = (int)(i % nst);
-    const uint32_t par = (uint32_t)((i / nst) & 1);
-    const int64_t r0 = (g + i * G) * RB;
-    const int nr = (int)(a.R - r0 < RB ? a.R - r0 : RB);
-    float mu[RB], rho[RB];
+    const float inv_H = 1.f / (float)H;
+    bool failed = false;
+    for (int64_t i = grp; i < nmine; i += NGRP) {
+      const int s = (int)(i % NS);
+      const uint32_t par = (uint32_t)((i / NS) & 1);
+      const int64_t r0 = (g + i * G) * RB;
+      const int nr = (int)(a.R - r0 < RB ? a.R - r0 : RB);
+      float mu[RPS], rho[RPS];
 #pragma unroll
-    for (int rr = 0; rr < RB; ++rr) {
-      mu[rr] = rr < nr ? a.mean[r0 + rr] : 0.f;
-      rho[rr] = rr < nr ? a.rstd[r0 + rr] : 0.f;
-    }
-    const bool ok = mbar_wait_bounded(&bar[s], par);
-    const unsigned char* st = data + (size_t)s * a.stage_bytes;
+      for (int q = 0; q < RPS; ++q) {
+        const int rr = q;
+        mu[q] = rr < nr ? __ldg(a.mean + r0 + rr) : 0.f;
+        rho[q] = rr < nr ? __ldg(a.rstd + r0 + rr) : 0.f;
+      }
+      const bool ok = __all_sync(0xffffffffu, ring_wait(&sh.full[s], par, &sh.abort));
+      if (i == 0 && ct == 0) GBN_RING_TRACE(1);
+      // This thread's vectors of its rows, into registers; then the stage is
+      // released so that the producer can refill it while we compute.
+      const unsigned char* st = data + (size_t)s * a.stage_bytes;
+      uint4 rdy[RPS][KV], rx[RPS][KV], rres[RPS][KV];
+      MaskRaw rmk[RPS][KV];
+#pragma unroll
+      for (int q = 0; q < RPS; ++q)
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+          const int rr = q, vi = lr + k * TPR;
+          const bool in = ok && rr < nr && vi < a.Hv;
+          const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
+          rdy[q][k] = in ? *reinterpret_cast<const uint4*>(st + a.off_dy + o) : make_uint4(0u, 0u, 0u, 0u);
+          rx[q][k] = in ? *reinterpret_cast<const uint4*>(st + a.off_x + o) : make_uint4(0u, 0u, 0u, 0u);
+          rres[q][k] = (in && with_res) ? *reinterpret_cast<const uint4*>(st + a.off_res + o)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+          if (in && has_mask)
+            rmk[q][k] = *reinterpret_cast<const MaskRaw*>(st + a.off_mask + (size_t)rr * H +
+                                                          (size_t)vi * VE);
+          else
+            rmk[q][k] = MaskRaw{};
+        }
+      if (ok) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[s]);
+      }
 
-    // Pass 1 over the stage: row sums of g and g*xhat.
-    float* slot = red + (i & 1) * (2 * RB * 32);
+      // Row sums of g and g*xhat of the stage's rows: per warp into the
+      // group's slots [buffer][row][sum][warp], double-buffered by stage.
+      // bf16 outputs keep xhat and the keep factors for the second pass.
+      float* slot = red + ((grp * 2 + (int)((i / NGRP) & 1)) * RB) * 2 * TPRW;
+      f2 xhs[COMP ? 1 : RPS][KV][NP], kps[COMP ? 1 : RPS][KV][NP];
+      float rsum[RPS][2];
 #pragma unroll
-    for (int rr = 0; rr < RB; ++rr) {
-      float sg = 0.f, sgx = 0.f;
-      if (ok && rr < nr) {
-        const f2 mu2 = f2_splat(mu[rr]), rho2 = f2_splat(rho[rr]);
+      for (int q = 0; q < RPS; ++q) {
+        const f2 mu2 = f2_splat(mu[q]), rho2 = f2_splat(rho[q]);
         f2 sg2 = 0ull, sgx2 = 0ull;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-          if (tid + k * (int)blockDim.x >= a.Hv) continue;
           f2 dy2[NP], z2[NP], keep2[NP];
-          load_pairs(st, rr, k, dy2, z2, keep2);
+          pairs(k, rdy[q][k], rx[q][k], rres[q][k], rmk[q][k], dy2, z2, keep2);
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
             const f2 xh2 = f2_mul(f2_sub(z2[p], mu2), rho2);
             const f2 g2 = f2_mul(dy2[p], gam2[k][p]);
             sg2 = f2_add(sg2, g2);
             sgx2 = f2_fma(g2, xh2, sgx2);
+            if constexpr (!COMP) {
+              xhs[q][k][p] = xh2;
+              kps[q][k][p] = keep2[p];
+            }
           }
         }
-        sg = f2_hsum(sg2);
-        sgx = f2_hsum(sgx2);
+        rsum[q][0] = f2_hsum(sg2);
+        rsum[q][1] = f2_hsum(sgx2);
       }
-      sg = warp_sum(sg);
-      sgx = warp_sum(sgx);
-      if (lane == 0) { slot[(2 * rr) * 32 + warp] = sg; slot[(2 * rr + 1) * 32 + warp] = sgx; }
-    }
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    if (tid == 0 && i >= 1 && i - 1 + nst < nmine) {
-      fence_proxy_async_smem();
-      issue(i - 1 + nst);
-    }
+      if constexpr (RPS == 2) {
+        const float v = warp_sum4_transposed(rsum[0][0], rsum[0][1], rsum[1][0], rsum[1][1]);
+        if ((lane & 7) == 0) slot[(lane >> 3) * TPRW + wis] = v;  // [row][sum] = lane / 8
+      } else {
+#pragma unroll
+        for (int q = 0; q < RPS; ++q) {
+          const float sg = warp_sum(rsum[q][0]), sgx = warp_sum(rsum[q][1]);
+          if (lane == 0) {
+            slot[(q * 2 + 0) * TPRW + wis] = sg;
+            slot[(q * 2 + 1) * TPRW + wis] = sgx;
+          }
+        }
+      }
+      if (consumers_bar_or(!ok, TPR, gbar)) {
+        failed = true;
+        if (lr == 0) ring_abort(sh, a.status);
+        break;
+      }
 
-    // Pass 2 over the stage: dz, outputs, column sums.
+      // dz, outputs and column sums for the stage's rows.
 #pragma unroll
-    for (int rr = 0; rr < RB; ++rr) {
-      if (rr >= nr) break;
-      const float mg = sum_warp_slots<MAXT / 32>(slot + (2 * rr) * 32, nwarps) * inv_H;
-      const float mgx = sum_warp_slots<MAXT / 32>(slot + (2 * rr + 1) * 32, nwarps) * inv_H;
-      const int64_t r = r0 + rr;
+      for (int q = 0; q < RPS; ++q) {
+        const int rr = q;
+        if (rr >= nr) break;
+        float SG = 0.f, SGX = 0.f;
+        for (int w = 0; w < TPRW; ++w) {
+          SG += slot[(rr * 2 + 0) * TPRW + w];
+          SGX += slot[(rr * 2 + 1) * TPRW + w];
+        }
+        const float mg = SG * inv_H, mgx = SGX * inv_H;
+        const int64_t r = r0 + rr;
 #pragma unroll
-      for (int k = 0; k < KV; ++k) {
-        const int vi = tid + k * blockDim.x;
-        if (vi >= a.Hv) continue;
-        const int64_t go = r * H + (int64_t)vi * VE;
-        if constexpr (COMP) {
-          float dzx[VE];
-          if (a.dzx != nullptr) {
-#pragma unroll
-            for (int e = 0; e < VE; e += 4) {
-              const float4 t = *reinterpret_cast<const float4*>(a.dzx + go + e);
-              dzx[e] = t.x; dzx[e + 1] = t.y; dzx[e + 2] = t.z; dzx[e + 3] = t.w;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < VE; ++e) dzx[e] = 0.f;
-          }
-          float dyv[VE], keep[VE];
-          DF z[VE];
-          load_elem(st, rr, k, dyv, z, keep);
-          float o_dz[VE], o_dx[VE];
-#pragma unroll
-          for (int e = 0; e < VE; ++e) {
-            // fp32 outputs: column sums of exactly evaluated terms
-            const float dyy = dyv[e];
-            const DF xh = df_mul(df_plus(two_sum(z[e].hi, -mu[rr]), z[e].lo), rho[rr]);
-            DF inner = df_plus(two_prod(dyy, gam[k][e]), -mg);
-            const DF xm = df_mul(xh, mgx);
-            inner = df_plus(DF{inner.hi, inner.lo - xm.lo}, -xm.hi);
-            const DF dz = df_plus(df_mul(inner, rho[rr]), dzx[e]);
-            const DF dxd = df_mul(dz, keep[e]);
-            o_dz[e] = df_round(dz);
-            o_dx[e] = df_round(dxd);
-            df_acc(acc_g[k][e], df_mul(xh, dyy));
-            df_add(acc_b[k][e], dyy);
-            if (FUSED) df_acc(acc_x[k][e], dxd);
-          }
-          Vec16<T>::store(static_cast<T*>(a.dx) + go, o_dx);
-          if (FUSED && a.dres != nullptr) Vec16<T>::store(static_cast<T*>(a.dres) + go, o_dz);
-        } else {
-          f2 dy2[NP], z2[NP], keep2[NP], dz2[NP], dx2[NP];
-          load_pairs(st, rr, k, dy2, z2, keep2);
-          const f2 mu2 = f2_splat(mu[rr]), rho2 = f2_splat(rho[rr]);
-          const f2 mg2 = f2_splat(mg), nmgx2 = f2_splat(-mgx);
-#pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            const f2 xh2 = f2_mul(f2_sub(z2[p], mu2), rho2);
-            const f2 g2 = f2_mul(dy2[p], gam2[k][p]);
-            const f2 inner = f2_fma(xh2, nmgx2, f2_sub(g2, mg2));
-            f2 extra = 0ull;
+        for (int k = 0; k < KV; ++k) {
+          const int vi = lr + k * TPR;
+          if (vi >= a.Hv) continue;
+          const int64_t go = r * H + (int64_t)vi * VE;
+          if constexpr (COMP) {
+            float dzx[VE];
             if (a.dzx != nullptr) {
-              const float2 t = *reinterpret_cast<const float2*>(a.dzx + go + 2 * p);
-              extra = f2_pack(t.x, t.y);
-            }
-            dz2[p] = f2_fma(inner, rho2, extra);
-            dx2[p] = FUSED ? f2_mul(dz2[p], keep2[p]) : dz2[p];
-            sg_g[k][p] = f2_fma(dy2[p], xh2, sg_g[k][p]);
-            sg_b[k][p] = f2_add(sg_b[k][p], dy2[p]);
-            if (FUSED) sg_x[k][p] = f2_add(sg_x[k][p], dx2[p]);
-          }
-          *reinterpret_cast<uint4*>(static_cast<T*>(a.dx) + go) = PK::put(dx2);
-          if (FUSED && a.dres != nullptr) {
-            if (a.dres_f32) {
-              float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.dres) + go);
 #pragma unroll
-              for (int p = 0; p < NP; p += 2) {
-                const float2 u = f2_unpack(dz2[p]), w = f2_unpack(dz2[p + 1]);
-                d4[p / 2] = make_float4(u.x, u.y, w.x, w.y);
+              for (int e = 0; e < VE; e += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(a.dzx + go + e);
+                dzx[e] = t.x; dzx[e + 1] = t.y; dzx[e + 2] = t.z; dzx[e + 3] = t.w;
               }
             } else {
-              *reinterpret_cast<uint4*>(static_cast<T*>(a.dres) + go) = PK::put(dz2);
+#pragma unroll
+              for (int e = 0; e < VE; ++e) dzx[e] = 0.f;
+            }
+            float dyv[VE], keep[VE];
+            DF z[VE];
+            elems(k, rdy[q][k], rx[q][k], rres[q][k], rmk[q][k], dyv, z, keep);
+            float o_dz[VE], o_dx[VE];
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+              // fp32 outputs: column sums of exactly evaluated terms
+              const float dyy = dyv[e];
+              const DF xh = df_mul(df_plus(two_sum(z[e].hi, -mu[q]), z[e].lo), rho[q]);
+              DF inner = df_plus(two_prod(dyy, gam[k][e]), -mg);
+              const DF xm = df_mul(xh, mgx);
+              inner = df_plus(DF{inner.hi, inner.lo - xm.lo}, -xm.hi);
+              const DF dz = df_plus(df_mul(inner, rho[q]), dzx[e]);
+              const DF dxd = df_mul(dz, keep[e]);
+              o_dz[e] = df_round(dz);
+              o_dx[e] = df_round(dxd);
+              df_acc(acc_g[k][e], df_mul(xh, dyy));
+              df_add(acc_b[k][e], dyy);
+              if (FUSED) df_acc(acc_x[k][e], dxd);
+            }
+            Vec16<T>::store(static_cast<T*>(a.dx) + go, o_dx);
+            if (FUSED && a.dres != nullptr) Vec16<T>::store(static_cast<T*>(a.dres) + go, o_dz);
+          } else {
+            f2 dy2[NP], dz2[NP], dx2[NP];
+            PK::get(rdy[q][k], dy2);
+            const f2 rho2 = f2_splat(rho[q]);
+            const f2 mg2 = f2_splat(mg), nmgx2 = f2_splat(-mgx);
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+              const f2 xh2 = xhs[q][k][p];
+              const f2 g2 = f2_mul(dy2[p], gam2[k][p]);
+              const f2 inner = f2_fma(xh2, nmgx2, f2_sub(g2, mg2));
+              f2 extra = 0ull;
+              if (a.dzx != nullptr) {
+                const float2 t = *reinterpret_cast<const float2*>(a.dzx + go + 2 * p);
+                extra = f2_pack(t.x, t.y);
+              }
+              dz2[p] = f2_fma(inner, rho2, extra);
+              dx2[p] = FUSED ? f2_mul(dz2[p], kps[q][k][p]) : dz2[p];
+              sg_g[k][p] = f2_fma(dy2[p], xh2, sg_g[k][p]);
+              sg_b[k][p] = f2_add(sg_b[k][p], dy2[p]);
+              if (FUSED) sg_x[k][p] = f2_add(sg_x[k][p], dx2[p]);
+            }
+            *reinterpret_cast<uint4*>(static_cast<T*>(a.dx) + go) = PK::put(dx2);
+            if (FUSED && a.dres != nullptr) {
+              if (a.dres_f32) {
+                float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.dres) + go);
+#pragma unroll
+                for (int p = 0; p < NP; p += 2) {
+                  const float2 u = f2_unpack(dz2[p]), w = f2_unpack(dz2[p + 1]);
+                  d4[p / 2] = make_float4(u.x, u.y, w.x, w.y);
+                }
+              } else {
+                *reinterpret_cast<uint4*>(static_cast<T*>(a.dres) + go) = PK::put(dz2);
+              }
             }
           }
         }
       }
     }
-  }
-
-  if (failed) {
-    report_status(a.status, GBN_DEV_WAIT_TIMEOUT);
-    if (tid == 0) {
-      // Blocks issued and not consumed: i .. i + nst - 2 (lagged refill).
-      for (int64_t k = i; k < nmine && k < i + nst - 1; ++k)
-        mbar_wait_bounded(&bar[k % nst], (uint32_t)((k / nst) & 1), kWaitLimitNs / 8);
-    }
-    __syncthreads();
-    return;
-  }
-
-  if constexpr (!COMP) {
+    // every group has left its loop (a failed group has set the abort flag,
+    // which ends the others' waits): one decision for all consumers
+    failed = consumers_bar_or(failed, NC);
+    if (ct == 0) GBN_RING_TRACE(2);
+    if (!failed) {
+      if constexpr (!COMP) {
 #pragma unroll
-    for (int k = 0; k < KV; ++k)
+        for (int k = 0; k < KV; ++k)
 #pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        const float2 a0 = f2_unpack(sg_g[k][p]), a1 = f2_unpack(sg_b[k][p]),
-                     a2 = f2_unpack(sg_x[k][p]);
-        acc_g[k][2 * p].hi = a0.x;
-        acc_g[k][2 * p + 1].hi = a0.y;
-        acc_b[k][2 * p].hi = a1.x;
-        acc_b[k][2 * p + 1].hi = a1.y;
-        acc_x[k][2 * p].hi = a2.x;
-        acc_x[k][2 * p + 1].hi = a2.y;
+          for (int p = 0; p < NP; ++p) {
+            const float2 a0 = f2_unpack(sg_g[k][p]), a1 = f2_unpack(sg_b[k][p]),
+                         a2 = f2_unpack(sg_x[k][p]);
+            acc_g[k][2 * p].hi = a0.x;
+            acc_g[k][2 * p + 1].hi = a0.y;
+            acc_b[k][2 * p].hi = a1.x;
+            acc_b[k][2 * p + 1].hi = a1.y;
+            acc_x[k][2 * p].hi = a2.x;
+            acc_x[k][2 * p + 1].hi = a2.y;
+          }
       }
-  }
-
-  // Column partials [nout][nplanes][G][H]: 0 = dgamma, 1 = dbeta, 2 = dbias.
-  auto store_part = [&](int o, int k, const DF (&acc)[VE]) {
-    const int vi = tid + k * blockDim.x;
-    float* hi = a.part + (((int64_t)o * a.nplanes + 0) * G + g) * H + (int64_t)vi * VE;
-    float* lo = a.part + (((int64_t)o * a.nplanes + 1) * G + g) * H + (int64_t)vi * VE;
+      // The groups' column sums, added in group order in shared memory
+      // (the ring is idle now: every stage has been consumed), then written
+      // as this CTA's partial row of each output:
+      // part[o][plane][g][h], o = 0 dgamma, 1 dbeta, 2 dbias.
+      const int nout = FUSED ? 3 : 2;
+      const int nplanes = COMP ? 2 : 1;
+      float* sm = reinterpret_cast<float*>(data);  // [nout][nplanes][H]
+      consumers_bar(NC);
+      for (int q = 0; q < NGRP; ++q) {
+        if (grp == q) {
 #pragma unroll
-    for (int e = 0; e < VE; e += 4) {
-      *reinterpret_cast<float4*>(hi + e) =
-          make_float4(acc[e].hi, acc[e + 1].hi, acc[e + 2].hi, acc[e + 3].hi);
-      if constexpr (COMP)
-        *reinterpret_cast<float4*>(lo + e) =
-            make_float4(acc[e].lo, acc[e + 1].lo, acc[e + 2].lo, acc[e + 3].lo);
+          for (int k = 0; k < KV; ++k) {
+            const int vi = lr + k * TPR;
+            if (vi >= a.Hv) continue;
+            auto put = [&](int o, const DF (&acc)[VE]) {
+              float* hi = sm + ((int64_t)o * nplanes) * H + (int64_t)vi * VE;
+              float* lo = hi + H;
+#pragma unroll
+              for (int e = 0; e < VE; ++e) {
+                if (q == 0) {
+                  hi[e] = acc[e].hi;
+                  if constexpr (COMP) lo[e] = acc[e].lo;
+                } else if constexpr (COMP) {
+                  const DF t = df_sum(DF{hi[e], lo[e]}, acc[e]);
+                  hi[e] = t.hi;
+                  lo[e] = t.lo;
+                } else {
+                  hi[e] += acc[e].hi;
+                }
+              }
+            };
+            put(0, acc_g[k]);
+            put(1, acc_b[k]);
+            if (FUSED) put(2, acc_x[k]);
+          }
+        }
+        consumers_bar(NC);
+      }
+      const int64_t n4 = (int64_t)nout * nplanes * H / 4;
+      for (int64_t v = ct; v < n4; v += NC) {
+        const int64_t e = v * 4;
+        const int64_t op = e / H, h = e - op * H;  // op = o * nplanes + plane
+        *reinterpret_cast<float4*>(a.part + (op * G + g) * H + h) =
+            *reinterpret_cast<const float4*>(sm + e);
+      }
+      if (ct == 0) GBN_RING_TRACE(3);
+      if (ring_exchange(sh, a.sync, G, ct, NC, a.status)) {
+        if (ct == 0) GBN_RING_TRACE(4);
+        T* outs[3] = {static_cast<T*>(a.dgamma), static_cast<T*>(a.dbeta),
+                      FUSED ? static_cast<T*>(a.dbias) : nullptr};
+        colsum_warps<T, COMP>(a.part, nout, G, H, outs, g, G, cw, NCW, lane);
+        if (ct == 0) GBN_RING_TRACE(5);
+      }
+    } else if (ct == 0) {
+      ring_abort(sh, a.status);
     }
-  };
-#pragma unroll
-  for (int k = 0; k < KV; ++k) {
-    if (tid + k * (int)blockDim.x >= a.Hv) continue;
-    store_part(0, k, acc_g[k]);
-    store_part(1, k, acc_b[k]);
-    if (FUSED) store_part(2, k, acc_x[k]);
   }
-  pdl_launch_dependents();
+  __syncthreads();
+  if (tid == 0 && sh.abort) ring_drain(sh, NS);
 }
 
 // Any H and alignment.  Block g owns rows g, g+G, ...; thread t owns columns
@@ -564,32 +690,37 @@ __global__ void __launch_bounds__(256) ln_bwd_generic_kernel(LnArgs a) {
   pdl_launch_dependents();
 }
 
-template <typename T, int KV, int RB, bool FUSED, int MAXT, int MINB>
-cudaError_t launch_fast(const RowPlan& p, const LnArgs& a, cudaStream_t st) {
-  return launch(ln_bwd_fast_kernel<T, KV, RB, FUSED, MAXT, MINB>, dim3(p.G), dim3(p.threads),
-                p.smem, st, false, a);
+template <typename T, int KV, bool FUSED>
+cudaError_t launch_ring(const RowPlan& p, const LnArgs& a, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.G);
+  cfg.blockDim = dim3((unsigned)p.threads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ln_bwd_ring_kernel<T, KV, FUSED, kLnRingWarps[KV]>, a);
 }
 
-// Instances (KV, RB, max threads, min blocks per SM).  Rows of at most 256
-// 16-byte vectors: four rows per stage and two blocks per SM (measured 6 %
-// faster than two rows and three blocks, which remains for smaller shared
-// memory); one block per SM otherwise (128 registers).  The plan keeps at
-// most 16 owned columns per thread, so kv is 1 or 2.
+// Ring instances: KV = 1 (at most 14 consumer warps) and, for bf16, KV = 2
+// (at most 8), the counts the plan uses.
 template <typename T, bool FUSED>
 cudaError_t launch_typed(const RowPlan& p, const LnArgs& a, cudaStream_t st) {
   if (!p.fast)
     return launch(ln_bwd_generic_kernel<T, FUSED>, dim3(p.G), dim3(p.threads), 0, st, false, a);
-  if (p.rb == 4) return launch_fast<T, 1, 4, FUSED, 256, 2>(p, a, st);
-  if (p.rb == 2) return launch_fast<T, 1, 2, FUSED, 256, 3>(p, a, st);
-  if (p.kv == 1) return launch_fast<T, 1, 1, FUSED, 512, 1>(p, a, st);
-  return launch_fast<T, 2, 1, FUSED, 512, 1>(p, a, st);
+  if constexpr (sizeof(T) == 2)
+    if (p.kv == 2) return launch_ring<T, 2, FUSED>(p, a, st);
+  return launch_ring<T, 1, FUSED>(p, a, st);
 }
 
-template <typename T, int KV, int RB, int MAXT, int MINB>
+template <typename T, int KV>
 cudaError_t set_smem(int bytes) {
-  cudaError_t e1 = cudaFuncSetAttribute(ln_bwd_fast_kernel<T, KV, RB, true, MAXT, MINB>,
+  cudaError_t e1 = cudaFuncSetAttribute(ln_bwd_ring_kernel<T, KV, true, kLnRingWarps[KV]>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  cudaError_t e2 = cudaFuncSetAttribute(ln_bwd_fast_kernel<T, KV, RB, false, MAXT, MINB>,
+  cudaError_t e2 = cudaFuncSetAttribute(ln_bwd_ring_kernel<T, KV, false, kLnRingWarps[KV]>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   return e1 != cudaSuccess ? e1 : e2;
 }
@@ -597,64 +728,69 @@ cudaError_t set_smem(int bytes) {
 template <typename T>
 cudaError_t set_smem_all(int bytes) {
   cudaError_t e = cudaSuccess, r;
-  if ((r = set_smem<T, 1, 4, 256, 2>(bytes)) != cudaSuccess) e = r;
-  if ((r = set_smem<T, 1, 2, 256, 3>(bytes)) != cudaSuccess) e = r;
-  if ((r = set_smem<T, 1, 1, 512, 1>(bytes)) != cudaSuccess) e = r;
-  if ((r = set_smem<T, 2, 1, 512, 1>(bytes)) != cudaSuccess) e = r;
+  if ((r = set_smem<T, 1>(bytes)) != cudaSuccess) e = r;
+  if constexpr (sizeof(T) == 2)
+    if ((r = set_smem<T, 2>(bytes)) != cudaSuccess) e = r;
   return e;
 }
 
 }  // namespace
 
-uint32_t ln_smem_header(int rb) { return ln_header(rb); }
-
 cudaError_t ln_configure(int smem_optin) {
-  cudaError_t e1 = set_smem_all<float>(smem_optin);
-  cudaError_t e2 = set_smem_all<bf16>(smem_optin);
+  const int dyn = smem_optin - kRowStaticSmem;
+  cudaError_t e1 = set_smem_all<float>(dyn);
+  cudaError_t e2 = set_smem_all<bf16>(dyn);
   return e1 != cudaSuccess ? e1 : e2;
 }
 
-cudaError_t ln_launch(const RowPlan& p, const LnPtrs& q, float* part, int* status,
+cudaError_t ln_launch(const RowPlan& p, const LnPtrs& q, void* ws, int* status,
                       cudaStream_t st) {
   const bool fused = p.kind == GBN_ROW_LN_FUSED;
-  cudaError_t e = cudaSuccess;
-  if (p.R > 0 && p.H > 0) {
-    LnArgs a;
-    a.dy = q.dy;
-    a.x = q.x;
-    a.res = q.residual;
-    a.bias = q.bias;
-    a.mask = q.mask;
-    a.dzx = q.dz_extra;
-    a.mean = q.mean;
-    a.rstd = q.rstd;
-    a.gamma = q.gamma;
-    a.dx = q.dx;
-    a.dres = q.dres;
-    a.part = part;
-    a.status = status;
-    a.R = p.R;
-    a.scale = q.scale;
-    a.H = (int32_t)p.H;
-    a.Hv = (int32_t)(p.H * (p.dtype == GBN_F32 ? 4 : 2) / 16);
-    a.nstage = p.nstage;
-    a.nplanes = p.nplanes;
-    a.zin = q.saved_z ? 1 : 0;
-    a.dres_f32 = q.dres_f32 ? 1 : 0;
-    a.stage_bytes = p.stage_bytes;
-    a.off_dy = p.off[0];
-    a.off_x = p.off[1];
-    a.off_res = p.off[2];
-    a.off_mask = p.off[3];
-    if (p.dtype == GBN_F32)
-      e = fused ? launch_typed<float, true>(p, a, st) : launch_typed<float, false>(p, a, st);
-    else
-      e = fused ? launch_typed<bf16, true>(p, a, st) : launch_typed<bf16, false>(p, a, st);
-    if (e != cudaSuccess) return e;
-  }
   void* outs[3] = {q.dgamma, q.dbeta, fused ? q.dbias : nullptr};
-  return colsum_launch(part, fused ? 3 : 2, p.nplanes, p.R > 0 ? p.G : 0, p.H, p.dtype, outs, st,
-                       p.R > 0 && p.H > 0);
+  if (p.R == 0 || p.H == 0)  // no rows: the column outputs are sums of nothing
+    return colsum_launch(nullptr, fused ? 3 : 2, p.nplanes, 0, p.H, p.dtype, outs, st, false);
+  LnArgs a;
+  a.dy = q.dy;
+  a.x = q.x;
+  a.res = q.residual;
+  a.bias = q.bias;
+  a.mask = q.mask;
+  a.dzx = q.dz_extra;
+  a.mean = q.mean;
+  a.rstd = q.rstd;
+  a.gamma = q.gamma;
+  a.dx = q.dx;
+  a.dres = q.dres;
+  a.dgamma = q.dgamma;
+  a.dbeta = q.dbeta;
+  a.dbias = fused ? q.dbias : nullptr;
+  a.sync = static_cast<unsigned long long*>(ws);
+  a.part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + p.part_offset);
+  a.nonce = next_nonce();
+  a.status = status;
+  a.R = p.R;
+  a.scale = q.scale;
+  a.H = (int32_t)p.H;
+  a.Hv = (int32_t)(p.H * (p.dtype == GBN_F32 ? 4 : 2) / 16);
+  a.nstage = p.nstage;
+  a.nplanes = p.nplanes;
+  a.zin = q.saved_z ? 1 : 0;
+  a.dres_f32 = q.dres_f32 ? 1 : 0;
+  a.stage_bytes = p.stage_bytes;
+  a.off_dy = p.off[0];
+  a.off_x = p.off[1];
+  a.off_res = p.off[2];
+  a.off_mask = p.off[3];
+  a.tprw = p.tprw;
+  a.rs = p.rs;
+  cudaError_t e;
+  if (p.dtype == GBN_F32)
+    e = fused ? launch_typed<float, true>(p, a, st) : launch_typed<float, false>(p, a, st);
+  else
+    e = fused ? launch_typed<bf16, true>(p, a, st) : launch_typed<bf16, false>(p, a, st);
+  if (e != cudaSuccess || p.fast) return e;
+  // the plain kernel leaves its column partials for a second launch
+  return colsum_launch(a.part, fused ? 3 : 2, p.nplanes, p.G, p.H, p.dtype, outs, st, true);
 }
 
 }  // namespace gbn

@@ -12,8 +12,6 @@
 
 namespace gbn {
 
-uint32_t rms_smem_header(int rb);
-uint32_t ln_smem_header(int rb);
 cudaError_t rms_configure(int smem_optin);
 cudaError_t ln_configure(int smem_optin);
 
@@ -22,6 +20,13 @@ namespace {
 constexpr int kColTile = 32;
 constexpr int kColGroups = 32;
 constexpr int kMaxStages = 8;
+constexpr int kRmsConsumers = 512;       // consumer threads of the RMSNorm ring kernel
+constexpr int kRowRingStatic = 4096;     // static shared memory of a ring kernel, at most
+constexpr int kLnMaxGroups = 14;         // consumer groups (named barriers 2..15) of the LayerNorm ring kernel
+
+// Epoch pair, arrival counter and one flag pair per CTA, rounded to 256
+// bytes (the layout of row_engine.cuh).
+size_t ring_sync_bytes(int G) { return ((size_t)32 + (size_t)16 * G + 255) & ~(size_t)255; }
 
 struct ColOuts {
   void* p[3];
@@ -94,45 +99,60 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
   p->nout = kind == GBN_ROW_RMS ? 1 : (kind == GBN_ROW_LN ? 2 : 3);
   p->nplanes = dtype == GBN_F32 ? 2 : 1;
   const int64_t esize = dtype == GBN_F32 ? 4 : 2;
-  const int64_t VE = 16 / esize;
   const bool fused = kind == GBN_ROW_LN_FUSED;
 
   bool fast = fast_ok && R > 0 && H > 0 && (H * esize) % 16 == 0 && (!has_mask || H % 16 == 0);
-  if (fast) {
+  if (fast && kind == GBN_ROW_RMS && H % 8 != 0) fast = false;  // column sums take 8 at a time
+  if (fast && kind == GBN_ROW_RMS) {
+    // Ring kernel: 16 consumer warps + the producer warp, one CTA per SM;
+    // each consumer thread owns kv 16-byte vectors of a row.
     const int64_t Hv = H * esize / 16;
-    const int64_t kv = (Hv + 511) / 512;
-    const int64_t threads = ((Hv + kv - 1) / kv + 31) / 32 * 32;
-    // Registers: at most 16 owned columns per thread (8 for the fp32
-    // LayerNorm, whose three column sums are double-fp32).
-    const int64_t max_cols = (kind != GBN_ROW_RMS && dtype == GBN_F32) ? 8 : 16;
-    if (kv * VE > max_cols || kv > 4 || (kind != GBN_ROW_RMS && kv > 2)) fast = false;
-    // (rows per stage, blocks per SM) in order of preference; these match
-    // the compiled kernel instances.
-    int cand[3][2];
-    int ncand = 0;
-    if (kind == GBN_ROW_RMS) {
-      // Two-vector rows (e.g. 8192 bf16): two rows per stage at one block
-      // per SM amortise the per-row barrier and bookkeeping over twice the
-      // elements (29.3 vs 32.4 us at [2048, 8192] bf16).
-      if (kv == 2) cand[ncand][0] = 2, cand[ncand++][1] = 1;
-      cand[ncand][0] = kv == 1 ? 2 : 1;
-      cand[ncand++][1] = kv <= 2 ? 2 : 1;
-    } else if (kv == 1 && threads <= 256) {
-      cand[ncand][0] = 4, cand[ncand++][1] = 2;
-      cand[ncand][0] = 2, cand[ncand++][1] = 3;
-    } else if (kv == 1) {
-      cand[ncand][0] = 1, cand[ncand++][1] = 1;
+    const int64_t kv = (Hv + kRmsConsumers - 1) / kRmsConsumers;
+    const int rb = kv == 1 ? 2 : 1;
+    const uint64_t stage = 2ull * rb * (uint64_t)H * esize;
+    const int64_t dyn = (int64_t)dev.smem_optin - kRowRingStatic;
+    int64_t nst = dyn / (int64_t)stage;
+    if (nst > kMaxStages) nst = kMaxStages;
+    if (kv <= 4 && nst >= 2) {
+      const int64_t nblk = (R + rb - 1) / rb;
+      p->fast = true;
+      p->threads = kRmsConsumers + 32;
+      p->kv = (int)kv;
+      p->rb = rb;
+      p->cps = 1;
+      p->nstage = (int)nst;
+      p->stage_bytes = (uint32_t)stage;
+      p->G = (int)(nblk < dev.sms ? nblk : dev.sms);
+      p->smem = (size_t)nst * stage;
+      p->part_offset = ring_sync_bytes(p->G);
     } else {
-      cand[ncand][0] = 1, cand[ncand++][1] = 1;
+      fast = false;
     }
-    bool placed = false;
-    for (int ci = 0; fast && ci < ncand && !placed; ++ci) {
-      const int rb = cand[ci][0], cps = cand[ci][1];
+  } else if (fast) {
+    // LayerNorm ring kernel: NGRP groups of TPRW consumer warps (at most 14
+    // or 8 warps in all) + the producer warp, one CTA per SM; each consumer
+    // thread owns kv 16-byte vectors of a row; a stage holds two rows for
+    // one-vector rows, else one, and goes to one group.
+    const int64_t Hv = H * esize / 16;
+    int64_t kv = 1, maxw = kLnRingWarpsKV1;
+    if (Hv > 32 * kLnRingWarpsKV1) {  // two vectors per thread (bf16 rows up to 4096)
+      kv = 2;
+      maxw = kLnRingWarpsKVn;
+    }
+    const int64_t tprw = (Hv + 32 * kv - 1) / (32 * kv);
+    // fp32 keeps three double-fp32 column sums per element: one vector per
+    // thread at most; the column sums take 8 columns at a time.
+    if (tprw > maxw || (dtype == GBN_F32 && kv > 1) || H % 8 != 0) {
+      fast = false;
+    } else {
+      const int rb = kv == 1 ? 2 : 1;
+      int64_t rs = maxw / tprw;  // groups
+      if (rs > kLnMaxGroups) rs = kLnMaxGroups;
       const uint64_t rowb = (uint64_t)H * esize;
       uint32_t off = 0;
-      p->off[0] = 0;  // dy (LayerNorm) / x (RMSNorm: x rows then dy rows)
+      p->off[0] = 0;  // dy
       off = round16(rb * rowb);
-      p->off[1] = off;  // x / input (LayerNorm)
+      p->off[1] = off;  // x / input
       off = round16(off + rb * rowb);
       if (fused) {
         p->off[2] = off;  // residual
@@ -142,35 +162,41 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
           off = round16(off + (uint64_t)rb * H);
         }
       }
-      const uint32_t header = kind == GBN_ROW_RMS ? rms_smem_header(rb) : ln_smem_header(rb);
-      int64_t per_block = (int64_t)dev.smem_per_sm / cps - dev.smem_reserved;
-      if (per_block > dev.smem_optin) per_block = dev.smem_optin;
-      int64_t nst = (per_block - header) / off;
+      const int64_t dyn = (int64_t)dev.smem_optin - kRowRingStatic;
+      int64_t nst = dyn / (int64_t)off;
       if (nst > kMaxStages) nst = kMaxStages;
-      if (nst < 2) continue;
-      const int64_t nblk = (R + rb - 1) / rb;
-      const int64_t slots = (int64_t)dev.sms * cps;
-      p->fast = true;
-      p->threads = (int)threads;
-      p->kv = (int)kv;
-      p->rb = rb;
-      p->cps = cps;
-      p->nstage = (int)nst;
-      p->stage_bytes = off;
-      p->smem = header + (size_t)nst * off;
-      p->G = (int)(nblk < slots ? nblk : slots);
-      placed = true;
+      // the slots' column sums are added in the idle ring at the end
+      const uint64_t combine = (uint64_t)p->nout * p->nplanes * (uint64_t)H * 4;
+      if (nst < 2 || combine > (uint64_t)dyn) {
+        fast = false;
+      } else {
+        const int64_t nblk = (R + rb - 1) / rb;
+        const uint64_t ring = (uint64_t)nst * off;
+        p->fast = true;
+        p->threads = (int)(32 + rs * tprw * 32);
+        p->kv = (int)kv;
+        p->rb = rb;
+        p->tprw = (int)tprw;
+        p->rs = (int)rs;
+        p->cps = 1;
+        p->nstage = (int)nst;
+        p->stage_bytes = off;
+        p->smem = (size_t)(ring > combine ? ring : combine);
+        p->G = (int)(nblk < dev.sms ? nblk : dev.sms);
+        p->part_offset = ring_sync_bytes(p->G);
+      }
     }
-    if (!placed) fast = false;
   }
   if (!fast) {
     p->fast = false;
     p->threads = 256;
+    p->part_offset = 0;
     const int64_t cap = 2 * (int64_t)dev.sms;
     p->G = (int)(R < cap ? R : cap);
   }
   const uint64_t g = p->G > 0 ? (uint64_t)p->G : 1;
-  const uint64_t bytes = (uint64_t)p->nout * p->nplanes * g * (uint64_t)(H > 0 ? H : 1) * 4;
+  const uint64_t bytes =
+      p->part_offset + (uint64_t)p->nout * p->nplanes * g * (uint64_t)(H > 0 ? H : 1) * 4;
   p->ws_bytes = (size_t)((bytes + 255) & ~(uint64_t)255);
   return true;
 }

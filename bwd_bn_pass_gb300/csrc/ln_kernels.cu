@@ -100,7 +100,9 @@ __device__ __forceinline__ f2 keep_pair(uint2 m, int p, float s) {
   return f2_pack(lo, hi);
 }
 
-constexpr int kLnMaxRedFloats = 16 * 2 * 2 * 2;  // [group, buffer, row, sum, warp] slots
+// Row-sum slots [group][buffer][row][sum][warp], each warp run padded to a
+// multiple of 4 floats (read as float4); at most 14 groups x 2 x 2 x 2 x 16.
+constexpr int kLnMaxRedFloats = 512;
 
 // Bit 7 of every byte of the result is set iff that byte of w is nonzero.
 __device__ __forceinline__ uint32_t bytes_nonzero(uint32_t w) {
@@ -185,6 +187,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
   const bool has_mask = FUSED && a.mask != nullptr;
   const bool with_res = FUSED && !a.zin;
 
+  const int P = (TPRW + 3) & ~3;  // padded warp run of a slot
+  for (int k = tid; k < kLnMaxRedFloats; k += blockDim.x) red[k] = 0.f;  // padding stays 0
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&sh.full[s], 1);
@@ -192,7 +196,6 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
       sh.issued[s] = 0;
     }
     sh.abort = 0;
-    sh.target = flag_target(a.sync, a.nonce);
     fence_mbarrier_init();
     GBN_RING_TRACE(0);
   }
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
   } else if (tid - 32 < NC) {
     const int ct = tid - 32, lane = ct & 31, cw = ct >> 5;
     const int grp = cw / TPRW, wis = cw - grp * TPRW, lr = ct - grp * TPR;
+    epoch_read(sh, a.sync, ct);
     const int gbar = 2 + grp;  // the group's named barrier
 
     // Per-column constants and accumulators of this thread's columns.  fp32
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
       // Row sums of g and g*xhat of the stage's rows: per warp into the
       // group's slots [buffer][row][sum][warp], double-buffered by stage.
       // bf16 outputs keep xhat and the keep factors for the second pass.
-      float* slot = red + ((grp * 2 + (int)((i / NGRP) & 1)) * RB) * 2 * TPRW;
+      float* slot = red + ((grp * 2 + (int)((i / NGRP) & 1)) * RB) * 2 * P;
       f2 xhs[COMP ? 1 : RPS][KV][NP], kps[COMP ? 1 : RPS][KV][NP];
       float rsum[RPS][2];
 #pragma unroll
@@ -390,14 +394,14 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
       }
       if constexpr (RPS == 2) {
         const float v = warp_sum4_transposed(rsum[0][0], rsum[0][1], rsum[1][0], rsum[1][1]);
-        if ((lane & 7) == 0) slot[(lane >> 3) * TPRW + wis] = v;  // [row][sum] = lane / 8
+        if ((lane & 7) == 0) slot[(lane >> 3) * P + wis] = v;  // [row][sum] = lane / 8
       } else {
 #pragma unroll
         for (int q = 0; q < RPS; ++q) {
           const float sg = warp_sum(rsum[q][0]), sgx = warp_sum(rsum[q][1]);
           if (lane == 0) {
-            slot[(q * 2 + 0) * TPRW + wis] = sg;
-            slot[(q * 2 + 1) * TPRW + wis] = sgx;
+            slot[(q * 2 + 0) * P + wis] = sg;
+            slot[(q * 2 + 1) * P + wis] = sgx;
           }
         }
       }
@@ -413,9 +417,12 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
         const int rr = q;
         if (rr >= nr) break;
         float SG = 0.f, SGX = 0.f;
-        for (int w = 0; w < TPRW; ++w) {
-          SG += slot[(rr * 2 + 0) * TPRW + w];
-          SGX += slot[(rr * 2 + 1) * TPRW + w];
+        const float4* s0 = reinterpret_cast<const float4*>(slot + (rr * 2 + 0) * P);
+        const float4* s1 = reinterpret_cast<const float4*>(slot + (rr * 2 + 1) * P);
+        for (int j = 0; j < P / 4; ++j) {
+          const float4 u = s0[j], w = s1[j];
+          SG += (u.x + u.y) + (u.z + u.w);
+          SGX += (w.x + w.y) + (w.z + w.w);
         }
         const float mg = SG * inv_H, mgx = SGX * inv_H;
         const int64_t r = r0 + rr;
@@ -531,19 +538,24 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
             const int vi = lr + k * TPR;
             if (vi >= a.Hv) continue;
             auto put = [&](int o, const DF (&acc)[VE]) {
-              float* hi = sm + ((int64_t)o * nplanes) * H + (int64_t)vi * VE;
-              float* lo = hi + H;
+              float4* hi = reinterpret_cast<float4*>(sm + ((int64_t)o * nplanes) * H + (int64_t)vi * VE);
+              float4* lo = reinterpret_cast<float4*>(reinterpret_cast<float*>(hi) + H);
 #pragma unroll
-              for (int e = 0; e < VE; ++e) {
+              for (int e = 0; e < VE; e += 4) {
+                float4 h = make_float4(acc[e].hi, acc[e + 1].hi, acc[e + 2].hi, acc[e + 3].hi);
                 if (q == 0) {
-                  hi[e] = acc[e].hi;
-                  if constexpr (COMP) lo[e] = acc[e].lo;
+                  hi[e / 4] = h;
+                  if constexpr (COMP)
+                    lo[e / 4] = make_float4(acc[e].lo, acc[e + 1].lo, acc[e + 2].lo, acc[e + 3].lo);
                 } else if constexpr (COMP) {
-                  const DF t = df_sum(DF{hi[e], lo[e]}, acc[e]);
-                  hi[e] = t.hi;
-                  lo[e] = t.lo;
+                  const float4 ph = hi[e / 4], pl = lo[e / 4];
+                  const DF t0 = df_sum(DF{ph.x, pl.x}, acc[e]), t1 = df_sum(DF{ph.y, pl.y}, acc[e + 1]);
+                  const DF t2 = df_sum(DF{ph.z, pl.z}, acc[e + 2]), t3 = df_sum(DF{ph.w, pl.w}, acc[e + 3]);
+                  hi[e / 4] = make_float4(t0.hi, t1.hi, t2.hi, t3.hi);
+                  lo[e / 4] = make_float4(t0.lo, t1.lo, t2.lo, t3.lo);
                 } else {
-                  hi[e] += acc[e].hi;
+                  const float4 ph = hi[e / 4];
+                  hi[e / 4] = make_float4(ph.x + h.x, ph.y + h.y, ph.z + h.z, ph.w + h.w);
                 }
               }
             };
@@ -562,7 +574,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
             *reinterpret_cast<const float4*>(sm + e);
       }
       if (ct == 0) GBN_RING_TRACE(3);
-      if (ring_exchange(sh, a.sync, G, ct, NC, a.status)) {
+      if (ring_exchange(sh, a.sync, G, ct, NC, a.status, a.nonce)) {
         if (ct == 0) GBN_RING_TRACE(4);
         T* outs[3] = {static_cast<T*>(a.dgamma), static_cast<T*>(a.dbeta),
                       FUSED ? static_cast<T*>(a.dbias) : nullptr};

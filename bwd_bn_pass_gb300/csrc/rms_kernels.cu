@@ -101,7 +101,6 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
       sh.issued[s] = 0;
     }
     sh.abort = 0;
-    sh.target = flag_target(a.sync, a.nonce);
     fence_mbarrier_init();
     GBN_RING_TRACE(0);
   }
@@ -123,6 +122,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
     }
   } else {
     const int ct = tid - 32, lane = ct & 31, cw = ct >> 5;
+    epoch_read(sh, a.sync, ct);
     // Weights and the dweight accumulators of this thread's columns, packed.
     f2 w2[KV][NP], acc[KV][NP], acc_lo[KV][NP];
     const T* w = static_cast<const T*>(a.w);
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
         }
       }
       if (ct == 0) GBN_RING_TRACE(3);
-      if (ring_exchange(sh, a.sync, G, ct, NC, a.status)) {
+      if (ring_exchange(sh, a.sync, G, ct, NC, a.status, a.nonce)) {
         if (ct == 0) GBN_RING_TRACE(4);
         T* outs[1] = {static_cast<T*>(a.dw)};
         colsum_warps<T, COMP>(a.part, 1, G, a.H, outs, g, G, cw, NCW, lane);

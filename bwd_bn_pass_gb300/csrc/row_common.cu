@@ -22,6 +22,7 @@ constexpr int kColGroups = 32;
 constexpr int kMaxStages = 8;
 constexpr int kRmsConsumers = 512;       // consumer threads of the RMSNorm ring kernel
 constexpr int kRowRingStatic = 4096;     // static shared memory of a ring kernel, at most
+constexpr int64_t kRingBytesPerSm = 128 << 10;  // ring bytes in flight per SM, about
 constexpr int kLnMaxGroups = 14;         // consumer groups (named barriers 2..15) of the LayerNorm ring kernel
 
 // Epoch pair, arrival counter and one flag pair per CTA, rounded to 256
@@ -113,6 +114,10 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
     const int64_t dyn = (int64_t)dev.smem_optin - kRowRingStatic;
     int64_t nst = dyn / (int64_t)stage;
     if (nst > kMaxStages) nst = kMaxStages;
+    // about 128 KB in flight per SM: deeper rings measured slower (RMSNorm
+    // bf16 [2048, 8192]: 26.3 us at 2-5 stages of 32 KB, 28.0 us at 6)
+    const int64_t cap = (kRingBytesPerSm + (int64_t)stage - 1) / (int64_t)stage;
+    if (nst > cap && cap >= 2) nst = cap;
     if (kv <= 4 && nst >= 2) {
       const int64_t nblk = (R + rb - 1) / rb;
       p->fast = true;

@@ -30,6 +30,7 @@ struct RowShared {
   uint64_t full[kRowMaxStages];   // stage landed (transaction count)
   uint64_t empty[kRowMaxStages];  // stage released by every consumer warp
   unsigned long long target;      // flag value of this launch
+  unsigned long long epoch[2];    // the workspace's epoch pair as the kernel found it
   int issued[kRowMaxStages];      // stages the producer has issued into each slot
   volatile int abort;             // a wait expired: stop issuing and computing
 };
@@ -177,6 +178,16 @@ __device__ void colsum_warps(const float* __restrict__ part, int nout, int G, in
   }
 }
 
+// Consumer thread 0 reads the epoch pair into shared memory as the kernel
+// starts: the value is needed only at the hand-off, and the first stage takes
+// longer to land than the load, so the load stays off the ring's start.
+__device__ __forceinline__ void epoch_read(RowShared& sh, const unsigned long long* sync, int t) {
+  if (t == 0) {
+    sh.epoch[0] = ld_relaxed_u64(sync);
+    sh.epoch[1] = ld_relaxed_u64(sync + 1);
+  }
+}
+
 // After this CTA's partials are written, the hand-off between CTAs: every
 // CTA arrives on the workspace's counter (a fence, then one atomic add) and
 // waits until all G have arrived; the last to arrive resets the counter for
@@ -187,17 +198,24 @@ __device__ void colsum_warps(const float* __restrict__ part, int nout, int G, in
 // counter.  CTA 0 advances the epoch once it has seen every arrival.
 // Consumer threads only; returns false (for every consumer) if a wait
 // expired.
+// sh.epoch holds the workspace's epoch pair (epoch_read at the kernel's
+// start); `nonce` is the host's value for a workspace without a valid pair.
 __device__ __forceinline__ bool ring_exchange(RowShared& sh, unsigned long long* sync, int G,
-                                              int t, int nthreads, int* status) {
+                                              int t, int nthreads, int* status,
+                                              unsigned long long nonce) {
   __shared__ int use_flags;
+  if (t == 0) sh.target = (sh.epoch[1] == ~sh.epoch[0] ? sh.epoch[0] : nonce) + 1ull;
   consumers_bar(nthreads);  // every consumer's partial stores precede the arrival
   unsigned long long* ctr = sync + kRingCounterWord;
   unsigned long long* flags = sync + kRingFlagWord;
   const unsigned int tag = (unsigned int)sh.target, next_tag = (unsigned int)(sh.target + 1ull);
   bool ok = true;
   if (t == 0) {
-    __threadfence();
-    const unsigned long long old = atomicAdd(ctr, 1ull);
+    // acq_rel: publishes this CTA's partials (every consumer's stores reach
+    // this thread through the barrier above) and, for the last arrival,
+    // acquires everyone else's
+    unsigned long long old;
+    asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
     const bool tagged = (unsigned int)(old >> 32) == tag;
     use_flags = !tagged;
     if (tagged) {
@@ -216,7 +234,6 @@ __device__ __forceinline__ bool ring_exchange(RowShared& sh, unsigned long long*
           }
         }
       }
-      __threadfence();
     } else {
       flag_publish(flags - 2, blockIdx.x, sh.target);  // flag pair k at word 4 + 2k
     }

@@ -58,6 +58,11 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 
+# Latency-bound BatchNorm shapes (the tiny [8,4,8,8] and the ragged
+# [3,37,41,40] workloads): microseconds per call, eager and from a CUDA-graph
+# replay, reported in `latency_ops` and kept out of `value`.
+LATENCY_OPS = ["bn_tiny_f32_fwd", "bn_tiny_f32_bwd", "bn_ragged_f32_fwd", "bn_ragged_f32_bwd"]
+
 OPS_ALL = ["bn_f32_fwd", "bn_f32_bwd", "rms_bf16_bwd", "rms_f32_bwd", "ln_bf16_bwd",
            "bn_bf16_fwd", "bn_bf16_bwd"]
 
@@ -190,8 +195,13 @@ def build_ops(names, dev):
     ops = []
     for name in names:
         if name.startswith("bn_"):
-            # bn[_relu][_nhwc]_{f32,bf16}_{fwd,bwd}
-            case = synth.CASES["bn_offset_f32" if "f32" in name else "bn_offset_bf16"]
+            # bn[_relu][_nhwc]_{f32,bf16}_{fwd,bwd}; bn_{tiny,ragged}_f32_{fwd,bwd}
+            if name.startswith("bn_tiny_"):
+                case = synth.CASES["bn_tiny_f32"]
+            elif name.startswith("bn_ragged_"):
+                case = synth.CASES["bn_ragged_f32"]
+            else:
+                case = synth.CASES["bn_offset_f32" if "f32" in name else "bn_offset_bf16"]
             act = "relu" if "_relu_" in name else None
             nhwc = "_nhwc_" in name
             inp = synth.bn_inputs(case)
@@ -200,11 +210,17 @@ def build_ops(names, dev):
                 inp["dy"] = inp["dy"].permute(0, 2, 3, 1).contiguous()
             hx, hdy = _pin(inp["x"]), _pin(inp["dy"])
             x, dy = hx.to(dev), hdy.to(dev)
-            g, b = inp["gamma"].to(dev), inp["beta"].to(dev)
-            rm, rv = inp["running_mean"].to(dev), inp["running_var"].to(dev)
             C = x.shape[-1] if nhwc else x.shape[1]
+            # per-channel vectors in one buffer [gamma | beta | running_mean |
+            # running_var | stats (8 C)], so that the end-to-end leg moves
+            # them with one copy each way
+            par = torch.empty(12 * C, dtype=torch.float32, device=dev)
+            g, b, rm, rv = (par[k * C:(k + 1) * C] for k in range(4))
+            stats = par[4 * C:]
+            for t, src in ((g, "gamma"), (b, "beta"), (rm, "running_mean"),
+                           (rv, "running_var")):
+                t.copy_(inp[src])
             y = torch.empty_like(x)
-            stats = G.bn_stats_tensor(C, dev)
             fwd_fn = G.bn_nhwc_forward_train if nhwc else G.bn_forward_train
             bwd_fn = G.bn_nhwc_backward if nhwc else G.bn_backward
             ws = G.bn_nhwc_workspace(x) if nhwc else G.bn_workspace(x)
@@ -220,6 +236,7 @@ def build_ops(names, dev):
             # threshold on, else stats + apply (grad sums + dx); NHWC: three.
             in_bytes = T * (1 if name.endswith("fwd") else 2)
             launches = 3 if nhwc else (1 if in_bytes >= G.bn_persistent_min_bytes() else 2)
+            pin = lambda t: torch.empty_like(t, device="cpu").pin_memory()  # noqa: E731
             if name.endswith("fwd"):
                 # the composite call a user makes: statistics, finalize and apply
                 phases = [
@@ -228,10 +245,13 @@ def build_ops(names, dev):
                      f=fwd_fn, a=act:
                      f(x, g, b, rm, rv, c.momentum, c.eps, y=y, stats=stats, ws=ws, act=a)),
                 ]
-                hy = torch.empty_like(hx).pin_memory()
+                # end to end: every input up (x; gamma, beta and the running
+                # stats in one copy), every output down (y; the updated
+                # running stats and stats in one copy)
+                h2d = [(hx, x), (_pin(par[:4 * C].cpu()), par[:4 * C])]
+                d2h = [(y, pin(y)), (par[2 * C:], pin(par[2 * C:]))]
                 ops.append(Op(name, f"{kind} fwd {case.dtype} [{shape}]", phases,
-                              2 * T + small, {key: 2 * T + small}, launches,
-                              [(hx, x)], [(y, hy)], None))
+                              2 * T + small, {key: 2 * T + small}, launches, h2d, d2h, None))
             else:
                 dx = torch.empty_like(x)
                 grads = torch.empty(4 * C, dtype=torch.float32, device=dev)
@@ -239,11 +259,15 @@ def build_ops(names, dev):
                     (key, lambda x=x, dy=dy, s=stats, dx=dx, gr=grads, ws=ws, b=b, f=bwd_fn,
                      a=act: f(x, dy, s, dx=dx, grads=gr, ws=ws, beta=b if a else None, act=a)),
                 ]
-                hdx = torch.empty_like(hx).pin_memory()
                 ub = 3 * T + 8 * C * 4 + 4 * C * 4
+                # end to end: x, dy and the saved stats up (beta too with an
+                # activation); dx and grads down
+                h2d = [(hx, x), (hdy, dy), (_pin(stats.cpu()), stats)]
+                if act:
+                    h2d.append((_pin(b.cpu()), b))
+                d2h = [(dx, pin(dx)), (grads, pin(grads))]
                 ops.append(Op(name, f"{kind} bwd {case.dtype} [{shape}]", phases,
-                              ub, {key: ub}, launches,
-                              [(hx, x), (hdy, dy)], [(dx, hdx)], None))
+                              ub, {key: ub}, launches, h2d, d2h, None))
         elif name in ("rms_bf16_fwd", "rms_f32_fwd"):
             case = synth.CASES["rms_bf16" if "bf16" in name else "rms_f32"]
             inp = synth.rms_inputs(case)
@@ -489,6 +513,8 @@ def run_ours(args, rank, world, local_rank):
         }
 
     graph = run_graph(ops, stream, dev, args.steps, world, flush_l2)
+    latency = None if args.ops else run_latency(build_ops(LATENCY_OPS, dev), stream, dev,
+                                                max(args.steps, 20), flush_l2)
 
     e2e = None
     if not args.no_e2e:
@@ -518,6 +544,7 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_region": round(wall, 4),
         "e2e": e2e,
         "graph_step": graph,
+        "latency_ops": latency,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -525,6 +552,53 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.destroy_process_group()
     return line
+
+
+def run_latency(ops, stream, dev, steps, flush_l2):
+    """Microseconds per call of latency-bound ops: each call timed alone with
+    CUDA events after an L2 flush, eagerly and as a replay of a CUDA graph
+    that holds just that call (the launch overhead a graph removes)."""
+    import torch
+    out = {}
+    for op in ops:
+        def call(op=op):
+            for _, fn in op.phases:
+                fn()
+
+        eager = []
+        for it in range(steps + 3):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            if it >= 3:
+                eager.append(e0.elapsed_time(e1) * 1e3)
+        graph = []
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                call()
+            for it in range(steps + 3):
+                flush_l2()
+                e0, e1 = (torch.cuda.Event(enable_timing=True),
+                          torch.cuda.Event(enable_timing=True))
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                if it >= 3:
+                    graph.append(e0.elapsed_time(e1) * 1e3)
+        except RuntimeError:
+            graph = []
+        out[op.name] = {
+            "desc": op.desc, "launches": op.launches,
+            "us_median": round(statistics.median(eager), 2), "us_min": round(min(eager), 2),
+            "us_graph_median": round(statistics.median(graph), 2) if graph else None,
+            "us_graph_min": round(min(graph), 2) if graph else None,
+        }
+    return out
 
 
 def run_graph(ops, stream, dev, steps, world, flush_l2):

@@ -43,6 +43,13 @@
 #include "gbn_common.cuh"
 #include "gbn_internal.h"
 
+// Optional per-CTA timestamps for studying the kernel's phases: a build that
+// defines GBN_RING_TRACE(point) records them; the library's own build
+// compiles the hook away.
+#ifndef GBN_RING_TRACE
+#define GBN_RING_TRACE(point) ((void)0)
+#endif
+
 namespace gbn {
 
 namespace {
@@ -82,6 +89,7 @@ struct FArgs {
   int32_t G;
   int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
   int32_t l2_window; // phase-1 stages before the resident tail kept at normal L2 priority
+  int32_t stream_out; // outputs with the evict-first hint (tensors larger than L2 holds)
   float Mh, Ml;      // per-channel count M = Mh + Ml exactly
 };
 
@@ -372,6 +380,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
     for (int q = 0; q < nq; ++q, ++i) {
       const int slot = i % NS;
       if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
+      if (i == 0 && ct == 0) GBN_RING_TRACE(1);
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
@@ -418,6 +427,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
     __threadfence();
     st_relaxed_u64(f + 1, ~sh.target);
     st_release_u64(f, sh.target);
+    GBN_RING_TRACE(2);
   }
   __syncwarp();
 }
@@ -490,6 +500,7 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
     if (!__any_sync(0xffffffffu, sh.abort != 0)) finalize_segment<BWD>(a, sh, s);
   __syncwarp();
   consumers_sync();
+  if (ct == 0) GBN_RING_TRACE(3);
   T* out = static_cast<T*>(a.out);
   int q2 = 0;
   for (int s = sh.nseg - 1; s >= 0; --s) {
@@ -532,7 +543,10 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
             e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
           }
         }
-        store16_cs(out + gvo * VEC, e);
+        if (a.stream_out)
+          store16_cs(out + gvo * VEC, e);
+        else
+          V::store(out + gvo * VEC, e);
         pv += a.dp;
         n += a.dn;
         if (pv >= a.Pv) {
@@ -561,8 +575,6 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
       sh.issued[s] = 0;
     }
     sh.abort = 0;
-    const unsigned long long ea = ld_relaxed_u64(a.sync), eb = ld_relaxed_u64(a.sync + 1);
-    sh.target = (eb == ~ea ? ea : a.nonce) + 1ull;
     // Segments of this CTA's range [k*Wv, (k+1)*Wv) of the channel-major view.
     const int64_t e0 = (int64_t)blockIdx.x * a.Wv;
     const int64_t e1 = min(e0 + a.Wv, a.C * (int64_t)a.Mv);
@@ -582,6 +594,7 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
     sh.nseg = ns;
     sh.nst = nst;
     fence_mbarrier_init();
+    GBN_RING_TRACE(0);
   }
   __syncthreads();
 
@@ -589,7 +602,12 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
     producer<T, BWD>(a, sh, ring);
     __syncwarp();
   } else {
-    // Per-segment parameters (global loads, off the producer's start path).
+    // The launch's flag value and the per-segment parameters: global loads,
+    // off the producer's start path (the first stage takes longer to land).
+    if (tid == 32) {
+      const unsigned long long ea = ld_relaxed_u64(a.sync), eb = ld_relaxed_u64(a.sync + 1);
+      sh.target = (eb == ~ea ? ea : a.nonce) + 1ull;
+    }
     if (tid - 32 < sh.nseg) {
       const int s = tid - 32;
       const int64_t c = sh.seg_c[s];
@@ -612,6 +630,7 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
       consumer_phase2<T, BWD, GBN_ACT_LEAKY_RELU>(a, sh, ring, fpar);
     else
       consumer_phase2<T, BWD, GBN_ACT_NONE>(a, sh, ring, fpar);
+    if (tid == 32) GBN_RING_TRACE(4);
   }
   __syncthreads();
 
@@ -672,6 +691,7 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
   a.dn = (int32_t)(kFConsumers / p.Pv);
   a.dp = (int32_t)(kFConsumers % p.Pv);
   a.l2_window = p.l2_window;
+  a.stream_out = p.stream_out ? 1 : 0;
   a.Mh = (float)p.M;
   a.Ml = (float)(p.M - (int64_t)a.Mh);
   return a;
@@ -739,6 +759,11 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
   // three quarters of L2, shared by the G CTAs.
   const int64_t stage_bytes = (int64_t)ninputs * stage_v * 16;
   p->l2_window = (int)((int64_t)dev.l2_bytes * 3 / 4 / ((int64_t)p->G * stage_bytes));
+  // Outputs stream past L2 (evict-first) only when the call's tensors do not
+  // fit in half of it: then they would push out the inputs that phase 2
+  // re-reads; smaller outputs are left to L2, which absorbs the writes.
+  const int64_t call_bytes = (int64_t)(ninputs + 1) * C * p->M * esize;
+  p->stream_out = call_bytes > (int64_t)dev.l2_bytes / 2;
   p->part_offset = ((size_t)16 + (size_t)16 * p->G + 255) & ~(size_t)255;
   p->ws_bytes = p->part_offset + (size_t)2 * p->grid_y * C * sizeof(float2);
   p->ws_bytes = (p->ws_bytes + 255) & ~(size_t)255;

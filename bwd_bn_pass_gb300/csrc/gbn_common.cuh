@@ -511,11 +511,13 @@ __device__ __forceinline__ float2 ld_relaxed_f2(const float2* p) {
 __device__ __forceinline__ bool flag_ready(const unsigned long long* f, unsigned long long t) {
   return ld_acquire_u64(f) == t && ld_relaxed_u64(f + 1) == ~t;
 }
+// Polls back to back for the first few hundred tries (a flag is usually
+// published within microseconds), then with short sleeps.
 __device__ __forceinline__ bool wait_flag(const unsigned long long* f, unsigned long long t) {
   if (flag_ready(f, t)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    __nanosleep(100);
+    if (it > 256) __nanosleep(64);
     if (flag_ready(f, t)) return true;
     if ((it & 15u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
   }

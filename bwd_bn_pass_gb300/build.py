@@ -21,8 +21,8 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libgbnorm.so"
 
 SOURCES = ["abi.cu", "bn_kernels.cu", "rms_kernels.cu", "ln_kernels.cu",
-           "row_common.cu", "noalloc.cu", "bn_fused.cu", "fwd_kernels.cu", "bn_nhwc.cu",
-           "selftest.cu"]
+           "row_common.cu", "noalloc.cu", "bn_fused.cu", "bn_small.cu", "fwd_kernels.cu",
+           "bn_nhwc.cu", "selftest.cu"]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -178,6 +178,11 @@ static bool bn_empty(int64_t B, int64_t C, int64_t HW) { return C == 0 || B == 0
 // ~200 MB).
 static std::atomic<int64_t> g_fused_min_bytes{128ll << 20};
 
+// Channels of at most this many elements (M = B*HW) run the single-launch
+// small-channel kernels in the composite calls (below the persistent
+// kernel's threshold); 0 disables them.
+static std::atomic<int64_t> g_small_max_m{kBnSmallMaxM};
+
 // act one of GBN_ACT_*; LeakyReLU's slope finite.
 static bool act_ok(int act, float slope) {
   if (act == GBN_ACT_NONE || act == GBN_ACT_RELU) return true;
@@ -229,6 +234,9 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
     return to_status(bn_fused_forward(fp, dtype, x, y, gamma, beta, stats, running_mean,
                                       running_var, momentum, eps, act, slope,
                                       const_cast<void*>(ws), dev->status, st));
+  if (with_stats_pass && M <= g_small_max_m.load())
+    return to_status(bn_small_forward(dtype, x, y, B, C, HW, gamma, beta, stats, running_mean,
+                                      running_var, momentum, eps, act, slope, st));
   if (with_stats_pass) {
     cudaError_t e = bn_launch_stats(x, dtype, p, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;
@@ -279,6 +287,12 @@ int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes) {
 }
 
 int64_t gbn_bn_persistent_min_bytes(void) { return g_fused_min_bytes.load(); }
+
+int64_t gbn_bn_set_small_max_elems(int64_t m) {
+  if (m < 0) m = 0;
+  if (m > kBnSmallMaxM) m = kBnSmallMaxM;
+  return g_small_max_m.exchange(m);
+}
 
 int gbn_bn_set_wide_offsets(int force) { return bn_set_wide_offsets(force); }
 
@@ -369,6 +383,9 @@ static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B,
       ws_bytes >= fp.ws_bytes)
     return to_status(bn_fused_backward(fp, dtype, x, dy, dx, stats, beta, act, slope, grads,
                                        const_cast<void*>(ws), dev->status, st));
+  if (sums && finalize && M <= g_small_max_m.load())
+    return to_status(bn_small_backward(dtype, x, dy, dx, B, C, HW, stats, beta, act, slope,
+                                       grads, st));
   if (sums) {
     cudaError_t e = bn_launch_grad_sums(x, dy, dtype, p, stats, part, beta, act, slope, st);
     if (e != cudaSuccess) return GBN_ECUDA;

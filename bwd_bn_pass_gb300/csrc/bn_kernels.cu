@@ -14,7 +14,8 @@
 //     finalize to grads (dgamma, dbeta, k1, k2), dx = dy*scale + (x-mean)*k1
 //     + k2.
 //
-// GB300 design (differs from the page's three launches per direction):
+// GB300 design (differs from the three launches per direction of Aether-ML
+// PR #18, "Reduction grid" and "Backward finalize"):
 //   * Two launches per direction.  The finalize is the prologue of the
 //     consuming kernel: every block of channel c reduces that channel's
 //     partials in the same fixed order (so all blocks hold bit-identical
@@ -611,8 +612,8 @@ bool bn_plan(int64_t B, int64_t C, int64_t HW, const DevInfo& dev, BnPlan* plan)
   plan->C = C;
   plan->P = HW;
   plan->M = B * HW;
-  // Fill every resident block slot once ("Reduction grid": the page counts
-  // mp_count * max_threads_per_mp / 256 slots; these kernels hold 64
+  // Fill every resident block slot once (Aether-ML PR #18, "Reduction grid",
+  // counts mp_count * max_threads_per_mp / 256 slots; these kernels hold 64
   // registers per thread, so kBnBlocksPerSm 256-thread blocks are resident
   // per SM), but give each block at least kBnMinElemsPerBlock elements.
   const int64_t slots = (int64_t)dev.sms * kBnBlocksPerSm;

@@ -1,0 +1,195 @@
+// Single-launch BatchNorm2d training forward and backward (NCHW) for small
+// channels: the latency-bound shapes (a few thousand elements per channel)
+// that the two-launch kernels would spend two launches on.
+//
+// Method: Aether-ML PR #18 "perf(batchnorm): device-sized grid, one-pass
+// statistics, finalize kernels" -- per channel the shifted one-pass sums
+// (d = x - x[0,c]), the forward finalize (mean, biased variance, inv_std,
+// scale, running statistics) and the centred apply; backward the sums of dy
+// and dy*(x - shift), the backward finalize (dgamma, dbeta, k1, k2) and
+// dx = dy*scale + (x - mean)*k1 + k2.  The arithmetic is that of the other
+// BatchNorm kernels (the same finalize helpers, exact per-element sums).
+//
+// GB300 design: one 256-thread block per channel stages the whole channel
+// (at most 2048 elements, 8 KB of fp32; 16 KB backward) in shared memory as
+// it reads it once -- every load of a thread in flight at once, so a channel
+// costs one memory round trip -- reduces in a fixed tree, finalizes, and
+// writes the outputs from shared memory.  One launch, no workspace, no
+// second read from global memory.  (Larger channels take the two-launch
+// kernels, which spread a channel over several blocks: at 4920 elements per
+// channel one block per channel measured slower.)
+#include "bn_finalize.cuh"
+#include "gbn_common.cuh"
+#include "gbn_internal.h"
+
+namespace gbn {
+
+namespace {
+
+constexpr int kSmallThreads = 256;
+
+// x - shift and, for fp32 input, the rounding error of the subtraction
+// (TwoSum); bf16 differences are exact unless the magnitudes differ by more
+// than 2^16 (then one fp32 rounding per term).
+template <typename T>
+__device__ __forceinline__ void shifted(float e, float shift, float& d, float& d_lo) {
+  d = __fsub_rn(e, shift);
+  if constexpr (sizeof(T) == 4) {
+    const float bb = __fsub_rn(d, e);
+    d_lo = __fadd_rn(__fsub_rn(e, __fsub_rn(d, bb)), __fsub_rn(-shift, bb));
+  } else {
+    d_lo = 0.f;
+  }
+}
+
+// Loads per thread issued together: a whole channel (kBnSmallMaxM / 256).
+constexpr int kSmallBatch = (int)(kBnSmallMaxM / kSmallThreads);
+
+__device__ __forceinline__ int64_t elem_offset(int m, int C, int c, int P) {
+  const int n = m / P;
+  return ((int64_t)n * C + c) * P + (m - n * P);
+}
+
+// Dynamic shared memory: the channel's M values in (b, h, w) order, fp32
+// (forward: x; backward: x, then the gated dy).
+template <typename T>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    bn_small_fwd_kernel(const T* __restrict__ x, T* __restrict__ y, int B, int C, int P,
+                        const float* __restrict__ gamma, const float* __restrict__ beta,
+                        float* __restrict__ stats, float* running_mean, float* running_var,
+                        float momentum, float eps, float Mh, float Ml, int act, float slope) {
+  extern __shared__ float vals[];
+  __shared__ float2 red[64];
+  const int c = blockIdx.x, t = threadIdx.x, M = B * P;
+  const float shift = to_f32(x[(int64_t)c * P]);  // x[0, c, 0, 0]
+  DF s1{0.f, 0.f}, s2{0.f, 0.f};
+  for (int m0 = t; m0 < M; m0 += kSmallBatch * kSmallThreads) {
+    float v[kSmallBatch];
+#pragma unroll
+    for (int u = 0; u < kSmallBatch; ++u) {
+      const int m = m0 + u * kSmallThreads;
+      v[u] = m < M ? to_f32(x[elem_offset(m, C, c, P)]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kSmallBatch; ++u) {
+      const int m = m0 + u * kSmallThreads;
+      if (m < M) {
+        vals[m] = v[u];
+        float d, d_lo;
+        shifted<T>(v[u], shift, d, d_lo);
+        df_add(s1, d);
+        if constexpr (sizeof(T) == 4) s1.lo = __fadd_rn(s1.lo, d_lo);
+        df_add(s2, d * d);
+      }
+    }
+  }
+  block_sum2_df(s1, s2, red);  // contains __syncthreads: vals is complete
+  const BnFwdFinal f = bn_fwd_final(s1, s2, Mh, Ml, gamma ? gamma[c] : 1.f, eps);
+  if (t == 0)
+    bn_fwd_write(f, shift, C, c, Mh + Ml, stats, running_mean, running_var, momentum);
+  const float b = beta ? beta[c] : 0.f, mean_d = f.md.hi, scale = f.scale;
+  for (int m = t; m < M; m += kSmallThreads)
+    y[elem_offset(m, C, c, P)] =
+        from_f32<T>(act_out(fmaf((vals[m] - shift) - mean_d, scale, b), act, slope));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    bn_small_bwd_kernel(const T* __restrict__ x, const T* __restrict__ dy, T* __restrict__ dx,
+                        int B, int C, int P, const float* __restrict__ stats,
+                        const float* __restrict__ beta, float* __restrict__ grads, float Mf,
+                        int act, float slope) {
+  extern __shared__ float vals[];  // [2][M]: x, then the gated dy
+  __shared__ float2 red[64];
+  const int c = blockIdx.x, t = threadIdx.x, M = B * P;
+  const float inv_std = stats[2 * C + c], scale = stats[3 * C + c];
+  const float shift = stats[4 * C + c], mean_d = stats[5 * C + c];
+  const DF md{stats[6 * C + c], stats[7 * C + c]};
+  const float bta = beta ? beta[c] : 0.f;
+  DF p0{0.f, 0.f}, p1{0.f, 0.f};
+  for (int m0 = t; m0 < M; m0 += kSmallBatch * kSmallThreads) {
+    float xv[kSmallBatch], gv[kSmallBatch];
+#pragma unroll
+    for (int u = 0; u < kSmallBatch; ++u) {
+      const int m = m0 + u * kSmallThreads;
+      const int64_t o = m < M ? elem_offset(m, C, c, P) : 0;
+      xv[u] = m < M ? to_f32(x[o]) : 0.f;
+      gv[u] = m < M ? to_f32(dy[o]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kSmallBatch; ++u) {
+      const int m = m0 + u * kSmallThreads;
+      if (m < M) {
+        float g = gv[u];
+        // with an activation, dy gated by d act / d pre (pre as in the forward)
+        if (act != GBN_ACT_NONE)
+          g = __fmul_rn(g, act_gate(fmaf((xv[u] - shift) - mean_d, scale, bta), act, slope));
+        vals[m] = xv[u];
+        vals[M + m] = g;
+        float d, d_lo;
+        shifted<T>(xv[u], shift, d, d_lo);
+        df_add(p0, g);
+        df_add_prod(p1, g, d);
+        if constexpr (sizeof(T) == 4) p1.lo = fmaf(g, d_lo, p1.lo);
+      }
+    }
+  }
+  block_sum2_df(p0, p1, red);  // contains __syncthreads: vals is complete
+  const BnBwdFinal f = bn_bwd_final(p0, p1, md, inv_std, scale, Mf);
+  if (t == 0) {
+    grads[c] = f.dgamma;
+    grads[C + c] = f.dbeta;
+    grads[2 * C + c] = f.k1;
+    grads[3 * C + c] = f.k2;
+  }
+  for (int m = t; m < M; m += kSmallThreads) {
+    const float xc = (vals[m] - shift) - mean_d;
+    dx[elem_offset(m, C, c, P)] = from_f32<T>(fmaf(vals[M + m], scale, fmaf(xc, f.k1, f.k2)));
+  }
+}
+
+template <typename T>
+cudaError_t small_fwd(const void* x, void* y, int64_t B, int64_t C, int64_t HW, const float* gamma,
+                      const float* beta, float* stats, float* running_mean, float* running_var,
+                      float momentum, float eps, int act, float slope, cudaStream_t st) {
+  const int64_t M = B * HW;
+  const float Mh = (float)M, Ml = (float)(M - (int64_t)Mh);
+  return launch(bn_small_fwd_kernel<T>, dim3((unsigned)C), dim3(kSmallThreads),
+                (size_t)M * sizeof(float), st, false, static_cast<const T*>(x),
+                static_cast<T*>(y), (int)B, (int)C, (int)HW, gamma, beta, stats, running_mean,
+                running_var, momentum, eps, Mh, Ml, act, slope);
+}
+
+template <typename T>
+cudaError_t small_bwd(const void* x, const void* dy, void* dx, int64_t B, int64_t C, int64_t HW,
+                      const float* stats, const float* beta, int act, float slope, float* grads,
+                      cudaStream_t st) {
+  const int64_t M = B * HW;
+  return launch(bn_small_bwd_kernel<T>, dim3((unsigned)C), dim3(kSmallThreads),
+                2 * (size_t)M * sizeof(float), st, false, static_cast<const T*>(x),
+                static_cast<const T*>(dy), static_cast<T*>(dx), (int)B, (int)C, (int)HW, stats,
+                beta, grads, (float)M, act, slope);
+}
+
+}  // namespace
+
+cudaError_t bn_small_forward(int dtype, const void* x, void* y, int64_t B, int64_t C,
+                             int64_t HW, const float* gamma, const float* beta, float* stats,
+                             float* running_mean, float* running_var, float momentum, float eps,
+                             int act, float slope, cudaStream_t st) {
+  if (dtype == GBN_F32)
+    return small_fwd<float>(x, y, B, C, HW, gamma, beta, stats, running_mean, running_var,
+                            momentum, eps, act, slope, st);
+  return small_fwd<bf16>(x, y, B, C, HW, gamma, beta, stats, running_mean, running_var, momentum,
+                         eps, act, slope, st);
+}
+
+cudaError_t bn_small_backward(int dtype, const void* x, const void* dy, void* dx, int64_t B,
+                              int64_t C, int64_t HW, const float* stats, const float* beta,
+                              int act, float slope, float* grads, cudaStream_t st) {
+  if (dtype == GBN_F32)
+    return small_bwd<float>(x, dy, dx, B, C, HW, stats, beta, act, slope, grads, st);
+  return small_bwd<bf16>(x, dy, dx, B, C, HW, stats, beta, act, slope, grads, st);
+}
+
+}  // namespace gbn

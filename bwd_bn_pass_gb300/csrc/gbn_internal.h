@@ -88,6 +88,17 @@ cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, con
                          const float* stats, const float2* part, float* grads, const float* beta,
                          int act, float slope, cudaStream_t st, bool pdl);
 
+// Single-launch BatchNorm for small channels (bn_small.cu): one block per
+// channel holds the channel's M <= kBnSmallMaxM elements in registers.
+constexpr int64_t kBnSmallMaxM = 2048;
+cudaError_t bn_small_forward(int dtype, const void* x, void* y, int64_t B, int64_t C,
+                             int64_t HW, const float* gamma, const float* beta, float* stats,
+                             float* running_mean, float* running_var, float momentum, float eps,
+                             int act, float slope, cudaStream_t st);
+cudaError_t bn_small_backward(int dtype, const void* x, const void* dy, void* dx, int64_t B,
+                              int64_t C, int64_t HW, const float* stats, const float* beta,
+                              int act, float slope, float* grads, cudaStream_t st);
+
 // Persistent single-launch BatchNorm (bn_fused.cu): one CTA per SM owns a
 // contiguous range of the channel-major view; see that file.
 constexpr int64_t kBnFusedMinVectors = 2048;  // 16-byte vectors per CTA, at least

@@ -61,6 +61,7 @@ _SIGNATURES = {
     "gbn_selftest_bounded_wait": (_INT, [_I64, _P]),
     "gbn_bn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "gbn_bn_set_persistent_min_bytes": (_I64, [_I64]),
+    "gbn_bn_set_small_max_elems": (_I64, [_I64]),
     "gbn_bn_persistent_min_bytes": (_I64, []),
     "gbn_bn_set_wide_offsets": (_INT, [_INT]),
     "gbn_bn_forward_train": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
@@ -207,6 +208,13 @@ def bn_set_persistent_min_bytes(nbytes):
     single-launch persistent kernel (process-wide); returns the previous
     value."""
     return lib().gbn_bn_set_persistent_min_bytes(int(nbytes))
+
+
+def bn_set_small_max_elems(m):
+    """Per-channel element count up to which the composite BatchNorm calls
+    run the single-launch small-channel kernels (default and maximum 2048;
+    0 disables them).  Returns the previous value."""
+    return lib().gbn_bn_set_small_max_elems(int(m))
 
 
 def bn_persistent_min_bytes():

@@ -166,6 +166,16 @@ GBN_API int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes);
 /* The current threshold (bytes).                                           */
 GBN_API int64_t gbn_bn_persistent_min_bytes(void);
 
+/* Below the persistent kernel's threshold, the composite calls run channels
+ * of at most this many elements (M = B*HW per channel) in ONE launch: a
+ * block per channel stages the channel in shared memory as it reads it
+ * once, reduces, finalizes and writes the outputs ([P4]'s stats / finalize
+ * / apply, or grad_sums / finalize / dx, fused for latency-bound shapes).  Default and maximum
+ * 2048; 0 sends every shape to the two-launch kernels.  Results are within
+ * the parity tolerance of the other paths.  Process-wide; returns the
+ * previous value.  The pages have no counterpart: a tuning knob.           */
+GBN_API int64_t gbn_bn_set_small_max_elems(int64_t m);
+
 /* The two-launch BatchNorm kernels (NCHW) address vectors with 32-bit
  * offsets while the tensor holds fewer than 2^32 16-byte-or-smaller vectors,
  * and with 64-bit offsets beyond.  A nonzero `force` makes every later call

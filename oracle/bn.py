@@ -22,13 +22,13 @@ writes the definitions out (two-pass variance, float64, no shift).
 Readings where the pages are silent
 -----------------------------------
 * ``N`` in k1/k2 is the per-channel element count ``M = B * H * W``.
-* The batch variance is biased (divides by M), as in the page's test that
-  compares it with "the float64 variance of the same data".
+* The batch variance is biased (divides by M), as in the test of Aether-ML
+  PR #18 ("Testing") that compares it with "the float64 variance of the same data".
 * running_var takes the unbiased ``var * M / (M - 1)``; momentum follows
   ``new = (1 - m) * old + m * batch`` (the PyTorch BatchNorm2d convention).
-* Fusing ReLU / LeakyReLU into BatchNorm is the page's "Part 2" (section
-  "Context"; "Follow-ups": ReLU costs more per step than the BatchNorm
-  forward).  The page gives no definition beyond the names, so the reading
+* Fusing ReLU / LeakyReLU into BatchNorm is "Part 2" of Aether-ML PR #18
+  (section "Context"; "Follow-ups": ReLU costs more per step than the BatchNorm
+  forward).  That page gives no definition beyond the names, so the reading
   here is the composition: y = act(pre) with pre the BatchNorm output, and
   the backward gates dy by d act / d pre -- 1 where pre > 0, else 0 (ReLU)
   or the negative slope (LeakyReLU) -- before the BatchNorm backward.

@@ -175,6 +175,14 @@ def test_bn_nhwc_argument_errors(gbn):
     assert L.gbn_bn_nhwc_apply(A16, 0, 0, 4, NULL, NULL, NULL, NULL, 0, 0.0, A16, NULL) == OK
 
 
+def test_bn_small_channel_switch(gbn):
+    L = gbn.lib()
+    prev = L.gbn_bn_set_small_max_elems(100)
+    assert L.gbn_bn_set_small_max_elems(-5) == 100
+    assert L.gbn_bn_set_small_max_elems(1 << 40) == 0      # negative stored as 0
+    assert L.gbn_bn_set_small_max_elems(prev) == 2048      # capped at the kernels' limit
+
+
 def test_bn_persistent_threshold(gbn):
     L = gbn.lib()
     prev = L.gbn_bn_set_persistent_min_bytes(12345)

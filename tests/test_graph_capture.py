@@ -49,10 +49,11 @@ def _replay_matches(run, outs, reps=3):
             assert torch.equal(t, r)
 
 
-@pytest.mark.parametrize("path", ["two-launch", "persistent"])
+@pytest.mark.parametrize("path", ["two-launch", "small-channel", "persistent"])
 def test_batchnorm_in_a_graph(gbn, path):
     gbn.init(0)
-    prev = gbn.bn_set_persistent_min_bytes(1 << 62 if path == "two-launch" else 0)
+    prev = gbn.bn_set_persistent_min_bytes(0 if path == "persistent" else 1 << 62)
+    prev_small = gbn.bn_set_small_max_elems(0 if path == "two-launch" else 2048)
     try:
         inp = synth.bn_inputs(synth.BNCase("graph_bn", (16, 24, 14, 14), "bf16",
                                            mu_range=(-5.0, 5.0), seed=1101))
@@ -72,6 +73,7 @@ def test_batchnorm_in_a_graph(gbn, path):
         _replay_matches(run, [y, stats, dx, grads])
     finally:
         gbn.bn_set_persistent_min_bytes(prev)
+        gbn.bn_set_small_max_elems(prev_small)
 
 
 def test_rows_and_channels_last_in_a_graph(gbn):

@@ -58,11 +58,12 @@ class Guarded:
             assert torch.all(raw[BAND + nbytes:] == PATTERN), "band after an output was written"
 
 
-@pytest.mark.parametrize("path", ["two-launch", "persistent"])
+@pytest.mark.parametrize("path", ["two-launch", "small-channel", "persistent"])
 @pytest.mark.parametrize("dtype,shape", [("f32", (3, 37, 41, 40)), ("bf16", (5, 19, 7, 9)),
                                          ("bf16", (2, 300, 8, 8)), ("f32", (4, 3, 5, 5))])
 def test_batchnorm_writes_stay_inside(gbn, dtype, shape, path):
-    prev = gbn.bn_set_persistent_min_bytes(1 << 62 if path == "two-launch" else 0)
+    prev = gbn.bn_set_persistent_min_bytes(0 if path == "persistent" else 1 << 62)
+    prev_small = gbn.bn_set_small_max_elems(0 if path == "two-launch" else 2048)
     try:
         inp = synth.bn_inputs(synth.BNCase("guard_bn", shape, dtype, seed=1201))
         x, dy = inp["x"].to(DEV), inp["dy"].to(DEV)
@@ -80,6 +81,7 @@ def test_batchnorm_writes_stay_inside(gbn, dtype, shape, path):
         G.check()
     finally:
         gbn.bn_set_persistent_min_bytes(prev)
+        gbn.bn_set_small_max_elems(prev_small)
 
 
 @pytest.mark.parametrize("dtype,shape", [("f32", (3, 37, 5, 3)), ("bf16", (4, 24, 3, 7)),

@@ -59,7 +59,7 @@ def _shifted_f32_var(x):
 
 
 @pytest.mark.parametrize("mu,sigma,shape", [
-    (1e4, 0.01, (16, 3, 256)),          # the page's mean 1e4, std 0.01 case
+    (1e4, 0.01, (16, 3, 256)),          # Aether-ML PR #18 "Testing": mean 1e4, std 0.01
     (None, 1.0, (64, 8, 1024)),         # the large-offset BN workload's law
 ])
 def test_negative_control_naive_variance(mu, sigma, shape):

@@ -17,15 +17,25 @@ from . import tolerances as tol
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=["auto", "persistent"])
+@pytest.fixture(autouse=True, params=["auto", "persistent", "two_launch"])
 def _bn_path(request, gbn):
-    """Every test runs twice: with the library's default size threshold for
-    the single-launch persistent kernel, and with the threshold at 0 so that
-    the persistent kernel takes every eligible shape, small ones included."""
+    """Every test runs three times: with the library's defaults (the
+    single-launch small-channel kernels for channels of at most 2048
+    elements, the two-launch kernels, the persistent kernel from 128 MiB of
+    input); with the persistent kernel's threshold at 0, so that it takes
+    every eligible shape, small ones included; and with the small-channel
+    kernels off and the threshold out of reach, so that the two-launch
+    kernels take every shape."""
     if request.param == "persistent":
         prev = gbn.bn_set_persistent_min_bytes(0)
         yield
         gbn.bn_set_persistent_min_bytes(prev)
+    elif request.param == "two_launch":
+        prev = gbn.bn_set_persistent_min_bytes(1 << 62)
+        prev_small = gbn.bn_set_small_max_elems(0)
+        yield
+        gbn.bn_set_persistent_min_bytes(prev)
+        gbn.bn_set_small_max_elems(prev_small)
     else:
         yield
 

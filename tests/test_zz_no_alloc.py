@@ -10,8 +10,8 @@ each result three ways:
   * against the float64 oracle at the parity tolerances of the other tests;
   * bit for bit against the ordinary `gbn_bn_forward_train` (which takes a
     workspace) run on the same kernel path -- the entry point runs the same
-    deterministic kernels, either the two-launch pair or, when its scratch
-    fits, the single-launch persistent kernel;
+    deterministic kernels: the small-channel single launch, the two-launch
+    pair or, when its scratch fits, the single-launch persistent kernel;
   * bit for bit between its own two calls.
 It also checks the size limit (more channels than the fixed array can hold
 is GBN_EWORKSPACE, rejected before any launch) and that the device status
@@ -81,16 +81,21 @@ def _call(gbn, inp, case, noalloc):
 
 
 def _workspace_forms(gbn, inp, case):
-    """gbn_bn_forward_train on both kernel paths: the two-launch pair, and
-    the persistent kernel wherever the shape is eligible."""
+    """gbn_bn_forward_train on each kernel path it can take: the
+    small-channel single launch, the two-launch pair, and the persistent
+    kernel wherever the shape is eligible."""
     prev = gbn.bn_set_persistent_min_bytes(HUGE)
+    prev_small = gbn.bn_set_small_max_elems(0)
     try:
-        two = _call(gbn, inp, case, noalloc=False)
+        forms = [_call(gbn, inp, case, noalloc=False)]       # two launches
+        gbn.bn_set_small_max_elems(prev_small)
+        forms.append(_call(gbn, inp, case, noalloc=False))  # small channels: one launch
         gbn.bn_set_persistent_min_bytes(0)
-        pers = _call(gbn, inp, case, noalloc=False)
+        forms.append(_call(gbn, inp, case, noalloc=False))  # persistent
     finally:
         gbn.bn_set_persistent_min_bytes(prev)
-    return two, pers
+        gbn.bn_set_small_max_elems(prev_small)
+    return forms
 
 
 def _bit_equal(a, b):
@@ -133,14 +138,14 @@ def test_noalloc_forward_two_calls_in_a_row(gbn, case):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     inp = synth.bn_inputs(case)
-    two, pers = _workspace_forms(gbn, inp, case)
+    forms = _workspace_forms(gbn, inp, case)
     gbn.get_device_status(clear=True)
     first = _call(gbn, inp, case, noalloc=True)
     second = _call(gbn, inp, case, noalloc=True)   # the same inputs, right after
     assert _bit_equal(first, second), f"{case.name}: two calls differ"
     for got in (first, second):
-        assert _bit_equal(got, two) or _bit_equal(got, pers), (
-            f"{case.name}: matches neither kernel path of the workspace forward bit for bit")
+        assert any(_bit_equal(got, f) for f in forms), (
+            f"{case.name}: matches no kernel path of the workspace forward bit for bit")
         _check_oracle(got, inp, case)
     assert gbn.get_device_status() == 0, "device status word reports an error"
 

@@ -29,6 +29,13 @@
 //     the range BACKWARD: the last ring-full of stages is still in shared
 //     memory (no reload), and the stages before it were read last, so they
 //     are the likeliest to be in L2.  Outputs are written with 16-byte stores.
+//   * Tensor memory (TMEM, 256 KB per SM, otherwise idle in this kernel) is a
+//     second on-chip tier: in phase 1 each consumer thread also copies its
+//     vectors of the nt stages just before the resident tail into its own
+//     TMEM columns (tcgen05.st), and phase 2 reads them back (tcgen05.ld)
+//     instead of loading those stages again; the L2 window moves back by nt
+//     stages.  The CTA holds all 512 columns for the whole launch (one CTA
+//     per SM) and frees them before it exits, also after a failed wait.
 //   * Flags carry an epoch: (e+1, ~(e+1)) per CTA, with e read at kernel
 //     start from the workspace's epoch pair (or a host nonce if that pair is
 //     not self-consistent); CTA 0 advances the epoch once every CTA has
@@ -88,7 +95,8 @@ struct FArgs {
   int32_t grid_y;
   int32_t G;
   int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
-  int32_t l2_window; // phase-1 stages before the resident tail kept at normal L2 priority
+  int32_t l2_window; // phase-1 stages before the TMEM stages kept at normal L2 priority
+  int32_t nt;        // stages kept in TMEM between the phases (0: none)
   int32_t stream_out; // outputs with the evict-first hint (tensors larger than L2 holds)
   float Mh, Ml;      // per-channel count M = Mh + Ml exactly
 };
@@ -102,6 +110,8 @@ struct FShared {
   unsigned long long target;  // flag value of this launch (epoch + 1)
   int nseg;
   int nst;                    // stages in the range
+  int t_lo, t_hi;             // stages [t_lo, t_hi) are kept in TMEM; stages < t_lo reload
+  uint32_t tmem;              // TMEM base address (written by tcgen05.alloc)
   volatile int abort;
   int seg_c[kFMaxSegs];
   int seg_rv0[kFMaxSegs];     // first vector of the segment inside its channel
@@ -160,6 +170,68 @@ __device__ __forceinline__ void store16_cs(float* p, const float (&e)[4]) {
 __device__ __forceinline__ void store16_cs(bf16* p, const float (&e)[8]) {
   __stcs(reinterpret_cast<uint4*>(p), make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
                                                 pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7])));
+}
+
+// ------------------------------------------------------------- TMEM tier --
+// Thread t of warp w reaches TMEM lanes 32*(w % 4) .. 32*(w % 4) + 31 (its
+// own lane is 32*(w % 4) + t); the 16 consumer warps share each lane quarter
+// four ways, 128 of the 512 columns each.  Address: lane << 16 | column.
+
+constexpr uint32_t kTmemCols = 512;
+constexpr int kTmemColsPerThread = kTmemCols / (kFConsumerWarps / 4);  // 128
+
+__device__ __forceinline__ void tmem_alloc_all(uint32_t* dst) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "n"(kTmemCols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free_all(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+               "n"(kTmemCols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 bytes of this thread into columns [col, col + 4) of its lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, uint4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// Loads and the wait for them in one statement, so that no use of the
+// results can be scheduled before the wait.
+__device__ __forceinline__ uint4 tmem_ld16(uint32_t taddr) {
+  uint4 v;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(taddr)
+      : "memory");
+  return v;
+}
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint4& a, uint4& b) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%8];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4, %5, %6, %7}, [%9];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+// This consumer thread's first TMEM column address (consumer warp cw).
+__device__ __forceinline__ uint32_t tmem_thread_base(uint32_t tmem, int cw) {
+  const uint32_t quarter = (uint32_t)((cw + 1) & 3);  // warp index cw + 1 in the CTA
+  return tmem + ((quarter * 32u) << 16) + (uint32_t)(cw >> 2) * (uint32_t)kTmemColsPerThread;
 }
 
 // Stage q of segment s: its first vector inside the channel and its length.
@@ -221,15 +293,15 @@ __device__ __forceinline__ bool producer_wait_empty(FShared& sh, int slot, uint3
 }
 
 // The producer warp (all 32 lanes).  L2 policy of the loads: phase 2 reads
-// the resident tail from shared memory, then the l2_window stages before it
-// (which phase 1 loaded at normal priority, so they are likely still in L2),
-// then the rest from DRAM; every other load is marked evict-first so that it
-// does not displace that window.
+// the resident tail from shared memory, then the TMEM stages before it, then
+// the l2_window stages before those (which phase 1 loaded at normal
+// priority, so they are likely still in L2), then the rest from DRAM; every
+// other load is marked evict-first so that it does not displace that window.
 template <typename T, bool BWD>
 __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
   const int NS = a.nstage, N1 = sh.nst;
   const uint64_t keep = l2_policy_evict_normal(), drop = l2_policy_evict_first();
-  const int keep_lo = N1 - NS - a.l2_window, keep_hi = N1 - NS;  // phase-1 stages kept in L2
+  const int keep_lo = sh.t_lo - a.l2_window, keep_hi = sh.t_lo;  // phase-1 stages kept in L2
   uint32_t epar = 0;  // parity of the next "empty" completion per slot
   // Phase 1: forward.  A slot is refilled once its previous stage is released.
   int i = 0;
@@ -245,12 +317,14 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
                           (i >= keep_lo && i < keep_hi) ? keep : drop);
     }
   }
-  // Phase 2: backward; the last NS stages are still resident.
+  // Phase 2: backward; the last NS stages are still resident and stages
+  // [t_lo, t_hi) are in TMEM: only stages i < t_lo are loaded again, each
+  // into slot i % NS.
   int q2 = 0;
   for (int s = sh.nseg - 1; s >= 0; --s) {
     const int nq = stages_in(sh, a, s);
     for (int q = nq - 1; q >= 0; --q, ++q2) {
-      if (q2 < NS) continue;
+      if (N1 - 1 - q2 >= sh.t_lo) continue;
       const int slot = (N1 - 1 - q2) % NS;
       if (!producer_wait_empty(sh, slot, epar, a.status)) return;
       if (__any_sync(0xffffffffu, sh.abort != 0)) return;
@@ -365,6 +439,9 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
   const int ct = threadIdx.x - 32, lane = ct & 31;
   const int NS = a.nstage, N1 = sh.nst;
   const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
+  // TMEM stages: KV vector slots per thread and input, cps columns a stage.
+  const int KV = a.stage_v / kFConsumers, cps = KV * (BWD ? 8 : 4);
+  const uint32_t tbase = tmem_thread_base(sh.tmem, ct >> 5);
   int i = 0;
   for (int s = 0; s < sh.nseg; ++s) {
     const float shift = sh.seg_par[s][0];
@@ -384,7 +461,31 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
-      if constexpr (!BWD) {
+      if (i >= sh.t_lo && i < sh.t_hi) {
+        // A TMEM stage: every lane copies all its vector slots of the stage
+        // (the tcgen05 copies are warp-wide; a slot past len holds stale
+        // ring bytes that phase 2 never uses) and sums the valid ones.
+        uint32_t ta = tbase + (uint32_t)((i - sh.t_lo) * cps);
+        for (int k = 0; k < KV; ++k, ta += (BWD ? 8u : 4u)) {
+          const int v = ct + k * kFConsumers;
+          const uint4 rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
+          tmem_st16(ta, rx);
+          if constexpr (!BWD) {
+            if (v < len) fwd_acc<T>(rx, sh2, nsh2, a0, a1);
+          } else {
+            const uint4 rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
+            tmem_st16(ta + 4u, rd);
+            if (v < len) {
+              if (a.act == GBN_ACT_NONE)
+                bwd_acc<T, GBN_ACT_NONE>(rx, rd, sh2, nsh2, ap, a0, a1);
+              else if (a.act == GBN_ACT_RELU)
+                bwd_acc<T, GBN_ACT_RELU>(rx, rd, sh2, nsh2, ap, a0, a1);
+              else
+                bwd_acc<T, GBN_ACT_LEAKY_RELU>(rx, rd, sh2, nsh2, ap, a0, a1);
+            }
+          }
+        }
+      } else if constexpr (!BWD) {
         for (int v = ct; v < len; v += kFConsumers)
           fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a0, a1);
       } else if (a.act == GBN_ACT_NONE) {
@@ -421,6 +522,8 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
     }
     __syncwarp();
   }
+  // The TMEM copies complete before phase 2 reads them back.
+  if (sh.t_hi > sh.t_lo) tmem_wait_st();
   // Publish: every partial of this CTA was written by this thread above.
   if (ct == 0 && !sh.abort) {
     unsigned long long* f = a.sync + 2 + 2 * (int64_t)blockIdx.x;
@@ -496,6 +599,8 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
   const int ct = threadIdx.x - 32, lane = ct & 31, cw = ct >> 5;
   const int NS = a.nstage, N1 = sh.nst;
   const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
+  const int KV = a.stage_v / kFConsumers, cps = KV * (BWD ? 8 : 4);
+  const uint32_t tbase = tmem_thread_base(sh.tmem, cw);
   for (int s = cw; s < sh.nseg; s += kFConsumerWarps)
     if (!__any_sync(0xffffffffu, sh.abort != 0)) finalize_segment<BWD>(a, sh, s);
   __syncwarp();
@@ -510,8 +615,10 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
     const float slope = a.slope;
     const int nq = stages_in(sh, a, s);
     for (int q = nq - 1; q >= 0; --q, ++q2) {
-      const int slot = (N1 - 1 - q2) % NS;
-      if (q2 >= NS) {
+      const int i = N1 - 1 - q2;  // the stage's index in phase 1
+      const int slot = i % NS;
+      const bool in_tmem = i >= sh.t_lo && i < sh.t_hi;
+      if (i < sh.t_lo) {
         if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
       } else if (__any_sync(0xffffffffu, sh.abort != 0)) {
         continue;
@@ -519,21 +626,37 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
+      const uint32_t ta0 = tbase + (uint32_t)((i - sh.t_lo) * cps);
       // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv.
       const int rv = rv0 + ct;
       int n = rv / a.Pv;
       int pv = rv - n * a.Pv;
-      for (int v = ct; v < len; v += kFConsumers) {
+      // A TMEM stage runs all KV slots on every lane (the TMEM loads are
+      // warp-wide); only slots v < len are computed and stored.
+      for (int u = 0; u < KV; ++u) {
+        const int v = ct + u * kFConsumers;
+        if (!in_tmem && v >= len) break;
+        uint4 rx, rd = make_uint4(0u, 0u, 0u, 0u);
+        if (in_tmem) {
+          if constexpr (BWD)
+            tmem_ld16x2(ta0 + (uint32_t)u * 8u, ta0 + (uint32_t)u * 8u + 4u, rx, rd);
+          else
+            rx = tmem_ld16(ta0 + (uint32_t)u * 4u);
+        } else {
+          rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
+          if constexpr (BWD) rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
+        }
+        if (v >= len) continue;
         const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
         float e[VEC];
-        V::cvt(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), e);
+        V::cvt(rx, e);
         if constexpr (!BWD) {
 #pragma unroll
           for (int k = 0; k < VEC; ++k)
             e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), ACT, slope);
         } else {
           float g[VEC];
-          V::cvt(*reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16), g);
+          V::cvt(rd, g);
 #pragma unroll
           for (int k = 0; k < VEC; ++k) {
             const float xc = (e[k] - shift) - mean_d;
@@ -554,7 +677,10 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
           ++n;
         }
       }
-      if (q2 + NS < N1) {
+      // Release the slot if a later stage of phase 2 is loaded into it: a
+      // reloaded stage i refills i % NS, so a stage < t_lo congruent to i
+      // must exist below i.
+      if (!in_tmem && (i < sh.t_lo ? i >= NS : slot < sh.t_lo)) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.empty[slot]);
       }
@@ -593,6 +719,9 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
     }
     sh.nseg = ns;
     sh.nst = nst;
+    sh.t_hi = max(nst - a.nstage, 0);
+    sh.t_lo = max(sh.t_hi - a.nt, 0);
+    sh.tmem = 0;
     fence_mbarrier_init();
     GBN_RING_TRACE(0);
   }
@@ -608,6 +737,9 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
       const unsigned long long ea = ld_relaxed_u64(a.sync), eb = ld_relaxed_u64(a.sync + 1);
       sh.target = (eb == ~ea ? ea : a.nonce) + 1ull;
     }
+    // Consumer warp 0 takes the SM's TMEM (all columns; the only CTA here).
+    const bool use_tmem = sh.t_hi > sh.t_lo;
+    if (use_tmem && tid < 64) tmem_alloc_all(&sh.tmem);
     if (tid - 32 < sh.nseg) {
       const int s = tid - 32;
       const int64_t c = sh.seg_c[s];
@@ -621,7 +753,9 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
         sh.seg_par[s][5] = a.beta ? a.beta[c] : 0.f;
       }
     }
+    if (use_tmem) tmem_fence_before_sync();
     consumers_sync();
+    if (use_tmem) tmem_fence_after_sync();
     uint32_t fpar = 0;
     consumer_phase1<T, BWD>(a, sh, ring, fpar);
     if (a.act == GBN_ACT_RELU)
@@ -631,6 +765,16 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
     else
       consumer_phase2<T, BWD, GBN_ACT_NONE>(a, sh, ring, fpar);
     if (tid == 32) GBN_RING_TRACE(4);
+    // Every consumer's TMEM loads have completed (each waited for its own);
+    // warp 0 frees the columns.  Reached on every path, aborted or not.
+    if (use_tmem) {
+      tmem_fence_before_sync();
+      consumers_sync();
+      if (tid < 64) {
+        tmem_fence_after_sync();
+        tmem_free_all(sh.tmem);
+      }
+    }
   }
   __syncthreads();
 
@@ -691,6 +835,7 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
   a.dn = (int32_t)(kFConsumers / p.Pv);
   a.dp = (int32_t)(kFConsumers % p.Pv);
   a.l2_window = p.l2_window;
+  a.nt = p.tmem_stages;
   a.stream_out = p.stream_out ? 1 : 0;
   a.Mh = (float)p.M;
   a.Ml = (float)(p.M - (int64_t)a.Mh);
@@ -755,6 +900,11 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
   p->stage_v = (int)stage_v;
   p->nstage = kBnFusedStages;
   p->smem = (size_t)kBnFusedStages * ninputs * (size_t)stage_v * 16;
+  // Stages kept in TMEM between the phases: a consumer thread holds
+  // stage_v / 512 vectors per input and stage in 4 columns each, within its
+  // 128 columns.
+  const int64_t cps = stage_v / kFConsumers * ninputs * 4;
+  p->tmem_stages = cps <= kTmemColsPerThread ? (int)(kTmemColsPerThread / cps) : 0;
   // Stages per CTA whose phase-1 loads stay at normal L2 priority: about
   // three quarters of L2, shared by the G CTAs.
   const int64_t stage_bytes = (int64_t)ninputs * stage_v * 16;

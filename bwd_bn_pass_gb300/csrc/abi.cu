@@ -296,6 +296,8 @@ int64_t gbn_bn_set_small_max_elems(int64_t m) {
 
 int gbn_bn_set_wide_offsets(int force) { return bn_set_wide_offsets(force); }
 
+int gbn_bn_set_persistent_tmem(int enable) { return bn_fused_set_tmem(enable); }
+
 int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                          const float* gamma, const float* beta, float* running_mean,
                          float* running_var, float momentum, float eps, void* y, float* stats,

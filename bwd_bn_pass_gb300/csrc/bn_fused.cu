@@ -620,6 +620,8 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
       const bool in_tmem = i >= sh.t_lo && i < sh.t_hi;
       if (i < sh.t_lo) {
         if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
+        if (ct == 0 && i == sh.t_lo - 1) GBN_RING_TRACE(5);
+        if (ct == 0 && i == sh.t_lo / 2) GBN_RING_TRACE(6);
       } else if (__any_sync(0xffffffffu, sh.abort != 0)) {
         continue;
       }
@@ -846,7 +848,10 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
 
 namespace {
 std::atomic<unsigned long long> g_nonce{0};
+std::atomic<int> g_tmem{1};
 }  // namespace
+
+int bn_fused_set_tmem(int enable) { return g_tmem.exchange(enable != 0 ? 1 : 0); }
 
 // A fresh 64-bit value per call (splitmix64 of a process counter): the flag
 // epoch used when a workspace holds no valid epoch pair.
@@ -904,7 +909,8 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
   // stage_v / 512 vectors per input and stage in 4 columns each, within its
   // 128 columns.
   const int64_t cps = stage_v / kFConsumers * ninputs * 4;
-  p->tmem_stages = cps <= kTmemColsPerThread ? (int)(kTmemColsPerThread / cps) : 0;
+  p->tmem_stages =
+      (g_tmem.load() != 0 && cps <= kTmemColsPerThread) ? (int)(kTmemColsPerThread / cps) : 0;
   // Stages per CTA whose phase-1 loads stay at normal L2 priority: about
   // three quarters of L2, shared by the G CTAs.
   const int64_t stage_bytes = (int64_t)ninputs * stage_v * 16;

@@ -64,6 +64,7 @@ _SIGNATURES = {
     "gbn_bn_set_small_max_elems": (_I64, [_I64]),
     "gbn_bn_persistent_min_bytes": (_I64, []),
     "gbn_bn_set_wide_offsets": (_INT, [_INT]),
+    "gbn_bn_set_persistent_tmem": (_INT, [_INT]),
     "gbn_bn_forward_train": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                     _P, _P, _P, _SZ, _P]),
     "gbn_bn_forward_train_noalloc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F,
@@ -219,6 +220,13 @@ def bn_set_small_max_elems(m):
 
 def bn_persistent_min_bytes():
     return lib().gbn_bn_persistent_min_bytes()
+
+
+def bn_set_persistent_tmem(enable):
+    """Whether the persistent BatchNorm kernel keeps stages in tensor memory
+    between its passes (default on; results are bit-identical either way).
+    Returns the previous setting."""
+    return lib().gbn_bn_set_persistent_tmem(1 if enable else 0)
 
 
 def bn_set_wide_offsets(force):

@@ -176,6 +176,14 @@ GBN_API int64_t gbn_bn_persistent_min_bytes(void);
  * previous value.  The pages have no counterpart: a tuning knob.           */
 GBN_API int64_t gbn_bn_set_small_max_elems(int64_t m);
 
+/* The persistent BatchNorm kernel keeps a few stages per SM in tensor
+ * memory (TMEM) between its reduction and output passes, instead of loading
+ * them again.  enable = 0 turns that off for later calls, nonzero turns it
+ * back on (the default).  Results are bit-identical either way; only where
+ * phase 2 reads those stages from changes.  Process-wide; returns the
+ * previous setting.  The pages have no counterpart: a tuning knob.         */
+GBN_API int gbn_bn_set_persistent_tmem(int enable);
+
 /* The two-launch BatchNorm kernels (NCHW) address vectors with 32-bit
  * offsets while the tensor holds fewer than 2^32 16-byte-or-smaller vectors,
  * and with 64-bit offsets beyond.  A nonzero `force` makes every later call

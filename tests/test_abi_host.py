@@ -183,6 +183,14 @@ def test_bn_small_channel_switch(gbn):
     assert L.gbn_bn_set_small_max_elems(prev) == 2048      # capped at the kernels' limit
 
 
+def test_bn_persistent_tmem_switch(gbn):
+    L = gbn.lib()
+    prev = L.gbn_bn_set_persistent_tmem(0)
+    assert prev in (0, 1)
+    assert L.gbn_bn_set_persistent_tmem(7) == 0
+    assert L.gbn_bn_set_persistent_tmem(prev) == 1          # nonzero stored as 1
+
+
 def test_bn_persistent_threshold(gbn):
     L = gbn.lib()
     prev = L.gbn_bn_set_persistent_min_bytes(12345)

@@ -143,6 +143,36 @@ def test_bn_offset_bf16_full_size_bit_deterministic(gbn):
         assert torch.equal(a[k], b[k]), f"{k} differs between two runs"
 
 
+TMEM_CASES = [
+    synth.CASES["bn_offset_bf16"],
+    synth.CASES["bn_offset_f32"],
+    synth.BNCase("segs_bf16", (16, 2048, 8, 8), "bf16", mu_range=(-100, 100),
+                 sigma_range=(0.01, 10), seed=91),
+    synth.BNCase("mid_bf16", (64, 96, 28, 28), "bf16", mu_range=(-100, 100),
+                 sigma_range=(0.01, 10), seed=92),
+]
+
+
+@pytest.mark.parametrize("case", TMEM_CASES, ids=lambda c: c.name)
+def test_bn_persistent_tmem_bit_identical(gbn, case):
+    """The persistent kernel with and without its tensor-memory tier (five
+    stages per SM kept in TMEM between the passes) gives the same bits: full
+    bf16 [128,256,56,56], fp32 [256,32,32,32], a range of 16 one-stage
+    channel segments per CTA ([16,2048,8,8]) and a short range
+    ([64,96,28,28]).  Runs on the persistent-everywhere setting only."""
+    if gbn.bn_persistent_min_bytes() != 0:
+        pytest.skip("checked once, with the persistent kernel taking every shape")
+    inp = synth.bn_inputs(case)
+    prev = gbn.bn_set_persistent_tmem(False)
+    try:
+        off = run_gpu(gbn, inp)
+    finally:
+        gbn.bn_set_persistent_tmem(prev)
+    on = run_gpu(gbn, inp)
+    for k in on:
+        assert torch.equal(on[k], off[k]), f"{k} differs with the TMEM tier"
+
+
 @pytest.mark.parametrize("name", ["bn_offset_f32", "bn_ragged_f32"])
 def test_bn_bit_deterministic(gbn, name):
     inp = synth.bn_inputs(synth.CASES[name])

@@ -36,6 +36,17 @@
 //     instead of loading those stages again; the L2 window moves back by nt
 //     stages.  The CTA holds all 512 columns for the whole launch (one CTA
 //     per SM) and frees them before it exits, also after a failed wait.
+//   * Work stealing at the end of phase 2: a CTA's first stages (the last
+//     it would reload) form a small pool that other CTAs may take once they
+//     run out of their own work, so that CTAs on slower SMs (the phase-2
+//     time of a CTA depends on the SM it runs on) finish with the rest.  A
+//     pool word per CTA holds the unclaimed stages [lo, hi): the owner
+//     claims from the top with an atomic subtract, other CTAs from the
+//     bottom with an atomic add, so every stage is processed exactly once,
+//     with the owner's finalized channel parameters (published after its
+//     finalize, behind a release flag) -- the same bits either way.  In
+//     phase 2 the producer hands each loaded stage to the consumers with a
+//     descriptor (channel, vectors, parameters) in shared memory.
 //   * Flags carry an epoch: (e+1, ~(e+1)) per CTA, with e read at kernel
 //     start from the workspace's epoch pair (or a host nonce if that pair is
 //     not self-consistent); CTA 0 advances the epoch once every CTA has
@@ -67,6 +78,12 @@ constexpr int kFThreads = kFConsumers + 32;        // + the producer warp
 constexpr int kFMaxStages = 8;
 constexpr int kFMaxSegs = 32;                      // channel segments per CTA
 constexpr int kFStaticSmem = 4096;                 // bound on the static shared memory
+constexpr int kPoolMax = 8;       // stages per CTA that other CTAs may take in phase 2, at most
+constexpr int kPubFloats = 8;     // published parameters per segment (6 used)
+constexpr int kStealScans = 64;   // claims (and victim scans) of a CTA's producer, at most
+constexpr int kStealBatch = 2;    // pool stages taken per claim, at most
+constexpr int kMaxCtas = 160;     // CTAs of a launch, at most (one per SM)
+constexpr int kPoolMinStages = 16;  // reloaded stages per CTA from which the pool is used
 
 struct FArgs {
   const void* x;
@@ -82,6 +99,9 @@ struct FArgs {
   int32_t act;           // GBN_ACT_*: output act(pre) forward, gate on dy backward
   float slope;           // LeakyReLU negative slope
   unsigned long long* sync;  // [2] epoch pair, then [G][2] flag pairs
+  uint32_t* steal;           // [G] pool words: unclaimed pool stages [lo, hi) as hi << 16 | lo
+  unsigned long long* pubflag;  // [G] set (release) once the CTA's parameters are published
+  float* pub;                // [G][kPoolMax][kPubFloats] parameters of a CTA's first segments
   float2* part;              // [2][grid_y][C]
   int* status;
   unsigned long long nonce;
@@ -97,8 +117,17 @@ struct FArgs {
   int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
   int32_t l2_window; // phase-1 stages before the TMEM stages kept at normal L2 priority
   int32_t nt;        // stages kept in TMEM between the phases (0: none)
+  int32_t pool;      // a CTA's first stages (at most kPoolMax) open to other CTAs in phase 2
   int32_t stream_out; // outputs with the evict-first hint (tensors larger than L2 holds)
   float Mh, Ml;      // per-channel count M = Mh + Ml exactly
+};
+
+// A phase-2 stage as the producer hands it to the consumers: channel c,
+// first vector rv0 inside the channel, len vectors, the channel's parameters
+// (as seg_par), or the end of the CTA's work.
+struct FDesc {
+  int c, rv0, len, end;
+  float par[6];
 };
 
 // Parameters per segment: [0] shift, [1] mean - shift (rounded),
@@ -112,6 +141,9 @@ struct FShared {
   int nst;                    // stages in the range
   int t_lo, t_hi;             // stages [t_lo, t_hi) are kept in TMEM; stages < t_lo reload
   uint32_t tmem;              // TMEM base address (written by tcgen05.alloc)
+  int pool;                   // this CTA's pool stages [0, pool)
+  volatile int p2ready;       // set once this CTA has finalized (and published)
+  FDesc desc[kFMaxStages];    // phase 2: what the producer loaded into each slot
   volatile int abort;
   int seg_c[kFMaxSegs];
   int seg_rv0[kFMaxSegs];     // first vector of the segment inside its channel
@@ -246,6 +278,42 @@ __device__ __forceinline__ int stages_in(const FShared& sh, const FArgs& a, int 
   return (sh.seg_len[s] + a.stage_v - 1) / a.stage_v;
 }
 
+// Stage j (phase-1 numbering) of CTA v's range: its channel c, first vector
+// rv0 inside the channel, length and segment index -- the segments computed
+// the way the kernel's set-up computes its own.
+__device__ bool range_stage(const FArgs& a, int v, int j, int& c, int& rv0, int& len, int& seg) {
+  const int64_t e0 = (int64_t)v * a.Wv;
+  const int64_t e1 = min(e0 + a.Wv, a.C * (int64_t)a.Mv);
+  int sg = 0;
+  for (int64_t e = e0; e < e1 && sg < kFMaxSegs; ++sg) {
+    const int64_t cc = e / a.Mv;
+    const int64_t cend = min((cc + 1) * (int64_t)a.Mv, e1);
+    const int slen = (int)(cend - e);
+    const int nq = (slen + a.stage_v - 1) / a.stage_v;
+    if (j < nq) {
+      c = (int)cc;
+      rv0 = (int)(e - cc * a.Mv) + j * a.stage_v;
+      len = min(a.stage_v, slen - j * a.stage_v);
+      seg = sg;
+      return true;
+    }
+    j -= nq;
+    e = cend;
+  }
+  return false;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------- producer --
 
 // Bulk copies of one stage (plane runs of channel c) into `slot`, issued by
@@ -317,22 +385,159 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
                           (i >= keep_lo && i < keep_hi) ? keep : drop);
     }
   }
-  // Phase 2: backward; the last NS stages are still resident and stages
-  // [t_lo, t_hi) are in TMEM: only stages i < t_lo are loaded again, each
-  // into slot i % NS.
+  // Phase 2.  The consumers first work through the resident tail and the
+  // TMEM stages, which need no loads; everything else goes through the
+  // slots they free, push j into slot (N1 - 1 - j) mod NS, each with a
+  // descriptor: this CTA's stages from t_lo - 1 down to its pool, then the
+  // pool stages it still claims (from the top), then stages it claims from
+  // other CTAs' pools (from the bottom), then an end marker.  A pool word
+  // holds the unclaimed pool stages [lo, hi) as hi << 16 | lo: the owner
+  // takes hi - 1 by subtracting 1 << 16, another CTA takes lo by adding 1,
+  // and the atomic order decides every stage exactly once.
+  const int lane = threadIdx.x & 31;
+  int j = 0;
+  auto push = [&](int c, int rv0, int len, const float* par, bool end) -> bool {
+    const int slot = ((N1 - 1 - j) % NS + NS) % NS;
+    if (sh.issued[slot] > 0 && !producer_wait_empty(sh, slot, epar, a.status)) return false;
+    if (__any_sync(0xffffffffu, sh.abort != 0)) return false;
+    if (lane == 0) {
+      FDesc& d = sh.desc[slot];
+      d.c = c;
+      d.rv0 = rv0;
+      d.len = len;
+      d.end = end ? 1 : 0;
+      for (int f = 0; f < 6; ++f) d.par[f] = end ? 0.f : par[f];
+    }
+    __syncwarp();
+    if (end) {
+      if (lane == 0) {
+        sh.issued[slot] += 1;
+        mbar_arrive(&sh.full[slot]);
+      }
+      __syncwarp();
+    } else {
+      issue_stage<T, BWD>(a, sh, ring, slot, c, rv0, len, drop);
+    }
+    ++j;
+    return true;
+  };
+  // this CTA's stages below the on-chip ones, down to the pool
   int q2 = 0;
   for (int s = sh.nseg - 1; s >= 0; --s) {
     const int nq = stages_in(sh, a, s);
     for (int q = nq - 1; q >= 0; --q, ++q2) {
-      if (N1 - 1 - q2 >= sh.t_lo) continue;
-      const int slot = (N1 - 1 - q2) % NS;
-      if (!producer_wait_empty(sh, slot, epar, a.status)) return;
-      if (__any_sync(0xffffffffu, sh.abort != 0)) return;
+      const int i2 = N1 - 1 - q2;
+      if (i2 >= sh.t_lo || i2 < sh.pool) continue;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
-      issue_stage<T, BWD>(a, sh, ring, slot, sh.seg_c[s], rv0, len, drop);
+      if (!push(sh.seg_c[s], rv0, len, sh.seg_par[s], false)) return;
     }
   }
+  // this CTA's pool stages that no other CTA has taken
+  for (int left = sh.pool; left > 0; --left) {
+    uint32_t old = 0;
+    if (lane == 0) old = atomicSub(a.steal + blockIdx.x, 1u << 16);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    const int hi = (int)(old >> 16), lo = (int)(old & 0xffffu);
+    if (hi <= lo) break;
+    int rem = hi - 1, s = 0;
+    while (s < sh.nseg - 1 && rem >= stages_in(sh, a, s)) rem -= stages_in(sh, a, s++);
+    int rv0, len;
+    stage_of(sh, a, s, rem, rv0, len);
+    if (!push(sh.seg_c[s], rv0, len, sh.seg_par[s], false)) return;
+  }
+  // stages from the pools of other CTAs: the one with the most left first
+  // (once this CTA's consumers have finalized: sh.target is set by then)
+  bool ready = a.pool > 0;
+  if (ready) {
+    const uint64_t t0 = global_timer_ns();
+    while (!sh.p2ready && !sh.abort) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        ready = false;
+        break;
+      }
+    }
+    ready = __all_sync(0xffffffffu, ready && !sh.abort);
+  }
+  // A claim takes up to kStealBatch stages at once; a CTA keeps claiming
+  // from the same owner until that pool is empty, and keeps the owner's
+  // parameters of the last segment it read.
+  int victim = -1, pv_seg = -1;
+  float par[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int scan = 0; scan < kStealScans && ready; ++scan) {
+    if (victim < 0) {
+      // Owners with at least half the largest number of unclaimed pool
+      // stages qualify; each CTA takes the first of them after itself in
+      // block order, so that the CTAs spread over the owners instead of all
+      // contending for the one with the most left.
+      constexpr int kWordsPerLane = (kMaxCtas + 31) / 32;
+      int rem[kWordsPerLane];
+      int rmax = 0;
+#pragma unroll
+      for (int u = 0; u < kWordsPerLane; ++u) {
+        const int v = lane + 32 * u;
+        rem[u] = 0;
+        if (v < a.G && v != (int)blockIdx.x) {
+          const uint32_t w = ld_relaxed_u32(a.steal + v);
+          rem[u] = (int)(w >> 16) - (int)(w & 0xffffu);
+        }
+        rmax = max(rmax, rem[u]);
+      }
+      for (int o = 16; o > 0; o >>= 1) rmax = max(rmax, __shfl_xor_sync(0xffffffffu, rmax, o));
+      if (rmax <= 0) break;
+      const int thr = max(1, rmax / 2);
+      int bd = a.G, best = -1;  // rotated distance from this CTA, and the owner
+#pragma unroll
+      for (int u = 0; u < kWordsPerLane; ++u) {
+        const int v = lane + 32 * u;
+        const int d = (v - (int)blockIdx.x + a.G) % a.G;
+        if (rem[u] >= thr && d < bd) {
+          bd = d;
+          best = v;
+        }
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        const int d2 = __shfl_xor_sync(0xffffffffu, bd, o);
+        const int b2 = __shfl_xor_sync(0xffffffffu, best, o);
+        if (d2 < bd) {
+          bd = d2;
+          best = b2;
+        }
+      }
+      if (best < 0) break;
+      // the owner's parameters must be published before its pool is used
+      int ok = 0;
+      if (lane == 0) ok = ld_acquire_u64(a.pubflag + best) == sh.target;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) continue;
+      victim = best;
+      pv_seg = -1;
+    }
+    uint32_t old = 0;
+    if (lane == 0) old = atomicAdd(a.steal + victim, (uint32_t)kStealBatch);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    const int lo = (int)(old & 0xffffu), hi = (int)(old >> 16);
+    if (lo >= hi) {
+      victim = -1;
+      continue;
+    }
+    for (int g = lo; g < min(lo + kStealBatch, hi); ++g) {
+      int c = 0, rv0 = 0, len = 0, sg = 0;
+      if (!range_stage(a, victim, g, c, rv0, len, sg) || sg >= kPoolMax) {
+        // cannot happen for a consistent pool word
+        if (lane == 0) set_abort(sh, a.status);
+        return;
+      }
+      if (sg != pv_seg) {
+        if (lane == 0) {
+          const float* src = a.pub + ((int64_t)victim * kPoolMax + sg) * kPubFloats;
+          for (int f = 0; f < 6; ++f) par[f] = ld_relaxed_f32(src + f);
+        }
+        pv_seg = sg;
+      }
+      if (!push(c, rv0, len, par, false)) return;
+    }
+  }
+  push(0, 0, 0, nullptr, true);
 }
 
 // ------------------------------------------------------------ consumers --
@@ -589,16 +794,80 @@ __device__ void finalize_segment(const FArgs& a, FShared& sh, int s) {
   __syncwarp();
 }
 
-// ACT is the activation (GBN_ACT_*) as a compile-time switch, so that the
-// plain pass carries no per-element test.
+// Outputs of one phase-2 stage (channel c, vectors [rv0, rv0 + len) of the
+// channel, parameters par as seg_par) from ring slot st, or from TMEM at ta0
+// when in_tmem.  A TMEM stage runs all KV slots on every lane (the TMEM
+// loads are warp-wide); only slots v < len are computed and stored.  ACT is
+// the activation (GBN_ACT_*) as a compile-time switch, so that the plain
+// pass carries no per-element test.
+template <typename T, bool BWD, int ACT>
+__device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int len,
+                                          const float* par, const unsigned char* st,
+                                          uint32_t in_bytes, bool in_tmem, uint32_t ta0, int KV) {
+  constexpr int VEC = 16 / sizeof(T);
+  using V = Vec<T, VEC>;
+  const int ct = threadIdx.x - 32;
+  const float shift = par[0], mean_d = par[1], scale = par[2];
+  const float p3 = par[3], p4 = par[4], beta = par[5];
+  const float slope = a.slope;
+  T* out = static_cast<T*>(a.out);
+  // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv.
+  const int rv = rv0 + ct;
+  int n = rv / a.Pv;
+  int pv = rv - n * a.Pv;
+  for (int u = 0; u < KV; ++u) {
+    const int v = ct + u * kFConsumers;
+    if (!in_tmem && v >= len) break;
+    uint4 rx, rd = make_uint4(0u, 0u, 0u, 0u);
+    if (in_tmem) {
+      if constexpr (BWD)
+        tmem_ld16x2(ta0 + (uint32_t)u * 8u, ta0 + (uint32_t)u * 8u + 4u, rx, rd);
+      else
+        rx = tmem_ld16(ta0 + (uint32_t)u * 4u);
+    } else {
+      rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
+      if constexpr (BWD) rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
+    }
+    if (v >= len) continue;
+    const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
+    float e[VEC];
+    V::cvt(rx, e);
+    if constexpr (!BWD) {
+#pragma unroll
+      for (int k = 0; k < VEC; ++k)
+        e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), ACT, slope);
+    } else {
+      float g[VEC];
+      V::cvt(rd, g);
+#pragma unroll
+      for (int k = 0; k < VEC; ++k) {
+        const float xc = (e[k] - shift) - mean_d;
+        const float gk = ACT == GBN_ACT_NONE
+                             ? g[k]
+                             : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), ACT, slope));
+        e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
+      }
+    }
+    if (a.stream_out)
+      store16_cs(out + gvo * VEC, e);
+    else
+      V::store(out + gvo * VEC, e);
+    pv += a.dp;
+    n += a.dn;
+    if (pv >= a.Pv) {
+      pv -= a.Pv;
+      ++n;
+    }
+  }
+}
+
 template <typename T, bool BWD, int ACT>
 __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char* ring,
                                 uint32_t& fpar) {
-  constexpr int VEC = 16 / sizeof(T);
-  using V = Vec<T, VEC>;
   const int ct = threadIdx.x - 32, lane = ct & 31, cw = ct >> 5;
   const int NS = a.nstage, N1 = sh.nst;
   const uint32_t in_bytes = (uint32_t)a.stage_v * 16u;
+  const size_t slot_bytes = (size_t)(BWD ? 2u : 1u) * in_bytes;
   const int KV = a.stage_v / kFConsumers, cps = KV * (BWD ? 8 : 4);
   const uint32_t tbase = tmem_thread_base(sh.tmem, cw);
   for (int s = cw; s < sh.nseg; s += kFConsumerWarps)
@@ -606,88 +875,59 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
   __syncwarp();
   consumers_sync();
   if (ct == 0) GBN_RING_TRACE(3);
-  T* out = static_cast<T*>(a.out);
+  // Publish the parameters of the first segments (those holding the pool
+  // stages) for CTAs that take pool stages of this one.
+  if (cw == 0 && a.pool > 0 && !__any_sync(0xffffffffu, sh.abort != 0)) {
+    const int np = min(sh.nseg, kPoolMax);
+    for (int x = lane; x < np * 6; x += 32)
+      a.pub[((int64_t)blockIdx.x * kPoolMax + x / 6) * kPubFloats + x % 6] =
+          sh.seg_par[x / 6][x % 6];
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      st_release_u64(a.pubflag + blockIdx.x, sh.target);
+    }
+    __syncwarp();
+  }
+  if (ct == 0) sh.p2ready = 1;
+  // The on-chip stages: the resident tail (released afterwards, the
+  // producer refills those slots) and the TMEM stages.
   int q2 = 0;
   for (int s = sh.nseg - 1; s >= 0; --s) {
-    const int c = sh.seg_c[s];
-    const float shift = sh.seg_par[s][0], mean_d = sh.seg_par[s][1], scale = sh.seg_par[s][2];
-    const float p3 = sh.seg_par[s][3], p4 = sh.seg_par[s][4], beta = sh.seg_par[s][5];
-    const float slope = a.slope;
     const int nq = stages_in(sh, a, s);
     for (int q = nq - 1; q >= 0; --q, ++q2) {
       const int i = N1 - 1 - q2;  // the stage's index in phase 1
+      if (i < sh.t_lo) continue;
+      if (__any_sync(0xffffffffu, sh.abort != 0)) continue;
       const int slot = i % NS;
-      const bool in_tmem = i >= sh.t_lo && i < sh.t_hi;
-      if (i < sh.t_lo) {
-        if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
-        if (ct == 0 && i == sh.t_lo - 1) GBN_RING_TRACE(5);
-        if (ct == 0 && i == sh.t_lo / 2) GBN_RING_TRACE(6);
-      } else if (__any_sync(0xffffffffu, sh.abort != 0)) {
-        continue;
-      }
+      const bool in_tmem = i < sh.t_hi;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
-      const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
-      const uint32_t ta0 = tbase + (uint32_t)((i - sh.t_lo) * cps);
-      // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv.
-      const int rv = rv0 + ct;
-      int n = rv / a.Pv;
-      int pv = rv - n * a.Pv;
-      // A TMEM stage runs all KV slots on every lane (the TMEM loads are
-      // warp-wide); only slots v < len are computed and stored.
-      for (int u = 0; u < KV; ++u) {
-        const int v = ct + u * kFConsumers;
-        if (!in_tmem && v >= len) break;
-        uint4 rx, rd = make_uint4(0u, 0u, 0u, 0u);
-        if (in_tmem) {
-          if constexpr (BWD)
-            tmem_ld16x2(ta0 + (uint32_t)u * 8u, ta0 + (uint32_t)u * 8u + 4u, rx, rd);
-          else
-            rx = tmem_ld16(ta0 + (uint32_t)u * 4u);
-        } else {
-          rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
-          if constexpr (BWD) rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
-        }
-        if (v >= len) continue;
-        const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
-        float e[VEC];
-        V::cvt(rx, e);
-        if constexpr (!BWD) {
-#pragma unroll
-          for (int k = 0; k < VEC; ++k)
-            e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), ACT, slope);
-        } else {
-          float g[VEC];
-          V::cvt(rd, g);
-#pragma unroll
-          for (int k = 0; k < VEC; ++k) {
-            const float xc = (e[k] - shift) - mean_d;
-            const float gk = ACT == GBN_ACT_NONE
-                                 ? g[k]
-                                 : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), ACT, slope));
-            e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
-          }
-        }
-        if (a.stream_out)
-          store16_cs(out + gvo * VEC, e);
-        else
-          V::store(out + gvo * VEC, e);
-        pv += a.dp;
-        n += a.dn;
-        if (pv >= a.Pv) {
-          pv -= a.Pv;
-          ++n;
-        }
-      }
-      // Release the slot if a later stage of phase 2 is loaded into it: a
-      // reloaded stage i refills i % NS, so a stage < t_lo congruent to i
-      // must exist below i.
-      if (!in_tmem && (i < sh.t_lo ? i >= NS : slot < sh.t_lo)) {
+      stage_out<T, BWD, ACT>(a, sh.seg_c[s], rv0, len, sh.seg_par[s],
+                             ring + (size_t)slot * slot_bytes, in_bytes, in_tmem,
+                             tbase + (uint32_t)((i - sh.t_lo) * cps), KV);
+      if (!in_tmem) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.empty[slot]);
       }
     }
   }
+  // Then what the producer loads, in its push order, until its end marker.
+  for (int j = 0;; ++j) {
+    const int slot = ((N1 - 1 - j) % NS + NS) % NS;
+    if (!warp_wait_full(sh, slot, fpar, a.status)) break;
+    const FDesc& d = sh.desc[slot];
+    if (d.end) break;
+    if (ct == 0 && j == 0) GBN_RING_TRACE(5);
+    float par[6];
+#pragma unroll
+    for (int f = 0; f < 6; ++f) par[f] = d.par[f];
+    stage_out<T, BWD, ACT>(a, d.c, d.rv0, d.len, par, ring + (size_t)slot * slot_bytes,
+                           in_bytes, false, 0u, KV);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[slot]);
+  }
+  if (ct == 0) GBN_RING_TRACE(6);
 }
 
 template <typename T, bool BWD>
@@ -724,6 +964,11 @@ __global__ void __launch_bounds__(kFThreads, 1) bn_fused_kernel(const FArgs a) {
     sh.t_hi = max(nst - a.nstage, 0);
     sh.t_lo = max(sh.t_hi - a.nt, 0);
     sh.tmem = 0;
+    sh.pool = min(a.pool, sh.t_lo);
+    sh.p2ready = 0;
+    // this CTA's pool word: stages [0, pool) unclaimed (published to the
+    // other CTAs by the release of pubflag after the finalize)
+    if (a.pool > 0) a.steal[blockIdx.x] = (uint32_t)sh.pool << 16;
     fence_mbarrier_init();
     GBN_RING_TRACE(0);
   }
@@ -820,10 +1065,26 @@ cudaError_t launch_fused(const FArgs& a, const BnFusedPlan& p, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, bn_fused_kernel<T, BWD>, a);
 }
 
+// Workspace of the persistent kernel: the epoch pair and a flag pair per CTA
+// (16 bytes each), the pool words (4 bytes per CTA), the publish flags (8
+// bytes per CTA), the published parameters (kPoolMax x kPubFloats floats per
+// CTA), then, from the next 256-byte boundary, the partials.
+size_t ws_steal_off(int G) { return ((size_t)16 + (size_t)16 * G + 15) & ~(size_t)15; }
+size_t ws_pubflag_off(int G) { return (ws_steal_off(G) + (size_t)4 * G + 15) & ~(size_t)15; }
+size_t ws_pub_off(int G) { return (ws_pubflag_off(G) + (size_t)8 * G + 15) & ~(size_t)15; }
+size_t ws_part_off(int G) {
+  return (ws_pub_off(G) + (size_t)G * kPoolMax * kPubFloats * sizeof(float) + 255) & ~(size_t)255;
+}
+
 FArgs make_args(const BnFusedPlan& p, void* ws) {
   FArgs a = {};
+  unsigned char* w = static_cast<unsigned char*>(ws);
   a.sync = static_cast<unsigned long long*>(ws);
-  a.part = reinterpret_cast<float2*>(static_cast<unsigned char*>(ws) + p.part_offset);
+  a.steal = reinterpret_cast<uint32_t*>(w + ws_steal_off(p.G));
+  a.pubflag = reinterpret_cast<unsigned long long*>(w + ws_pubflag_off(p.G));
+  a.pub = reinterpret_cast<float*>(w + ws_pub_off(p.G));
+  a.pool = p.pool;
+  a.part = reinterpret_cast<float2*>(w + p.part_offset);
   a.nonce = next_nonce();
   a.C = p.C;
   a.P = p.P;
@@ -920,7 +1181,13 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
   // re-reads; smaller outputs are left to L2, which absorbs the writes.
   const int64_t call_bytes = (int64_t)(ninputs + 1) * C * p->M * esize;
   p->stream_out = call_bytes > (int64_t)dev.l2_bytes / 2;
-  p->part_offset = ((size_t)16 + (size_t)16 * p->G + 255) & ~(size_t)255;
+  // A CTA's first stages that other CTAs may take over in phase 2, so that
+  // CTAs on slower SMs finish with the rest: only where a CTA reloads enough
+  // stages in phase 2 for the claims to pay (measured: about 1-4 us slower
+  // on short ranges, faster on [128,256,56,56] bf16).
+  const int64_t reload = (p->Wv + stage_v - 1) / stage_v - kBnFusedStages - p->tmem_stages;
+  p->pool = (reload >= kPoolMinStages && p->G <= kMaxCtas) ? kPoolMax : 0;
+  p->part_offset = ws_part_off(p->G);
   p->ws_bytes = p->part_offset + (size_t)2 * p->grid_y * C * sizeof(float2);
   p->ws_bytes = (p->ws_bytes + 255) & ~(size_t)255;
   p->ok = true;

@@ -115,6 +115,7 @@ struct BnFusedPlan {
   int nstage = 0;
   int l2_window = 0;       // phase-1 stages per CTA kept at normal L2 priority
   int tmem_stages = 0;     // stages per CTA kept in tensor memory between the phases
+  int pool = 0;            // a CTA's first stages open to other CTAs in phase 2
   bool stream_out = true;  // outputs stored with the evict-first hint
   size_t smem = 0;         // dynamic shared memory (the ring)
   size_t part_offset = 0;  // partials offset in the workspace (sync words first)

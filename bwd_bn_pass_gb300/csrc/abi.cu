@@ -298,6 +298,8 @@ int gbn_bn_set_wide_offsets(int force) { return bn_set_wide_offsets(force); }
 
 int gbn_bn_set_persistent_tmem(int enable) { return bn_fused_set_tmem(enable); }
 
+int gbn_bn_set_persistent_steal(int enable) { return bn_fused_set_steal(enable); }
+
 int gbn_bn_forward_train(const void* x, int dtype, int64_t B, int64_t C, int64_t HW,
                          const float* gamma, const float* beta, float* running_mean,
                          float* running_var, float momentum, float eps, void* y, float* stats,

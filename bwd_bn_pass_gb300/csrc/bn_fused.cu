@@ -1110,9 +1110,11 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
 namespace {
 std::atomic<unsigned long long> g_nonce{0};
 std::atomic<int> g_tmem{1};
+std::atomic<int> g_steal{1};
 }  // namespace
 
 int bn_fused_set_tmem(int enable) { return g_tmem.exchange(enable != 0 ? 1 : 0); }
+int bn_fused_set_steal(int enable) { return g_steal.exchange(enable != 0 ? 1 : 0); }
 
 // A fresh 64-bit value per call (splitmix64 of a process counter): the flag
 // epoch used when a workspace holds no valid epoch pair.
@@ -1186,7 +1188,8 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
   // stages in phase 2 for the claims to pay (measured: about 1-4 us slower
   // on short ranges, faster on [128,256,56,56] bf16).
   const int64_t reload = (p->Wv + stage_v - 1) / stage_v - kBnFusedStages - p->tmem_stages;
-  p->pool = (reload >= kPoolMinStages && p->G <= kMaxCtas) ? kPoolMax : 0;
+  p->pool =
+      (g_steal.load() != 0 && reload >= kPoolMinStages && p->G <= kMaxCtas) ? kPoolMax : 0;
   p->part_offset = ws_part_off(p->G);
   p->ws_bytes = p->part_offset + (size_t)2 * p->grid_y * C * sizeof(float2);
   p->ws_bytes = (p->ws_bytes + 255) & ~(size_t)255;

@@ -128,6 +128,8 @@ bool bn_fused_plan(int dtype, bool backward, int64_t B, int64_t C, int64_t HW,
                    const DevInfo& dev, BnFusedPlan* plan);
 // Whether later plans keep stages in TMEM (process-wide); returns the previous setting.
 int bn_fused_set_tmem(int enable);
+// Whether later plans let CTAs take other CTAs' last stages; returns the previous setting.
+int bn_fused_set_steal(int enable);
 cudaError_t bn_fused_forward(const BnFusedPlan& p, int dtype, const void* x, void* y,
                              const float* gamma, const float* beta, float* stats,
                              float* running_mean, float* running_var, float momentum, float eps,

@@ -65,6 +65,7 @@ _SIGNATURES = {
     "gbn_bn_persistent_min_bytes": (_I64, []),
     "gbn_bn_set_wide_offsets": (_INT, [_INT]),
     "gbn_bn_set_persistent_tmem": (_INT, [_INT]),
+    "gbn_bn_set_persistent_steal": (_INT, [_INT]),
     "gbn_bn_forward_train": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F, _F,
                                     _P, _P, _P, _SZ, _P]),
     "gbn_bn_forward_train_noalloc": (_INT, [_P, _INT, _I64, _I64, _I64, _P, _P, _P, _P, _F,
@@ -227,6 +228,13 @@ def bn_set_persistent_tmem(enable):
     between its passes (default on; results are bit-identical either way).
     Returns the previous setting."""
     return lib().gbn_bn_set_persistent_tmem(1 if enable else 0)
+
+
+def bn_set_persistent_steal(enable):
+    """Whether CTAs of the persistent BatchNorm kernel take other CTAs' last
+    stages at the end of its output pass (default on; results are
+    bit-identical either way).  Returns the previous setting."""
+    return lib().gbn_bn_set_persistent_steal(1 if enable else 0)
 
 
 def bn_set_wide_offsets(force):

@@ -184,6 +184,14 @@ GBN_API int64_t gbn_bn_set_small_max_elems(int64_t m);
  * previous setting.  The pages have no counterpart: a tuning knob.         */
 GBN_API int gbn_bn_set_persistent_tmem(int enable);
 
+/* The persistent BatchNorm kernel lets CTAs that run out of work take the
+ * last stages of others at the end of its output pass (on tensors large
+ * enough for it to pay).  enable = 0 turns that off for later calls,
+ * nonzero back on (the default).  Results are bit-identical either way.
+ * Process-wide; returns the previous setting.  A tuning knob; the pages
+ * have no counterpart.                                                     */
+GBN_API int gbn_bn_set_persistent_steal(int enable);
+
 /* The two-launch BatchNorm kernels (NCHW) address vectors with 32-bit
  * offsets while the tensor holds fewer than 2^32 16-byte-or-smaller vectors,
  * and with 64-bit offsets beyond.  A nonzero `force` makes every later call

@@ -191,6 +191,14 @@ def test_bn_persistent_tmem_switch(gbn):
     assert L.gbn_bn_set_persistent_tmem(prev) == 1          # nonzero stored as 1
 
 
+def test_bn_persistent_steal_switch(gbn):
+    L = gbn.lib()
+    prev = L.gbn_bn_set_persistent_steal(0)
+    assert prev in (0, 1)
+    assert L.gbn_bn_set_persistent_steal(3) == 0
+    assert L.gbn_bn_set_persistent_steal(prev) == 1         # nonzero stored as 1
+
+
 def test_bn_persistent_threshold(gbn):
     L = gbn.lib()
     prev = L.gbn_bn_set_persistent_min_bytes(12345)

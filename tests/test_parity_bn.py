@@ -156,21 +156,27 @@ TMEM_CASES = [
 @pytest.mark.parametrize("case", TMEM_CASES, ids=lambda c: c.name)
 def test_bn_persistent_tmem_bit_identical(gbn, case):
     """The persistent kernel with and without its tensor-memory tier (five
-    stages per SM kept in TMEM between the passes) gives the same bits: full
-    bf16 [128,256,56,56], fp32 [256,32,32,32], a range of 16 one-stage
-    channel segments per CTA ([16,2048,8,8]) and a short range
-    ([64,96,28,28]).  Runs on the persistent-everywhere setting only."""
+    stages per SM kept in TMEM between the passes) and its end-of-pass work
+    stealing gives the same bits: full bf16 [128,256,56,56] (where stealing
+    is used), fp32 [256,32,32,32], a range of 16 one-stage channel segments
+    per CTA ([16,2048,8,8]) and a short range ([64,96,28,28]).  Runs on the
+    persistent-everywhere setting only."""
     if gbn.bn_persistent_min_bytes() != 0:
         pytest.skip("checked once, with the persistent kernel taking every shape")
     inp = synth.bn_inputs(case)
     prev = gbn.bn_set_persistent_tmem(False)
+    prev_s = gbn.bn_set_persistent_steal(False)
     try:
-        off = run_gpu(gbn, inp)
+        plain = run_gpu(gbn, inp)
+        gbn.bn_set_persistent_tmem(True)
+        tmem = run_gpu(gbn, inp)
     finally:
         gbn.bn_set_persistent_tmem(prev)
-    on = run_gpu(gbn, inp)
-    for k in on:
-        assert torch.equal(on[k], off[k]), f"{k} differs with the TMEM tier"
+        gbn.bn_set_persistent_steal(prev_s)
+    full = run_gpu(gbn, inp)  # the defaults: TMEM tier and work stealing
+    for k in full:
+        assert torch.equal(tmem[k], plain[k]), f"{k} differs with the TMEM tier"
+        assert torch.equal(full[k], plain[k]), f"{k} differs with work stealing"
 
 
 @pytest.mark.parametrize("name", ["bn_offset_f32", "bn_ragged_f32"])

@@ -543,33 +543,73 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
 // ------------------------------------------------------------ consumers --
 
 // Phase-1 accumulation of one 16-byte vector.  Forward: sum d (d = x - shift)
-// per element in double-fp32 with, for fp32 input, the rounding error of
-// x - shift, so that the channel's sum d is exact to double-fp32 precision
-// (the backward's sum dy*(x - mean) relies on it: a constant dy must give 0);
-// sum d^2 over the vector's lanes in fp32, then one double-fp32 add per
-// vector (its rounding enters the variance only relatively).  Backward: sum
-// dy*d per element in double-fp32 with each product's exact residual and,
-// for fp32 input, the rounding error of x - shift; sum dy likewise for fp32,
-// while ungated bf16 dy is first summed over the vector's four elements per
-// lane in fp32 -- exact for 8-bit significands within 14 binades of each
-// other -- and then added in double-fp32 once per vector.
+// in double-fp32 so that the channel's sum d is exact to double-fp32
+// precision (the backward's sum dy*(x - mean) relies on it: a constant dy
+// must give 0): per element, with the rounding error of x - shift for fp32
+// input; for bf16 input, per vector when that is exact (below), else per
+// element.  Sum d^2 over the vector's lanes in fp32, then one double-fp32
+// add per vector (its rounding enters the variance only relatively).
+// Backward: sum dy*d per element in double-fp32 with each product's exact
+// residual and, for fp32 input, the rounding error of x - shift; sum dy
+// likewise for fp32, while ungated bf16 dy is first summed over the
+// vector's four elements per lane in fp32 -- exact for 8-bit significands
+// within 14 binades of each other -- and then added in double-fp32 once per
+// vector.
+//
+// The bf16 per-vector sum: when the exponents of the eight x and of shift
+// span at most 12 (E_min .. E_max), every value is a multiple of
+// Q = 2^(E_min - 7), each d = x - shift is exact, and every partial sum of
+// up to eight d is a multiple of Q below 2^(E_max + 5) <= 2^24 Q in
+// magnitude, so the fp32 sums of the vector's d are exact too.  smag holds
+// shift's bf16 magnitude bits in both halves.  Zeros and subnormals take
+// the per-element path.
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 template <typename T>
-__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2& a1, DF2& a2) {
+__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2& a1, DF2& a2,
+                                        uint32_t smag) {
   constexpr int NP = Pairs16<T>::NP;
-  f2 p[NP];
+  f2 p[NP], d[NP];
   Pairs16<T>::get(r, p);
   f2 l2 = 0ull;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
-    const f2 d = f2_sub(p[k], sh2);
-    df2_add(a1, d);
-    if constexpr (sizeof(T) == 4) {
-      const f2 bb = f2_sub(d, p[k]);
-      a1.lo = f2_add(a1.lo, f2_add(f2_sub(p[k], f2_sub(d, bb)), f2_sub(nsh2, bb)));
-    }
-    l2 = f2_fma(d, d, l2);
+    d[k] = f2_sub(p[k], sh2);
+    l2 = f2_fma(d[k], d[k], l2);
   }
   df2_add(a2, l2);
+  if constexpr (sizeof(T) == 2) {
+    // magnitudes as bf16x2 (sign cleared), their largest and smallest with
+    // the bf16x2 max / min instructions, folded across the two halves
+    const uint32_t k7 = 0x7fff7fffu;
+    const uint32_t m0 = r.x & k7, m1 = r.y & k7, m2 = r.z & k7, m3 = r.w & k7;
+    uint32_t hi = bf16x2_max(bf16x2_max(m0, m1), bf16x2_max(bf16x2_max(m2, m3), smag));
+    uint32_t lo = bf16x2_min(bf16x2_min(m0, m1), bf16x2_min(bf16x2_min(m2, m3), smag));
+    hi = bf16x2_max(hi, __byte_perm(hi, 0u, 0x1032));
+    lo = bf16x2_min(lo, __byte_perm(lo, 0u, 0x1032));
+    const uint32_t emax = hi & 0x7f80u, emin = lo & 0x7f80u;
+    if (emin != 0u && emax - emin <= (12u << 7)) {
+      df2_add(a1, f2_add(f2_add(d[0], d[1]), f2_add(d[2], d[3])));
+      return;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    df2_add(a1, d[k]);
+    if constexpr (sizeof(T) == 4) {
+      const f2 bb = f2_sub(d[k], p[k]);
+      a1.lo = f2_add(a1.lo, f2_add(f2_sub(p[k], f2_sub(d[k], bb)), f2_sub(nsh2, bb)));
+    }
+  }
 }
 
 // With an activation (ACT), dy is first gated by d act / d pre with
@@ -651,6 +691,9 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
   for (int s = 0; s < sh.nseg; ++s) {
     const float shift = sh.seg_par[s][0];
     const f2 sh2 = f2_splat(shift), nsh2 = f2_splat(-shift);
+    // shift's bf16 magnitude bits (shift is a bf16 value for bf16 input)
+    const uint32_t sm16 = (__float_as_uint(shift) >> 16) & 0x7fffu;
+    const uint32_t smag = sm16 | (sm16 << 16);
     ActPar ap;
     ap.md2 = f2_splat(sh.seg_par[s][1]);
     ap.sc2 = f2_splat(sh.seg_par[s][2]);
@@ -676,7 +719,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
           const uint4 rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
           tmem_st16(ta, rx);
           if constexpr (!BWD) {
-            if (v < len) fwd_acc<T>(rx, sh2, nsh2, a0, a1);
+            if (v < len) fwd_acc<T>(rx, sh2, nsh2, a0, a1, smag);
           } else {
             const uint4 rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
             tmem_st16(ta + 4u, rd);
@@ -692,7 +735,8 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
         }
       } else if constexpr (!BWD) {
         for (int v = ct; v < len; v += kFConsumers)
-          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a0, a1);
+          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a0, a1,
+                     smag);
       } else if (a.act == GBN_ACT_NONE) {
         for (int v = ct; v < len; v += kFConsumers)
           bwd_acc<T, GBN_ACT_NONE>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),

@@ -854,6 +854,8 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
   const float shift = par[0], mean_d = par[1], scale = par[2];
   const float p3 = par[3], p4 = par[4], beta = par[5];
   const float slope = a.slope;
+  const f2 sh2 = f2_splat(shift), md2 = f2_splat(mean_d), sc2 = f2_splat(scale);
+  const f2 p32 = f2_splat(p3), p42 = f2_splat(p4);
   T* out = static_cast<T*>(a.out);
   // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv.
   const int rv = rv0 + ct;
@@ -874,6 +876,29 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
     }
     if (v >= len) continue;
     const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
+    if constexpr (ACT == GBN_ACT_NONE) {
+      // two elements per instruction (fp32x2), the same roundings as the
+      // scalar form below
+      using PK = Pairs16<T>;
+      f2 px[PK::NP];
+      PK::get(rx, px);
+      if constexpr (!BWD) {
+#pragma unroll
+        for (int k = 0; k < PK::NP; ++k)
+          px[k] = f2_fma(f2_sub(f2_sub(px[k], sh2), md2), sc2, p32);
+      } else {
+        f2 pg[PK::NP];
+        PK::get(rd, pg);
+#pragma unroll
+        for (int k = 0; k < PK::NP; ++k)
+          px[k] = f2_fma(pg[k], sc2, f2_fma(f2_sub(f2_sub(px[k], sh2), md2), p32, p42));
+      }
+      const uint4 w = PK::put(px);
+      if (a.stream_out)
+        __stcs(reinterpret_cast<uint4*>(out + gvo * VEC), w);
+      else
+        *reinterpret_cast<uint4*>(out + gvo * VEC) = w;
+    } else {
     float e[VEC];
     V::cvt(rx, e);
     if constexpr (!BWD) {
@@ -896,6 +921,7 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
       store16_cs(out + gvo * VEC, e);
     else
       V::store(out + gvo * VEC, e);
+    }
     pv += a.dp;
     n += a.dn;
     if (pv >= a.Pv) {

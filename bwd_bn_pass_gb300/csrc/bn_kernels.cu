@@ -289,11 +289,28 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   if (threadIdx.x < 32) apply_prologue(g, a, c, j, to_f32(x[(int64_t)c * g.P]), fin);
   __syncthreads();
   const float shift = fin[0], mean_d = fin[1], scale = fin[2], beta = fin[3];
+  // 16-byte vectors without an activation: two elements per instruction
+  // (fp32x2), the same operations and rounding as the scalar form
+  constexpr bool kPacked = sizeof(typename V::raw) == 16;
+  const bool packed = kPacked && a.act == GBN_ACT_NONE;
+  const f2 sh2 = f2_splat(shift), md2 = f2_splat(mean_d), sc2 = f2_splat(scale),
+           be2 = f2_splat(beta);
 
   for (int32_t i = 0; i < cnt; i += kUApply) {
 #pragma unroll
     for (int u = 0; u < kUApply; ++u) {
       if (i + u < cnt) {
+        if constexpr (kPacked) {
+          if (packed) {
+            using PK = Pairs16<T>;
+            f2 p[PK::NP];
+            PK::get(r[u], p);
+#pragma unroll
+            for (int k = 0; k < PK::NP; ++k) p[k] = f2_fma(f2_sub(f2_sub(p[k], sh2), md2), sc2, be2);
+            *reinterpret_cast<uint4*>(y + (size_t)off[u] * VEC) = PK::put(p);
+            continue;
+          }
+        }
         float e[VEC];
         V::cvt(r[u], e);
 #pragma unroll
@@ -487,11 +504,30 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   __syncthreads();
   const float shift = fin[0], mean_d = fin[1], scale = fin[2], k1 = fin[3], k2 = fin[4];
   const float bta = fin[5];
+  // 16-byte vectors without an activation: two elements per instruction
+  // (fp32x2), the same operations and rounding as the scalar form
+  constexpr bool kPacked = sizeof(typename V::raw) == 16;
+  const bool packed = kPacked && act == GBN_ACT_NONE;
+  const f2 sh2 = f2_splat(shift), md2 = f2_splat(mean_d), sc2 = f2_splat(scale),
+           k12 = f2_splat(k1), k22 = f2_splat(k2);
 
   for (int32_t i = 0; i < cnt; i += kUDx) {
 #pragma unroll
     for (int u = 0; u < kUDx; ++u) {
       if (i + u < cnt) {
+        if constexpr (kPacked) {
+          if (packed) {
+            using PK = Pairs16<T>;
+            f2 px[PK::NP], pd[PK::NP];
+            PK::get(rx[u], px);
+            PK::get(rd[u], pd);
+#pragma unroll
+            for (int k = 0; k < PK::NP; ++k)
+              px[k] = f2_fma(pd[k], sc2, f2_fma(f2_sub(f2_sub(px[k], sh2), md2), k12, k22));
+            *reinterpret_cast<uint4*>(dx + (size_t)off[u] * VEC) = PK::put(px);
+            continue;
+          }
+        }
         float ex[VEC], ed[VEC];
         V::cvt(rx[u], ex);
         V::cvt(rd[u], ed);

@@ -115,6 +115,8 @@ struct FArgs {
   int32_t grid_y;
   int32_t G;
   int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
+  int64_t ostep;     // output vector offset step of a thread: dn*C*Pv + dp
+  int64_t owrap;     // added when the in-plane position wraps: C*Pv - Pv
   int32_t l2_window; // phase-1 stages before the TMEM stages kept at normal L2 priority
   int32_t nt;        // stages kept in TMEM between the phases (0: none)
   int32_t pool;      // a CTA's first stages (at most kPoolMax) open to other CTAs in phase 2
@@ -857,10 +859,12 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
   const f2 sh2 = f2_splat(shift), md2 = f2_splat(mean_d), sc2 = f2_splat(scale);
   const f2 p32 = f2_splat(p3), p42 = f2_splat(p4);
   T* out = static_cast<T*>(a.out);
-  // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv.
+  // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv,
+  // and the vector offset gvo = (n*C + c)*Pv + pv, advanced per step.
   const int rv = rv0 + ct;
-  int n = rv / a.Pv;
-  int pv = rv - n * a.Pv;
+  const int n0 = rv / a.Pv;
+  int pv = rv - n0 * a.Pv;
+  int64_t gvo = ((int64_t)n0 * a.C + c) * a.Pv + pv;
   for (int u = 0; u < KV; ++u) {
     const int v = ct + u * kFConsumers;
     if (!in_tmem && v >= len) break;
@@ -875,7 +879,6 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
       if constexpr (BWD) rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
     }
     if (v >= len) continue;
-    const int64_t gvo = ((int64_t)n * a.C + c) * a.Pv + pv;
     if constexpr (ACT == GBN_ACT_NONE) {
       // two elements per instruction (fp32x2), the same roundings as the
       // scalar form below
@@ -923,10 +926,10 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
       V::store(out + gvo * VEC, e);
     }
     pv += a.dp;
-    n += a.dn;
+    gvo += a.ostep;
     if (pv >= a.Pv) {
       pv -= a.Pv;
-      ++n;
+      gvo += a.owrap;
     }
   }
 }
@@ -1167,6 +1170,8 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
   a.G = p.G;
   a.dn = (int32_t)(kFConsumers / p.Pv);
   a.dp = (int32_t)(kFConsumers % p.Pv);
+  a.ostep = (int64_t)a.dn * p.C * p.Pv + a.dp;
+  a.owrap = p.C * p.Pv - p.Pv;
   a.l2_window = p.l2_window;
   a.nt = p.tmem_stages;
   a.stream_out = p.stream_out ? 1 : 0;

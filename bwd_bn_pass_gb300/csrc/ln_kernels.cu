@@ -322,9 +322,19 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
 
     const float inv_H = 1.f / (float)H;
     bool failed = false;
-    for (int64_t i = grp; i < nmine; i += NGRP) {
-      const int s = (int)(i % NS);
-      const uint32_t par = (uint32_t)((i / NS) & 1);
+    // ring slot s = i mod NS, its phase parity and this group's slot buffer
+    // (i / NGRP) & 1, advanced per stage (no 64-bit division in the loop)
+    int s = grp % NS;
+    uint32_t par = (uint32_t)((grp / NS) & 1);
+    int buf = 0;
+    for (int64_t i = grp; i < nmine; i += NGRP, buf ^= 1) {
+      if (i != grp) {
+        s += NGRP;
+        while (s >= NS) {
+          s -= NS;
+          par ^= 1u;
+        }
+      }
       const int64_t r0 = (g + i * G) * RB;
       const int nr = (int)(a.R - r0 < RB ? a.R - r0 : RB);
       float mu[RPS], rho[RPS];
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
       // Row sums of g and g*xhat of the stage's rows: per warp into the
       // group's slots [buffer][row][sum][warp], double-buffered by stage.
       // bf16 outputs keep xhat and the keep factors for the second pass.
-      float* slot = red + ((grp * 2 + (int)((i / NGRP) & 1)) * RB) * 2 * P;
+      float* slot = red + ((grp * 2 + buf) * RB) * 2 * P;
       f2 xhs[COMP ? 1 : RPS][KV][NP], kps[COMP ? 1 : RPS][KV][NP];
       float rsum[RPS][2];
 #pragma unroll

@@ -138,9 +138,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
     const float Hf = (float)a.H;
     bool failed = false;
     int64_t i = 0;
-    for (; i < nmine; ++i) {
-      const int s = (int)(i % NS);
-      const uint32_t par = (uint32_t)((i / NS) & 1);
+    // ring slot s = i mod NS and lap = i / NS, advanced per stage (no
+    // 64-bit division in the loop); the slot's phase parity is lap & 1
+    int s = 0;
+    uint32_t lap = 0;
+    for (; i < nmine; ++i, ring_advance(s, lap, NS)) {
+      const uint32_t par = lap & 1u;
       const int64_t r0 = (g + i * G) * RB;
       const int nr = (int)(a.R - r0 < RB ? a.R - r0 : RB);
       float rho[RB];

@@ -85,15 +85,24 @@ __device__ __forceinline__ void ring_abort(RowShared& sh, int* status) {
   }
 }
 
+// Next ring slot: s = i mod NS and lap = i / NS for i + 1.
+__device__ __forceinline__ void ring_advance(int& s, uint32_t& lap, int NS) {
+  if (++s == NS) {
+    s = 0;
+    ++lap;
+  }
+}
+
 // The producer (one lane): stage i of this CTA goes to slot i % NS once the
 // slot's previous stage has been released.  issue(i, slot) posts the stage's
 // expect_tx and bulk copies on sh.full[slot].
 template <typename IssueFn>
 __device__ void ring_produce(RowShared& sh, int NS, int64_t nmine, int* status, IssueFn issue) {
-  for (int64_t i = 0; i < nmine; ++i) {
-    const int s = (int)(i % NS);
+  int s = 0;         // i mod NS
+  uint32_t lap = 0;  // i / NS (no 64-bit division in the loop)
+  for (int64_t i = 0; i < nmine; ++i, ring_advance(s, lap, NS)) {
     if (i >= NS) {
-      if (!ring_wait(&sh.empty[s], (uint32_t)(((i / NS) - 1) & 1), &sh.abort)) {
+      if (!ring_wait(&sh.empty[s], (lap - 1u) & 1u, &sh.abort)) {
         ring_abort(sh, status);
         return;
       }

@@ -85,6 +85,20 @@ constexpr int kStealBatch = 2;    // pool stages taken per claim, at most
 constexpr int kMaxCtas = 160;     // CTAs of a launch, at most (one per SM)
 constexpr int kPoolMinStages = 16;  // reloaded stages per CTA from which the pool is used
 
+// n / d for 0 <= n < 2^31 by a precomputed multiplier (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994,
+// unsigned division with a 33-bit multiplier): q = (t + ((n - t) >> 1)) >>
+// (l - 1) with t = mulhi(m, n), l = ceil(log2 d), m = floor(2^32 (2^l - d) /
+// d) + 1; d = 1 is the identity (m = 0, shifts 0 and 0 with l = 0 handled
+// by sh1 = 0).
+struct FastDiv {
+  uint32_t d, m, sh1, sh2;
+};
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.sh1)) >> f.sh2;
+}
+
 struct FArgs {
   const void* x;
   const void* dy;        // backward
@@ -115,6 +129,7 @@ struct FArgs {
   int32_t grid_y;
   int32_t G;
   int32_t dn, dp;    // kFConsumers / Pv, kFConsumers % Pv
+  FastDiv pdiv;      // division by Pv
   int64_t ostep;     // output vector offset step of a thread: dn*C*Pv + dp
   int64_t owrap;     // added when the in-plane position wraps: C*Pv - Pv
   int32_t l2_window; // phase-1 stages before the TMEM stages kept at normal L2 priority
@@ -280,6 +295,11 @@ __device__ __forceinline__ int stages_in(const FShared& sh, const FArgs& a, int 
   return (sh.seg_len[s] + a.stage_v - 1) / a.stage_v;
 }
 
+// Ring slots walked forward and backward without a division per stage.
+__device__ __forceinline__ int slot_next(int s, int NS) { return s + 1 == NS ? 0 : s + 1; }
+__device__ __forceinline__ int slot_prev(int s, int NS) { return s == 0 ? NS - 1 : s - 1; }
+
+
 // Stage j (phase-1 numbering) of CTA v's range: its channel c, first vector
 // rv0 inside the channel, length and segment index -- the segments computed
 // the way the kernel's set-up computes its own.
@@ -334,8 +354,8 @@ __device__ void issue_stage(const FArgs& a, FShared& sh, unsigned char* ring, in
     sh.issued[slot] += 1;
   }
   __syncwarp();
-  const int n0 = rv0 / a.Pv;
-  const int nruns = (rv0 + len - 1) / a.Pv - n0 + 1;
+  const int n0 = (int)fast_div((uint32_t)rv0, a.pdiv);
+  const int nruns = (int)fast_div((uint32_t)(rv0 + len - 1), a.pdiv) - n0 + 1;
   for (int r = lane; r < nruns; r += 32) {
     const int n = n0 + r;
     const int b = max(rv0, n * a.Pv), e = min(rv0 + len, (n + 1) * a.Pv);
@@ -374,11 +394,10 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
   const int keep_lo = sh.t_lo - a.l2_window, keep_hi = sh.t_lo;  // phase-1 stages kept in L2
   uint32_t epar = 0;  // parity of the next "empty" completion per slot
   // Phase 1: forward.  A slot is refilled once its previous stage is released.
-  int i = 0;
+  int i = 0, slot = 0;  // slot = i mod NS
   for (int s = 0; s < sh.nseg; ++s) {
     const int nq = stages_in(sh, a, s);
-    for (int q = 0; q < nq; ++q, ++i) {
-      const int slot = i % NS;
+    for (int q = 0; q < nq; ++q, ++i, slot = slot_next(slot, NS)) {
       if (i >= NS && !producer_wait_empty(sh, slot, epar, a.status)) return;
       if (__any_sync(0xffffffffu, sh.abort != 0)) return;
       int rv0, len;
@@ -397,9 +416,9 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
   // takes hi - 1 by subtracting 1 << 16, another CTA takes lo by adding 1,
   // and the atomic order decides every stage exactly once.
   const int lane = threadIdx.x & 31;
-  int j = 0;
+  int j = 0, pslot = (N1 - 1) % NS;  // pslot = (N1 - 1 - j) mod NS
   auto push = [&](int c, int rv0, int len, const float* par, bool end) -> bool {
-    const int slot = ((N1 - 1 - j) % NS + NS) % NS;
+    const int slot = pslot;
     if (sh.issued[slot] > 0 && !producer_wait_empty(sh, slot, epar, a.status)) return false;
     if (__any_sync(0xffffffffu, sh.abort != 0)) return false;
     if (lane == 0) {
@@ -421,6 +440,7 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
       issue_stage<T, BWD>(a, sh, ring, slot, c, rv0, len, drop);
     }
     ++j;
+    pslot = slot_prev(pslot, NS);
     return true;
   };
   // this CTA's stages below the on-chip ones, down to the pool
@@ -689,7 +709,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
   // TMEM stages: KV vector slots per thread and input, cps columns a stage.
   const int KV = a.stage_v / kFConsumers, cps = KV * (BWD ? 8 : 4);
   const uint32_t tbase = tmem_thread_base(sh.tmem, ct >> 5);
-  int i = 0;
+  int i = 0, slot = 0;  // slot = i mod NS
   for (int s = 0; s < sh.nseg; ++s) {
     const float shift = sh.seg_par[s][0];
     const f2 sh2 = f2_splat(shift), nsh2 = f2_splat(-shift);
@@ -704,8 +724,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
     ap.slope = a.slope;
     DF2 a0{0ull, 0ull}, a1{0ull, 0ull};
     const int nq = stages_in(sh, a, s);
-    for (int q = 0; q < nq; ++q, ++i) {
-      const int slot = i % NS;
+    for (int q = 0; q < nq; ++q, ++i, slot = slot_next(slot, NS)) {
       if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
       if (i == 0 && ct == 0) GBN_RING_TRACE(1);
       int rv0, len;
@@ -862,7 +881,7 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
   // Output position of vector v = ct, ct + 512, ...: plane n, in-plane pv,
   // and the vector offset gvo = (n*C + c)*Pv + pv, advanced per step.
   const int rv = rv0 + ct;
-  const int n0 = rv / a.Pv;
+  const int n0 = (int)fast_div((uint32_t)rv, a.pdiv);
   int pv = rv - n0 * a.Pv;
   int64_t gvo = ((int64_t)n0 * a.C + c) * a.Pv + pv;
   for (int u = 0; u < KV; ++u) {
@@ -965,14 +984,13 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
   if (ct == 0) sh.p2ready = 1;
   // The on-chip stages: the resident tail (released afterwards, the
   // producer refills those slots) and the TMEM stages.
-  int q2 = 0;
+  int q2 = 0, slot = (N1 - 1) % NS;  // slot = i mod NS of stage i = N1 - 1 - q2
   for (int s = sh.nseg - 1; s >= 0; --s) {
     const int nq = stages_in(sh, a, s);
-    for (int q = nq - 1; q >= 0; --q, ++q2) {
+    for (int q = nq - 1; q >= 0; --q, ++q2, slot = slot_prev(slot, NS)) {
       const int i = N1 - 1 - q2;  // the stage's index in phase 1
       if (i < sh.t_lo) continue;
       if (__any_sync(0xffffffffu, sh.abort != 0)) continue;
-      const int slot = i % NS;
       const bool in_tmem = i < sh.t_hi;
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
@@ -985,9 +1003,10 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
       }
     }
   }
-  // Then what the producer loads, in its push order, until its end marker.
-  for (int j = 0;; ++j) {
-    const int slot = ((N1 - 1 - j) % NS + NS) % NS;
+  // Then what the producer loads, in its push order, until its end marker
+  // (push j in slot (N1 - 1 - j) mod NS).
+  slot = (N1 - 1) % NS;
+  for (int j = 0;; ++j, slot = slot_prev(slot, NS)) {
     if (!warp_wait_full(sh, slot, fpar, a.status)) break;
     const FDesc& d = sh.desc[slot];
     if (d.end) break;
@@ -1138,6 +1157,18 @@ cudaError_t launch_fused(const FArgs& a, const BnFusedPlan& p, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, bn_fused_kernel<T, BWD>, a);
 }
 
+// Multiplier and shifts of FastDiv for a divisor d >= 1.
+FastDiv make_fast_div(uint32_t d) {
+  FastDiv f{d, 0u, 0u, 0u};
+  if (d <= 1) return f;  // n / 1: t = 0, (0 + n) >> 0 >> 0
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+  f.sh1 = 1;
+  f.sh2 = l - 1;
+  return f;
+}
+
 // Workspace of the persistent kernel: the epoch pair and a flag pair per CTA
 // (16 bytes each), the pool words (4 bytes per CTA), the publish flags (8
 // bytes per CTA), the published parameters (kPoolMax x kPubFloats floats per
@@ -1171,6 +1202,7 @@ FArgs make_args(const BnFusedPlan& p, void* ws) {
   a.dn = (int32_t)(kFConsumers / p.Pv);
   a.dp = (int32_t)(kFConsumers % p.Pv);
   a.ostep = (int64_t)a.dn * p.C * p.Pv + a.dp;
+  a.pdiv = make_fast_div((uint32_t)p.Pv);
   a.owrap = p.C * p.Pv - p.Pv;
   a.l2_window = p.l2_window;
   a.nt = p.tmem_stages;

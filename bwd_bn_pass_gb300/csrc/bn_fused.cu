@@ -85,19 +85,6 @@ constexpr int kStealBatch = 2;    // pool stages taken per claim, at most
 constexpr int kMaxCtas = 160;     // CTAs of a launch, at most (one per SM)
 constexpr int kPoolMinStages = 16;  // reloaded stages per CTA from which the pool is used
 
-// n / d for 0 <= n < 2^31 by a precomputed multiplier (Granlund and
-// Montgomery, "Division by invariant integers using multiplication", 1994,
-// unsigned division with a 33-bit multiplier): q = (t + ((n - t) >> 1)) >>
-// (l - 1) with t = mulhi(m, n), l = ceil(log2 d), m = floor(2^32 (2^l - d) /
-// d) + 1; d = 1 is the identity (m = 0, shifts 0 and 0 with l = 0 handled
-// by sh1 = 0).
-struct FastDiv {
-  uint32_t d, m, sh1, sh2;
-};
-__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
-  const uint32_t t = __umulhi(f.m, n);
-  return (t + ((n - t) >> f.sh1)) >> f.sh2;
-}
 
 struct FArgs {
   const void* x;
@@ -1157,17 +1144,6 @@ cudaError_t launch_fused(const FArgs& a, const BnFusedPlan& p, cudaStream_t st) 
   return cudaLaunchKernelEx(&cfg, bn_fused_kernel<T, BWD>, a);
 }
 
-// Multiplier and shifts of FastDiv for a divisor d >= 1.
-FastDiv make_fast_div(uint32_t d) {
-  FastDiv f{d, 0u, 0u, 0u};
-  if (d <= 1) return f;  // n / 1: t = 0, (0 + n) >> 0 >> 0
-  uint32_t l = 0;
-  while ((1ull << l) < d) ++l;
-  f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
-  f.sh1 = 1;
-  f.sh2 = l - 1;
-  return f;
-}
 
 // Workspace of the persistent kernel: the epoch pair and a flag pair per CTA
 // (16 bytes each), the pool words (4 bytes per CTA), the publish flags (8

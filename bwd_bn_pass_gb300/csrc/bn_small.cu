@@ -45,8 +45,8 @@ __device__ __forceinline__ void shifted(float e, float shift, float& d, float& d
 // Loads per thread issued together: a whole channel (kBnSmallMaxM / 256).
 constexpr int kSmallBatch = (int)(kBnSmallMaxM / kSmallThreads);
 
-__device__ __forceinline__ int64_t elem_offset(int m, int C, int c, int P) {
-  const int n = m / P;
+__device__ __forceinline__ int64_t elem_offset(int m, int C, int c, int P, const FastDiv& pd) {
+  const int n = (int)fast_div((uint32_t)m, pd);
   return ((int64_t)n * C + c) * P + (m - n * P);
 }
 
@@ -57,7 +57,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     bn_small_fwd_kernel(const T* __restrict__ x, T* __restrict__ y, int B, int C, int P,
                         const float* __restrict__ gamma, const float* __restrict__ beta,
                         float* __restrict__ stats, float* running_mean, float* running_var,
-                        float momentum, float eps, float Mh, float Ml, int act, float slope) {
+                        float momentum, float eps, float Mh, float Ml, int act, float slope,
+                        FastDiv pd) {
   extern __shared__ float vals[];
   __shared__ float2 red[64];
   const int c = blockIdx.x, t = threadIdx.x, M = B * P;
@@ -68,7 +69,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 #pragma unroll
     for (int u = 0; u < kSmallBatch; ++u) {
       const int m = m0 + u * kSmallThreads;
-      v[u] = m < M ? to_f32(x[elem_offset(m, C, c, P)]) : 0.f;
+      v[u] = m < M ? to_f32(x[elem_offset(m, C, c, P, pd)]) : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < kSmallBatch; ++u) {
@@ -89,7 +90,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     bn_fwd_write(f, shift, C, c, Mh + Ml, stats, running_mean, running_var, momentum);
   const float b = beta ? beta[c] : 0.f, mean_d = f.md.hi, scale = f.scale;
   for (int m = t; m < M; m += kSmallThreads)
-    y[elem_offset(m, C, c, P)] =
+    y[elem_offset(m, C, c, P, pd)] =
         from_f32<T>(act_out(fmaf((vals[m] - shift) - mean_d, scale, b), act, slope));
 }
 
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     bn_small_bwd_kernel(const T* __restrict__ x, const T* __restrict__ dy, T* __restrict__ dx,
                         int B, int C, int P, const float* __restrict__ stats,
                         const float* __restrict__ beta, float* __restrict__ grads, float Mf,
-                        int act, float slope) {
+                        int act, float slope, FastDiv pd) {
   extern __shared__ float vals[];  // [2][M]: x, then the gated dy
   __shared__ float2 red[64];
   const int c = blockIdx.x, t = threadIdx.x, M = B * P;
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 #pragma unroll
     for (int u = 0; u < kSmallBatch; ++u) {
       const int m = m0 + u * kSmallThreads;
-      const int64_t o = m < M ? elem_offset(m, C, c, P) : 0;
+      const int64_t o = m < M ? elem_offset(m, C, c, P, pd) : 0;
       xv[u] = m < M ? to_f32(x[o]) : 0.f;
       gv[u] = m < M ? to_f32(dy[o]) : 0.f;
     }
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   }
   for (int m = t; m < M; m += kSmallThreads) {
     const float xc = (vals[m] - shift) - mean_d;
-    dx[elem_offset(m, C, c, P)] = from_f32<T>(fmaf(vals[M + m], scale, fmaf(xc, f.k1, f.k2)));
+    dx[elem_offset(m, C, c, P, pd)] = from_f32<T>(fmaf(vals[M + m], scale, fmaf(xc, f.k1, f.k2)));
   }
 }
 
@@ -157,7 +158,7 @@ cudaError_t small_fwd(const void* x, void* y, int64_t B, int64_t C, int64_t HW, 
   return launch(bn_small_fwd_kernel<T>, dim3((unsigned)C), dim3(kSmallThreads),
                 (size_t)M * sizeof(float), st, false, static_cast<const T*>(x),
                 static_cast<T*>(y), (int)B, (int)C, (int)HW, gamma, beta, stats, running_mean,
-                running_var, momentum, eps, Mh, Ml, act, slope);
+                running_var, momentum, eps, Mh, Ml, act, slope, make_fast_div((uint32_t)HW));
 }
 
 template <typename T>
@@ -168,7 +169,7 @@ cudaError_t small_bwd(const void* x, const void* dy, void* dx, int64_t B, int64_
   return launch(bn_small_bwd_kernel<T>, dim3((unsigned)C), dim3(kSmallThreads),
                 2 * (size_t)M * sizeof(float), st, false, static_cast<const T*>(x),
                 static_cast<const T*>(dy), static_cast<T*>(dx), (int)B, (int)C, (int)HW, stats,
-                beta, grads, (float)M, act, slope);
+                beta, grads, (float)M, act, slope, make_fast_div((uint32_t)HW));
 }
 
 }  // namespace

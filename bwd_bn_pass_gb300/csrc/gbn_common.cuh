@@ -36,6 +36,32 @@ template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
 
+// n / d for 0 <= n < 2^31 by a precomputed multiplier (Granlund and
+// Montgomery, "Division by invariant integers using multiplication", 1994,
+// unsigned division with a 33-bit multiplier): q = (t + ((n - t) >> 1)) >>
+// (l - 1) with t = mulhi(m, n), l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1.  For d = 1, m = 0 and both shifts are
+// 0, so q = n.  A few integer instructions instead of the division routine.
+struct FastDiv {
+  uint32_t d, m, sh1, sh2;
+};
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.sh1)) >> f.sh2;
+}
+
+// Multiplier and shifts of FastDiv for a divisor d >= 1.
+inline FastDiv make_fast_div(uint32_t d) {
+  FastDiv f{d, 0u, 0u, 0u};
+  if (d <= 1) return f;  // n / 1: t = 0, (0 + n) >> 0 >> 0
+  uint32_t l = 0;
+  while ((1ull << l) < d) ++l;
+  f.m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+  f.sh1 = 1;
+  f.sh2 = l - 1;
+  return f;
+}
+
 // VEC elements of T moved as one raw word group (VEC*sizeof(T) bytes, a
 // power of two <= 16) and converted to fp32 only when used, so a thread can
 // keep several vectors in flight in few registers.  bf16 element 0 sits in

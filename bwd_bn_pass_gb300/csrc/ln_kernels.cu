@@ -576,13 +576,11 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
         }
         consumers_bar(NC);
       }
-      const int64_t n4 = (int64_t)nout * nplanes * H / 4;
-      for (int64_t v = ct; v < n4; v += NC) {
-        const int64_t e = v * 4;
-        const int64_t op = e / H, h = e - op * H;  // op = o * nplanes + plane
-        *reinterpret_cast<float4*>(a.part + (op * G + g) * H + h) =
-            *reinterpret_cast<const float4*>(sm + e);
-      }
+      const int64_t H4 = H / 4;  // H is a multiple of 8
+      for (int op = 0; op < nout * nplanes; ++op)  // op = o * nplanes + plane
+        for (int64_t v = ct; v < H4; v += NC)
+          *reinterpret_cast<float4*>(a.part + ((int64_t)op * G + g) * H + v * 4) =
+              *reinterpret_cast<const float4*>(sm + (int64_t)op * H + v * 4);
       if (ct == 0) GBN_RING_TRACE(3);
       if (ring_exchange(sh, a.sync, G, ct, NC, a.status, a.nonce)) {
         if (ct == 0) GBN_RING_TRACE(4);

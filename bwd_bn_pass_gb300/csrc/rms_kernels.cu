@@ -135,7 +135,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
 #pragma unroll
       for (int p = 0; p < NP; ++p) { acc[k][p] = 0ull; acc_lo[k][p] = 0ull; }
     }
-    const float Hf = (float)a.H;
+    const float invH = 1.f / (float)a.H;  // one rounding more than / H, no division per row
     bool failed = false;
     int64_t i = 0;
     // ring slot s = i mod NS and lap = i / NS, advanced per stage (no
@@ -184,14 +184,18 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
         if constexpr (EARLY) return dr[rr][k];
         else return vec(rr, k, true);
       };
-      // Row sums S = sum_j w_j dy_j x_j (two lanes per instruction).
+      // Row sums S = sum_j w_j dy_j x_j (two lanes per instruction); with
+      // EARLY the unpacked pairs stay in registers for the second pass
+      // (the other instances would spill and unpack again).
       float* slot = &red[i & 1][0][0];
+      f2 xs[EARLY ? RB : 1][KV][NP], ds[EARLY ? RB : 1][KV][NP];
 #pragma unroll
       for (int rr = 0; rr < RB; ++rr) {
         f2 part = 0ull;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-          f2 x2[NP], d2[NP];
+          f2 (&x2)[NP] = xs[EARLY ? rr : 0][k];
+          f2 (&d2)[NP] = ds[EARLY ? rr : 0][k];
           PK::get(getx(rr, k), x2);
           PK::get(getd(rr, k), d2);
 #pragma unroll
@@ -208,7 +212,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
       for (int rr = 0; rr < RB; ++rr) {
         if (rr >= nr) break;
         const float S = sum_slots<NCW>(slot + rr * NCW);
-        const float coef = rho[rr] * rho[rr] * rho[rr] * S / Hf;
+        const float coef = rho[rr] * rho[rr] * rho[rr] * S * invH;
         const f2 rho2 = f2_splat(rho[rr]);
         const f2 ncoef2 = f2_splat(-coef);
         T* dxr = static_cast<T*>(a.dx) + (r0 + rr) * (int64_t)a.H;
@@ -216,9 +220,13 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) rms_bwd_ring_kernel(RmsArgs
         for (int k = 0; k < KV; ++k) {
           const int vi = ct + k * NC;
           if (vi >= a.Hv) continue;
-          f2 x2[NP], d2[NP], o2[NP];
-          PK::get(getx(rr, k), x2);
-          PK::get(getd(rr, k), d2);
+          f2 (&x2)[NP] = xs[EARLY ? rr : 0][k];
+          f2 (&d2)[NP] = ds[EARLY ? rr : 0][k];
+          if constexpr (!EARLY) {
+            PK::get(getx(rr, k), x2);
+            PK::get(getd(rr, k), d2);
+          }
+          f2 o2[NP];
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
             // dx = rstd*w*dy - x*rstd^3*S/H

@@ -141,9 +141,15 @@ __device__ void colsum_warps(const float* __restrict__ part, int nout, int G, in
   const int64_t u0 = (int64_t)cta * U / ncta, u1 = (int64_t)(cta + 1) * U / ncta;
   const int nplanes = COMP ? 2 : 1;
   const int half = lane & 1, r0 = lane >> 1;
-  for (int64_t u = u0 + cw; u < u1; u += ncw) {
-    const int o = (int)(u / H8);
-    const int64_t j = (u - (int64_t)o * H8) * 8 + 4 * half;
+  // u = o * H8 + jg, advanced without a division per group
+  int o = (int)((u0 + cw) / H8);
+  int64_t jg = (u0 + cw) - (int64_t)o * H8;
+  for (int64_t u = u0 + cw; u < u1; u += ncw, jg += ncw) {
+    while (jg >= H8) {
+      jg -= H8;
+      ++o;
+    }
+    const int64_t j = jg * 8 + 4 * half;
     const float* hi = part + (int64_t)o * nplanes * G * H + j;
     const float* lo = hi + (int64_t)G * H;
     DF acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};

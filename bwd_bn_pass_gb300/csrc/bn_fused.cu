@@ -584,7 +584,7 @@ __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
 }
 
 template <typename T>
-__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2& a1, DF2& a2,
+__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2 (&a1)[2], DF2& a2,
                                         uint32_t smag) {
   constexpr int NP = Pairs16<T>::NP;
   f2 p[NP], d[NP];
@@ -607,16 +607,18 @@ __device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2& a1, DF2& 
     lo = bf16x2_min(lo, __byte_perm(lo, 0u, 0x1032));
     const uint32_t emax = hi & 0x7f80u, emin = lo & 0x7f80u;
     if (emin != 0u && emax - emin <= (12u << 7)) {
-      df2_add(a1, f2_add(f2_add(d[0], d[1]), f2_add(d[2], d[3])));
+      df2_add(a1[0], f2_add(f2_add(d[0], d[1]), f2_add(d[2], d[3])));
       return;
     }
   }
+  // alternate pairs feed two accumulators (two dependency chains)
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
-    df2_add(a1, d[k]);
+    DF2& acc = a1[k & 1];
+    df2_add(acc, d[k]);
     if constexpr (sizeof(T) == 4) {
       const f2 bb = f2_sub(d[k], p[k]);
-      a1.lo = f2_add(a1.lo, f2_add(f2_sub(p[k], f2_sub(d[k], bb)), f2_sub(nsh2, bb)));
+      acc.lo = f2_add(acc.lo, f2_add(f2_sub(p[k], f2_sub(d[k], bb)), f2_sub(nsh2, bb)));
     }
   }
 }
@@ -633,7 +635,7 @@ struct ActPar {
 // exact, so its per-vector sum stays exact too; a LeakyReLU gate rounds.
 template <typename T, int ACT>
 __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, const ActPar& ap,
-                                        DF2& a0, DF2& a1) {
+                                        DF2& a0, DF2 (&a1)[2]) {
   constexpr int NP = Pairs16<T>::NP;
   f2 px[NP], pd[NP];
   Pairs16<T>::get(rx, px);
@@ -652,14 +654,17 @@ __device__ __forceinline__ void bwd_acc(uint4 rx, uint4 rd, f2 sh2, f2 nsh2, con
       l0 = f2_add(l0, pd[k]);
     else
       df2_add(a0, pd[k]);
+    // alternate pairs feed two accumulators: two independent dependency
+    // chains per thread
+    DF2& acc = a1[k & 1];
     const f2 prod = f2_mul_rounded(pd[k], d);
-    df2_add(a1, prod);
+    df2_add(acc, prod);
     // exact residual dy*d - prod (the negation flips the sign of both lanes)
-    a1.lo = f2_add(a1.lo, f2_fma(pd[k], d, prod ^ 0x8000000080000000ull));
+    acc.lo = f2_add(acc.lo, f2_fma(pd[k], d, prod ^ 0x8000000080000000ull));
     if constexpr (sizeof(T) == 4) {
       const f2 bb = f2_sub(d, px[k]);
       const f2 d_lo = f2_add(f2_sub(px[k], f2_sub(d, bb)), f2_sub(nsh2, bb));
-      a1.lo = f2_fma(pd[k], d_lo, a1.lo);
+      acc.lo = f2_fma(pd[k], d_lo, acc.lo);
     }
   }
   if constexpr (kLocalDy) df2_add(a0, l0);
@@ -709,7 +714,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
     ap.be2 = f2_splat(sh.seg_par[s][5]);
     ap.act = a.act;
     ap.slope = a.slope;
-    DF2 a0{0ull, 0ull}, a1{0ull, 0ull};
+    DF2 a0{0ull, 0ull}, a1[2] = {{0ull, 0ull}, {0ull, 0ull}};  // see the fold below
     const int nq = stages_in(sh, a, s);
     for (int q = 0; q < nq; ++q, ++i, slot = slot_next(slot, NS)) {
       if (!warp_wait_full(sh, slot, fpar, a.status)) continue;
@@ -727,7 +732,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
           const uint4 rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
           tmem_st16(ta, rx);
           if constexpr (!BWD) {
-            if (v < len) fwd_acc<T>(rx, sh2, nsh2, a0, a1, smag);
+            if (v < len) fwd_acc<T>(rx, sh2, nsh2, a1, a0, smag);
           } else {
             const uint4 rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
             tmem_st16(ta + 4u, rd);
@@ -743,7 +748,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
         }
       } else if constexpr (!BWD) {
         for (int v = ct; v < len; v += kFConsumers)
-          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a0, a1,
+          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a1, a0,
                      smag);
       } else if (a.act == GBN_ACT_NONE) {
         for (int v = ct; v < len; v += kFConsumers)
@@ -769,7 +774,9 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
         if (lane == 0) mbar_arrive(&sh.empty[slot]);
       }
     }
-    DF s0 = df2_fold(a0), s1 = df2_fold(a1);
+    // forward: a1 holds sum d, a0 sum d^2; backward: a0 sum dy, a1 sum dy*d
+    const DF sa = df_sum(df2_fold(a1[0]), df2_fold(a1[1]));
+    DF s0 = BWD ? df2_fold(a0) : sa, s1 = BWD ? sa : df2_fold(a0);
     consumers_sum2(sh, s0, s1);
     if (ct == 0 && !sh.abort) {
       const int j = (int)blockIdx.x - sh.seg_klo[s];

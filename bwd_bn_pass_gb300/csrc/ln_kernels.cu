@@ -322,6 +322,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
 
     const float inv_H = 1.f / (float)H;
     bool failed = false;
+
     // ring slot s = i mod NS, its phase parity and this group's slot buffer
     // (i / NGRP) & 1, advanced per stage (no 64-bit division in the loop)
     int s = grp % NS;
@@ -349,20 +350,23 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
       // This thread's vectors of its rows, into registers; then the stage is
       // released so that the producer can refill it while we compute.
       const unsigned char* st = data + (size_t)s * a.stage_bytes;
+      // Loads without a select: a lane past the row's end reads the row's
+      // last vector (its gamma and bias are 0, so it adds nothing to the row
+      // sums and it stores nothing), and a row past the stage's last
+      // (rr >= nr) reads the slot's stale bytes, which no output uses.
       uint4 rdy[RPS][KV], rx[RPS][KV], rres[RPS][KV];
       MaskRaw rmk[RPS][KV];
 #pragma unroll
       for (int q = 0; q < RPS; ++q)
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-          const int rr = q, vi = lr + k * TPR;
-          const bool in = ok && rr < nr && vi < a.Hv;
+          const int rr = q, vi = min(lr + k * TPR, a.Hv - 1);  // clamped to the row
           const size_t o = (size_t)rr * rowb + (size_t)vi * 16;
-          rdy[q][k] = in ? *reinterpret_cast<const uint4*>(st + a.off_dy + o) : make_uint4(0u, 0u, 0u, 0u);
-          rx[q][k] = in ? *reinterpret_cast<const uint4*>(st + a.off_x + o) : make_uint4(0u, 0u, 0u, 0u);
-          rres[q][k] = (in && with_res) ? *reinterpret_cast<const uint4*>(st + a.off_res + o)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-          if (in && has_mask)
+          rdy[q][k] = *reinterpret_cast<const uint4*>(st + a.off_dy + o);
+          rx[q][k] = *reinterpret_cast<const uint4*>(st + a.off_x + o);
+          rres[q][k] = with_res ? *reinterpret_cast<const uint4*>(st + a.off_res + o)
+                                : make_uint4(0u, 0u, 0u, 0u);
+          if (has_mask)
             rmk[q][k] = *reinterpret_cast<const MaskRaw*>(st + a.off_mask + (size_t)rr * H +
                                                           (size_t)vi * VE);
           else

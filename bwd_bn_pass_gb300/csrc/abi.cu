@@ -288,6 +288,8 @@ int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes) {
 
 int64_t gbn_bn_persistent_min_bytes(void) { return g_fused_min_bytes.load(); }
 
+int64_t gbn_bn_small_max_elems(void) { return g_small_max_m.load(); }
+
 int64_t gbn_bn_set_small_max_elems(int64_t m) {
   if (m < 0) m = 0;
   if (m > kBnSmallMaxM) m = kBnSmallMaxM;

@@ -62,6 +62,7 @@ _SIGNATURES = {
     "gbn_bn_workspace_bytes": (_SZ, [_I64, _I64, _I64, _INT]),
     "gbn_bn_set_persistent_min_bytes": (_I64, [_I64]),
     "gbn_bn_set_small_max_elems": (_I64, [_I64]),
+    "gbn_bn_small_max_elems": (_I64, []),
     "gbn_bn_persistent_min_bytes": (_I64, []),
     "gbn_bn_set_wide_offsets": (_INT, [_INT]),
     "gbn_bn_set_persistent_tmem": (_INT, [_INT]),
@@ -221,6 +222,10 @@ def bn_set_small_max_elems(m):
 
 def bn_persistent_min_bytes():
     return lib().gbn_bn_persistent_min_bytes()
+
+
+def bn_small_max_elems():
+    return lib().gbn_bn_small_max_elems()
 
 
 def bn_set_persistent_tmem(enable):

@@ -175,6 +175,8 @@ GBN_API int64_t gbn_bn_persistent_min_bytes(void);
  * the parity tolerance of the other paths.  Process-wide; returns the
  * previous value.  The pages have no counterpart: a tuning knob.           */
 GBN_API int64_t gbn_bn_set_small_max_elems(int64_t m);
+/* The current limit (elements per channel).                               */
+GBN_API int64_t gbn_bn_small_max_elems(void);
 
 /* The persistent BatchNorm kernel keeps a few stages per SM in tensor
  * memory (TMEM) between its reduction and output passes, instead of loading

@@ -178,6 +178,7 @@ def test_bn_nhwc_argument_errors(gbn):
 def test_bn_small_channel_switch(gbn):
     L = gbn.lib()
     prev = L.gbn_bn_set_small_max_elems(100)
+    assert L.gbn_bn_small_max_elems() == 100
     assert L.gbn_bn_set_small_max_elems(-5) == 100
     assert L.gbn_bn_set_small_max_elems(1 << 40) == 0      # negative stored as 0
     assert L.gbn_bn_set_small_max_elems(prev) == 2048      # capped at the kernels' limit

@@ -264,6 +264,24 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, uint4& a, 
       : "r"(ta), "r"(tb)
       : "memory");
 }
+// 24 consecutive columns of this thread's lane (three 8-column loads, each
+// at a multiple of 8 columns like every other access here), then one wait:
+// a whole TMEM stage of a thread on the device's stage size (6 vectors of x
+// forward, 3 of x and dy backward).
+__device__ __forceinline__ void tmem_ld24(uint32_t ta, uint32_t (&r)[24]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%24];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%25];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%26];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+      : "r"(ta), "r"(ta + 8u), "r"(ta + 16u)
+      : "memory");
+}
+
 // This consumer thread's first TMEM column address (consumer warp cw).
 __device__ __forceinline__ uint32_t tmem_thread_base(uint32_t tmem, int cw) {
   const uint32_t quarter = (uint32_t)((cw + 1) & 3);  // warp index cw + 1 in the CTA
@@ -878,20 +896,8 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
   const int n0 = (int)fast_div((uint32_t)rv, a.pdiv);
   int pv = rv - n0 * a.Pv;
   int64_t gvo = ((int64_t)n0 * a.C + c) * a.Pv + pv;
-  for (int u = 0; u < KV; ++u) {
-    const int v = ct + u * kFConsumers;
-    if (!in_tmem && v >= len) break;
-    uint4 rx, rd = make_uint4(0u, 0u, 0u, 0u);
-    if (in_tmem) {
-      if constexpr (BWD)
-        tmem_ld16x2(ta0 + (uint32_t)u * 8u, ta0 + (uint32_t)u * 8u + 4u, rx, rd);
-      else
-        rx = tmem_ld16(ta0 + (uint32_t)u * 4u);
-    } else {
-      rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
-      if constexpr (BWD) rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
-    }
-    if (v >= len) continue;
+  // One output vector from its raw 16 bytes of x (and dy).
+  auto emit = [&](uint4 rx, uint4 rd) {
     if constexpr (ACT == GBN_ACT_NONE) {
       // two elements per instruction (fp32x2), the same roundings as the
       // scalar form below
@@ -915,35 +921,71 @@ __device__ __forceinline__ void stage_out(const FArgs& a, int c, int rv0, int le
       else
         *reinterpret_cast<uint4*>(out + gvo * VEC) = w;
     } else {
-    float e[VEC];
-    V::cvt(rx, e);
-    if constexpr (!BWD) {
+      float e[VEC];
+      V::cvt(rx, e);
+      if constexpr (!BWD) {
 #pragma unroll
-      for (int k = 0; k < VEC; ++k)
-        e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), ACT, slope);
-    } else {
-      float g[VEC];
-      V::cvt(rd, g);
+        for (int k = 0; k < VEC; ++k)
+          e[k] = act_out(fmaf((e[k] - shift) - mean_d, scale, p3), ACT, slope);
+      } else {
+        float g[VEC];
+        V::cvt(rd, g);
 #pragma unroll
-      for (int k = 0; k < VEC; ++k) {
-        const float xc = (e[k] - shift) - mean_d;
-        const float gk = ACT == GBN_ACT_NONE
-                             ? g[k]
-                             : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), ACT, slope));
-        e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
+        for (int k = 0; k < VEC; ++k) {
+          const float xc = (e[k] - shift) - mean_d;
+          const float gk = ACT == GBN_ACT_NONE
+                               ? g[k]
+                               : __fmul_rn(g[k], act_gate(fmaf(xc, scale, beta), ACT, slope));
+          e[k] = fmaf(gk, scale, fmaf(xc, p3, p4));
+        }
       }
+      if (a.stream_out)
+        store16_cs(out + gvo * VEC, e);
+      else
+        V::store(out + gvo * VEC, e);
     }
-    if (a.stream_out)
-      store16_cs(out + gvo * VEC, e);
-    else
-      V::store(out + gvo * VEC, e);
-    }
+  };
+  auto step = [&]() {
     pv += a.dp;
     gvo += a.ostep;
     if (pv >= a.Pv) {
       pv -= a.Pv;
       gvo += a.owrap;
     }
+  };
+  // A TMEM stage of the device's usual size: all 24 of the thread's columns
+  // in two loads and one wait (instead of a wait per vector).
+  constexpr int KVT = BWD ? 3 : 6;  // vectors per thread, 24 columns
+  if (in_tmem && KV == KVT) {
+    uint32_t r[24];
+    tmem_ld24(ta0, r);
+#pragma unroll
+    for (int u = 0; u < KVT; ++u) {
+      const int v = ct + u * kFConsumers;
+      const int o = BWD ? 8 * u : 4 * u;
+      const uint4 rx = make_uint4(r[o], r[o + 1], r[o + 2], r[o + 3]);
+      const uint4 rd = BWD ? make_uint4(r[o + 4], r[o + 5], r[o + 6], r[o + 7])
+                           : make_uint4(0u, 0u, 0u, 0u);
+      if (v < len) emit(rx, rd);
+      step();
+    }
+    return;
+  }
+  for (int u = 0; u < KV; ++u) {
+    const int v = ct + u * kFConsumers;
+    if (!in_tmem && v >= len) break;
+    uint4 rx, rd = make_uint4(0u, 0u, 0u, 0u);
+    if (in_tmem) {
+      if constexpr (BWD)
+        tmem_ld16x2(ta0 + (uint32_t)u * 8u, ta0 + (uint32_t)u * 8u + 4u, rx, rd);
+      else
+        rx = tmem_ld16(ta0 + (uint32_t)u * 4u);
+    } else {
+      rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
+      if constexpr (BWD) rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
+    }
+    if (v < len) emit(rx, rd);
+    step();
   }
 }
 
@@ -976,6 +1018,7 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
     __syncwarp();
   }
   if (ct == 0) sh.p2ready = 1;
+  if (ct == 0) GBN_RING_TRACE(10);
   // The on-chip stages: the resident tail (released afterwards, the
   // producer refills those slots) and the TMEM stages.
   int q2 = 0, slot = (N1 - 1) % NS;  // slot = i mod NS of stage i = N1 - 1 - q2
@@ -986,6 +1029,7 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
       if (i < sh.t_lo) continue;
       if (__any_sync(0xffffffffu, sh.abort != 0)) continue;
       const bool in_tmem = i < sh.t_hi;
+      if (ct == 0 && i == sh.t_hi - 1) GBN_RING_TRACE(8);
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       stage_out<T, BWD, ACT>(a, sh.seg_c[s], rv0, len, sh.seg_par[s],
@@ -997,6 +1041,7 @@ __device__ void consumer_phase2(const FArgs& a, FShared& sh, const unsigned char
       }
     }
   }
+  if (ct == 0) GBN_RING_TRACE(9);
   // Then what the producer loads, in its push order, until its end marker
   // (push j in slot (N1 - 1 - j) mod NS).
   slot = (N1 - 1) % NS;

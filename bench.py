@@ -326,8 +326,9 @@ def build_ops(names, dev):
                         G.rmsnorm_backward(dy, x, w, rstd, dx=dx, dw=dw, ws=ws))]
             ub = _nbytes(x, dy, dx, w, dw, rstd)
             hdx, hdw = torch.empty_like(hx).pin_memory(), torch.empty_like(hw).pin_memory()
+            # one launch: the ring kernel finishes dweight in the same launch
             ops.append(Op(name, f"RMSNorm bwd {case.dtype} [{case.rows}x{case.hidden}]",
-                          phases, ub, {"rms_bwd": ub}, 2, [(hx, x), (hdy, dy), (hw, w), (hr, rstd)],
+                          phases, ub, {"rms_bwd": ub}, 1, [(hx, x), (hdy, dy), (hw, w), (hr, rstd)],
                           [(dx, hdx), (dw, hdw)], None))
         elif name.startswith("ln_"):
             case = synth.CASES["ln_fused_bf16"]
@@ -357,8 +358,9 @@ def build_ops(names, dev):
             order = ["dy", "inp", "residual", "mask", "mean", "rstd", "gamma", "bias"]
             outs = [(t, torch.empty_like(t, device="cpu").pin_memory())
                     for t in (dx, dres, dg, db, dbias)]
+            # one launch: the ring kernel finishes the column sums in the same launch
             ops.append(Op(name, f"bias+dropout+add+LayerNorm bwd bf16 "
-                          f"[{case.rows}x{case.hidden}]", phases, ub, {"ln_bwd": ub}, 2,
+                          f"[{case.rows}x{case.hidden}]", phases, ub, {"ln_bwd": ub}, 1,
                           [(host[k], d[k]) for k in order], outs, None))
         else:
             raise ValueError(f"unknown op {name}")

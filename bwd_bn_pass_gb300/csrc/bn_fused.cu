@@ -50,8 +50,14 @@
 //   * Flags carry an epoch: (e+1, ~(e+1)) per CTA, with e read at kernel
 //     start from the workspace's epoch pair (or a host nonce if that pair is
 //     not self-consistent); CTA 0 advances the epoch once every CTA has
-//     published.  No memset and no atomics; a relaunch on the same workspace
-//     always waits for fresh flags.
+//     published.  The flags need no memset and no atomics (the pool words
+//     above are the kernel's only atomics); a relaunch on the same
+//     workspace always waits for fresh flags.
+//   * Both phases run close to the copy rate once the instruction count is
+//     low: packed fp32x2 arithmetic in both passes, two accumulation chains
+//     per thread in phase 1, ring slots and output offsets advanced by
+//     counters, and the plane index by a precomputed multiplier -- no
+//     division in any per-stage or per-vector path.
 //   * Every wait is bounded (about one second).  On expiry the CTA records
 //     GBN_DEV_WAIT_TIMEOUT in the status word, stops issuing and computing,
 //     waits (bounded) for its own copies in flight and returns.

@@ -116,7 +116,11 @@ bool row_plan(int64_t R, int64_t H, int kind, int dtype, bool fast_ok, bool has_
     if (nst > kMaxStages) nst = kMaxStages;
     // about 128 KB in flight per SM: deeper rings measured slower (RMSNorm
     // bf16 [2048, 8192]: 26.3 us at 2-5 stages of 32 KB, 28.0 us at 6)
-    const int64_t cap = (kRingBytesPerSm + (int64_t)stage - 1) / (int64_t)stage;
+    int64_t cap = (kRingBytesPerSm + (int64_t)stage - 1) / (int64_t)stage;
+    // the instances that hold a stage until the end of their second pass
+    // (kv > 2) keep a third stage in flight (fp32 [2048, 8192]: 34.6 ->
+    // 33.1 us per launch)
+    if (kv > 2 && cap < 3) cap = 3;
     if (nst > cap && cap >= 2) nst = cap;
     if (kv <= 4 && nst >= 2) {
       const int64_t nblk = (R + rb - 1) / rb;

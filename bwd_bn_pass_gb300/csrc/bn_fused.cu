@@ -579,9 +579,10 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
 // in double-fp32 so that the channel's sum d is exact to double-fp32
 // precision (the backward's sum dy*(x - mean) relies on it: a constant dy
 // must give 0): per element, with the rounding error of x - shift for fp32
-// input; for bf16 input, per vector when that is exact (below), else per
-// element.  Sum d^2 over the vector's lanes in fp32, then one double-fp32
-// add per vector (its rounding enters the variance only relatively).
+// input; for bf16 input, per thread and stage when that is exact (below),
+// else per element.  Sum d^2 in fp32 over the vector's lanes (fp32 input)
+// or over the thread's vectors of the stage (bf16 input), then one
+// double-fp32 add (its rounding enters the variance only relatively).
 // Backward: sum dy*d per element in double-fp32 with each product's exact
 // residual and, for fp32 input, the rounding error of x - shift; sum dy
 // likewise for fp32, while ungated bf16 dy is first summed over the
@@ -589,13 +590,18 @@ __device__ void producer(const FArgs& a, FShared& sh, unsigned char* ring) {
 // within 14 binades of each other -- and then added in double-fp32 once per
 // vector.
 //
-// The bf16 per-vector sum: when the exponents of the eight x and of shift
-// span at most 12 (E_min .. E_max), every value is a multiple of
-// Q = 2^(E_min - 7), each d = x - shift is exact, and every partial sum of
-// up to eight d is a multiple of Q below 2^(E_max + 5) <= 2^24 Q in
-// magnitude, so the fp32 sums of the vector's d are exact too.  smag holds
-// shift's bf16 magnitude bits in both halves.  Zeros and subnormals take
-// the per-element path.
+// The bf16 sum per thread and stage: when the exponents of the thread's x
+// in the stage and of shift lie in E_min .. E_max, every value is a
+// multiple of Q = 2^(E_min - 7) below 2^(E_max + 1) in magnitude, so each
+// d = x - shift is a multiple of Q below 2^(E_max + 2), and a partial sum
+// of at most n of them is a multiple of Q below n 2^(E_max + 2).  With
+// E_max - E_min <= 15 - ceil(log2 n) that is at most 2^24 Q: every fp32
+// partial sum is exact, in any order.  n counts the terms of one lane (four
+// per vector).  The magnitudes' largest and smallest come from the bf16x2
+// max / min instructions over the stage, and only then is the sum added in
+// double-fp32; a stage that fails the test (zeros, subnormals, a wide
+// range) re-reads its vectors from the ring slot and sums per element.
+// smag holds shift's bf16 magnitude bits in both halves.
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -607,12 +613,11 @@ __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
   return r;
 }
 
-template <typename T>
-__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2 (&a1)[2], DF2& a2,
-                                        uint32_t smag) {
-  constexpr int NP = Pairs16<T>::NP;
+// fp32 forward, one vector (bf16 input sums per stage: FwdStage below).
+__device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2 (&a1)[2], DF2& a2) {
+  constexpr int NP = Pairs16<float>::NP;
   f2 p[NP], d[NP];
-  Pairs16<T>::get(r, p);
+  Pairs16<float>::get(r, p);
   f2 l2 = 0ull;
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
@@ -620,31 +625,61 @@ __device__ __forceinline__ void fwd_acc(uint4 r, f2 sh2, f2 nsh2, DF2 (&a1)[2], 
     l2 = f2_fma(d[k], d[k], l2);
   }
   df2_add(a2, l2);
-  if constexpr (sizeof(T) == 2) {
-    // magnitudes as bf16x2 (sign cleared), their largest and smallest with
-    // the bf16x2 max / min instructions, folded across the two halves
-    const uint32_t k7 = 0x7fff7fffu;
-    const uint32_t m0 = r.x & k7, m1 = r.y & k7, m2 = r.z & k7, m3 = r.w & k7;
-    uint32_t hi = bf16x2_max(bf16x2_max(m0, m1), bf16x2_max(bf16x2_max(m2, m3), smag));
-    uint32_t lo = bf16x2_min(bf16x2_min(m0, m1), bf16x2_min(bf16x2_min(m2, m3), smag));
-    hi = bf16x2_max(hi, __byte_perm(hi, 0u, 0x1032));
-    lo = bf16x2_min(lo, __byte_perm(lo, 0u, 0x1032));
-    const uint32_t emax = hi & 0x7f80u, emin = lo & 0x7f80u;
-    if (emin != 0u && emax - emin <= (12u << 7)) {
-      df2_add(a1[0], f2_add(f2_add(d[0], d[1]), f2_add(d[2], d[3])));
-      return;
-    }
-  }
-  // alternate pairs feed two accumulators (two dependency chains)
+  // alternate pairs feed two accumulators (two dependency chains), each
+  // with the rounding error of x - shift
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     DF2& acc = a1[k & 1];
     df2_add(acc, d[k]);
-    if constexpr (sizeof(T) == 4) {
-      const f2 bb = f2_sub(d[k], p[k]);
-      acc.lo = f2_add(acc.lo, f2_add(f2_sub(p[k], f2_sub(d[k], bb)), f2_sub(nsh2, bb)));
-    }
+    const f2 bb = f2_sub(d[k], p[k]);
+    acc.lo = f2_add(acc.lo, f2_add(f2_sub(p[k], f2_sub(d[k], bb)), f2_sub(nsh2, bb)));
   }
+}
+
+// bf16 forward: one thread's sums over its vectors of one stage.
+struct FwdStage {
+  f2 s0, s1;         // sum d, two chains
+  f2 q0, q1;         // sum d^2, two chains
+  uint32_t hi, lo;   // largest / smallest bf16 magnitude seen, per half
+};
+
+__device__ __forceinline__ void fwd_stage_begin(FwdStage& f, uint32_t smag) {
+  f.s0 = f.s1 = f.q0 = f.q1 = 0ull;
+  f.hi = f.lo = smag;
+}
+
+__device__ __forceinline__ void fwd_stage_vec(FwdStage& f, uint4 r, f2 sh2) {
+  f2 p[4];
+  Pairs16<bf16>::get(r, p);
+  const f2 d0 = f2_sub(p[0], sh2), d1 = f2_sub(p[1], sh2);
+  const f2 d2 = f2_sub(p[2], sh2), d3 = f2_sub(p[3], sh2);
+  f.s0 = f2_add(f.s0, f2_add(d0, d1));
+  f.s1 = f2_add(f.s1, f2_add(d2, d3));
+  f.q0 = f2_fma(d0, d0, f.q0);
+  f.q1 = f2_fma(d1, d1, f.q1);
+  f.q0 = f2_fma(d2, d2, f.q0);
+  f.q1 = f2_fma(d3, d3, f.q1);
+  const uint32_t k7 = 0x7fff7fffu;
+  const uint32_t m0 = r.x & k7, m1 = r.y & k7, m2 = r.z & k7, m3 = r.w & k7;
+  f.hi = bf16x2_max(f.hi, bf16x2_max(bf16x2_max(m0, m1), bf16x2_max(m2, m3)));
+  f.lo = bf16x2_min(f.lo, bf16x2_min(bf16x2_min(m0, m1), bf16x2_min(m2, m3)));
+}
+
+// Whether the stage's fp32 sums of d are exact: the exponent span of the
+// magnitudes (both halves folded) at most span7 >> 7, no zero or subnormal.
+__device__ __forceinline__ bool fwd_stage_exact(const FwdStage& f, uint32_t span7) {
+  const uint32_t hi = bf16x2_max(f.hi, __byte_perm(f.hi, 0u, 0x1032));
+  const uint32_t lo = bf16x2_min(f.lo, __byte_perm(f.lo, 0u, 0x1032));
+  const uint32_t emax = hi & 0x7f80u, emin = lo & 0x7f80u;
+  return emin != 0u && emax - emin <= span7;
+}
+
+// Per-element double-fp32 sum of one bf16 vector's d (the stage fallback).
+__device__ __forceinline__ void fwd_sum_elems(uint4 r, f2 sh2, DF2 (&a1)[2]) {
+  f2 p[4];
+  Pairs16<bf16>::get(r, p);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) df2_add(a1[k & 1], f2_sub(p[k], sh2));
 }
 
 // With an activation (ACT), dy is first gated by d act / d pre with
@@ -725,6 +760,12 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
   // TMEM stages: KV vector slots per thread and input, cps columns a stage.
   const int KV = a.stage_v / kFConsumers, cps = KV * (BWD ? 8 : 4);
   const uint32_t tbase = tmem_thread_base(sh.tmem, ct >> 5);
+  // bf16 forward: exponent span (times 128) for which a lane's fp32 sum of
+  // its n = 4 KV terms of a stage is exact, 15 - ceil(log2 n); none if < 0.
+  constexpr bool kStageSum = !BWD && sizeof(T) == 2;
+  const int span = 15 - (32 - __clz(4 * KV - 1));
+  const uint32_t span7 = span >= 0 ? (uint32_t)span << 7 : 0u;
+  const bool span_ok = span >= 0;
   int i = 0, slot = 0;  // slot = i mod NS
   for (int s = 0; s < sh.nseg; ++s) {
     const float shift = sh.seg_par[s][0];
@@ -746,7 +787,30 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
       int rv0, len;
       stage_of(sh, a, s, q, rv0, len);
       const unsigned char* st = ring + (size_t)slot * (BWD ? 2u : 1u) * in_bytes;
-      if (i >= sh.t_lo && i < sh.t_hi) {
+      if constexpr (kStageSum) {
+        FwdStage f;
+        fwd_stage_begin(f, smag);
+        if (i >= sh.t_lo && i < sh.t_hi) {
+          // a TMEM stage (see below): every slot copied, the valid ones summed
+          uint32_t ta = tbase + (uint32_t)((i - sh.t_lo) * cps);
+          for (int k = 0; k < KV; ++k, ta += 4u) {
+            const int v = ct + k * kFConsumers;
+            const uint4 rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
+            tmem_st16(ta, rx);
+            if (v < len) fwd_stage_vec(f, rx, sh2);
+          }
+        } else {
+          for (int v = ct; v < len; v += kFConsumers)
+            fwd_stage_vec(f, *reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2);
+        }
+        df2_add(a0, f2_add(f.q0, f.q1));
+        if (span_ok && fwd_stage_exact(f, span7)) {
+          df2_add(a1[0], f2_add(f.s0, f.s1));
+        } else {
+          for (int v = ct; v < len; v += kFConsumers)
+            fwd_sum_elems(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, a1);
+        }
+      } else if (i >= sh.t_lo && i < sh.t_hi) {
         // A TMEM stage: every lane copies all its vector slots of the stage
         // (the tcgen05 copies are warp-wide; a slot past len holds stale
         // ring bytes that phase 2 never uses) and sums the valid ones.
@@ -756,7 +820,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
           const uint4 rx = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
           tmem_st16(ta, rx);
           if constexpr (!BWD) {
-            if (v < len) fwd_acc<T>(rx, sh2, nsh2, a1, a0, smag);
+            if (v < len) fwd_acc(rx, sh2, nsh2, a1, a0);
           } else {
             const uint4 rd = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
             tmem_st16(ta + 4u, rd);
@@ -772,8 +836,7 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
         }
       } else if constexpr (!BWD) {
         for (int v = ct; v < len; v += kFConsumers)
-          fwd_acc<T>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a1, a0,
-                     smag);
+          fwd_acc(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, nsh2, a1, a0);
       } else if (a.act == GBN_ACT_NONE) {
         for (int v = ct; v < len; v += kFConsumers)
           bwd_acc<T, GBN_ACT_NONE>(*reinterpret_cast<const uint4*>(st + (size_t)v * 16),

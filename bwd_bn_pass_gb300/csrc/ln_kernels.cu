@@ -100,8 +100,9 @@ __device__ __forceinline__ f2 keep_pair(uint2 m, int p, float s) {
   return f2_pack(lo, hi);
 }
 
-// Row-sum slots [group][buffer][row][sum][warp], each warp run padded to a
-// multiple of 4 floats (read as float4); at most 14 groups x 2 x 2 x 2 x 16.
+// Row-sum slots [group][buffer][row][warp][sum], the warp run padded to a
+// multiple of 4 warps (read as float4: two warps' pairs of sums, added as
+// packed pairs); at most 14 groups x 2 x 2 x 16 x 2.
 constexpr int kLnMaxRedFloats = 512;
 
 // Bit 7 of every byte of the result is set iff that byte of w is nonzero.
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
     };
 
     const float inv_H = 1.f / (float)H;
+    const bool plain_out = a.dzx == nullptr && !a.dres_f32;
     bool failed = false;
 
     // ring slot s = i mod NS, its phase parity and this group's slot buffer
@@ -408,14 +410,15 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
       }
       if constexpr (RPS == 2) {
         const float v = warp_sum4_transposed(rsum[0][0], rsum[0][1], rsum[1][0], rsum[1][1]);
-        if ((lane & 7) == 0) slot[(lane >> 3) * P + wis] = v;  // [row][sum] = lane / 8
+        // lane / 8 = 2 row + sum
+        if ((lane & 7) == 0) slot[((lane >> 4) * P + wis) * 2 + ((lane >> 3) & 1)] = v;
       } else {
 #pragma unroll
         for (int q = 0; q < RPS; ++q) {
           const float sg = warp_sum(rsum[q][0]), sgx = warp_sum(rsum[q][1]);
           if (lane == 0) {
-            slot[(q * 2 + 0) * P + wis] = sg;
-            slot[(q * 2 + 1) * P + wis] = sgx;
+            slot[(q * P + wis) * 2 + 0] = sg;
+            slot[(q * P + wis) * 2 + 1] = sgx;
           }
         }
       }
@@ -425,20 +428,25 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
         break;
       }
 
-      // dz, outputs and column sums for the stage's rows.
+      // dz, outputs and column sums for the stage's rows.  GEN: the form
+      // with dz_extra and fp32 dresidual tested at run time; the common form
+      // (neither) carries no test in its loops.
+      auto rows_out = [&](auto gen) {
+      constexpr bool GEN = decltype(gen)::value;
 #pragma unroll
       for (int q = 0; q < RPS; ++q) {
         const int rr = q;
         if (rr >= nr) break;
-        float SG = 0.f, SGX = 0.f;
-        const float4* s0 = reinterpret_cast<const float4*>(slot + (rr * 2 + 0) * P);
-        const float4* s1 = reinterpret_cast<const float4*>(slot + (rr * 2 + 1) * P);
-        for (int j = 0; j < P / 4; ++j) {
-          const float4 u = s0[j], w = s1[j];
-          SG += (u.x + u.y) + (u.z + u.w);
-          SGX += (w.x + w.y) + (w.z + w.w);
+        // both sums at once: (sum g, sum g*xhat) pairs of four warps per step
+        const float4* sp = reinterpret_cast<const float4*>(slot + rr * 2 * P);
+        f2 acc = 0ull;
+        for (int j = 0; j < P / 2; j += 2) {
+          const float4 u = sp[j], w = sp[j + 1];
+          acc = f2_add(acc, f2_add(f2_add(f2_pack(u.x, u.y), f2_pack(u.z, u.w)),
+                                   f2_add(f2_pack(w.x, w.y), f2_pack(w.z, w.w))));
         }
-        const float mg = SG * inv_H, mgx = SGX * inv_H;
+        const float2 sums = f2_unpack(acc);
+        const float mg = sums.x * inv_H, mgx = sums.y * inv_H;
         const int64_t r = r0 + rr;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
@@ -447,7 +455,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
           const int64_t go = r * H + (int64_t)vi * VE;
           if constexpr (COMP) {
             float dzx[VE];
-            if (a.dzx != nullptr) {
+            if (GEN && a.dzx != nullptr) {
 #pragma unroll
               for (int e = 0; e < VE; e += 4) {
                 const float4 t = *reinterpret_cast<const float4*>(a.dzx + go + e);
@@ -490,7 +498,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
               const f2 g2 = f2_mul(dy2[p], gam2[k][p]);
               const f2 inner = f2_fma(xh2, nmgx2, f2_sub(g2, mg2));
               f2 extra = 0ull;
-              if (a.dzx != nullptr) {
+              if (GEN && a.dzx != nullptr) {
                 const float2 t = *reinterpret_cast<const float2*>(a.dzx + go + 2 * p);
                 extra = f2_pack(t.x, t.y);
               }
@@ -502,7 +510,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
             }
             *reinterpret_cast<uint4*>(static_cast<T*>(a.dx) + go) = PK::put(dx2);
             if (FUSED && a.dres != nullptr) {
-              if (a.dres_f32) {
+              if (GEN && a.dres_f32) {
                 float4* d4 = reinterpret_cast<float4*>(static_cast<float*>(a.dres) + go);
 #pragma unroll
                 for (int p = 0; p < NP; p += 2) {
@@ -516,6 +524,9 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) ln_bwd_ring_kernel(LnArgs 
           }
         }
       }
+      };
+      if (plain_out) rows_out(std::false_type{});
+      else rows_out(std::true_type{});
     }
     // every group has left its loop (a failed group has set the abort flag,
     // which ends the others' waits): one decision for all consumers

@@ -102,7 +102,9 @@ __device__ __forceinline__ f2 keep_pair(uint2 m, int p, float s) {
 
 // Row-sum slots [group][buffer][row][warp][sum], the warp run padded to a
 // multiple of 4 warps (read as float4: two warps' pairs of sums, added as
-// packed pairs); at most 14 groups x 2 x 2 x 16 x 2.
+// packed pairs).  The plan keeps groups x warps per group within 14, so
+// groups x padded warps is at most 56 (14 one-warp groups) and the slots
+// take at most 56 x 2 buffers x 2 rows x 2 sums = 448 floats.
 constexpr int kLnMaxRedFloats = 512;
 
 // Bit 7 of every byte of the result is set iff that byte of w is nonzero.

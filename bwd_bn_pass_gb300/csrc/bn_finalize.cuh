@@ -45,10 +45,13 @@ __device__ __forceinline__ BnFwdFinal bn_fwd_final(DF s1, DF s2, float mh, float
 }
 
 // Stats rows 0-7 of channel c (mean, var, inv_std, scale, shift, mean - shift
-// rounded, and mean - shift as a (hi, lo) pair) and the running update.
-__device__ __forceinline__ void bn_fwd_write(const BnFwdFinal& f, float shift, int64_t C, int c,
-                                             float M, float* stats, float* running_mean,
-                                             float* running_var, float momentum) {
+// rounded, and mean - shift as a (hi, lo) pair) and the running update, from
+// the running statistics' previous values rm, rv (read by the caller, which
+// may read them early: nothing else in a call writes them).
+__device__ __forceinline__ void bn_fwd_write_from(const BnFwdFinal& f, float shift, int64_t C,
+                                                  int c, float M, float* stats,
+                                                  float* running_mean, float* running_var,
+                                                  float momentum, float rm, float rv) {
   const float mean = df_round(df_plus(f.md, shift));
   stats[c] = mean;
   stats[C + c] = f.var;
@@ -59,8 +62,14 @@ __device__ __forceinline__ void bn_fwd_write(const BnFwdFinal& f, float shift, i
   stats[6 * C + c] = f.md.hi;
   stats[7 * C + c] = f.md.lo;
   const float m = momentum;
-  if (running_mean) running_mean[c] = (1.f - m) * running_mean[c] + m * mean;
-  if (running_var) running_var[c] = (1.f - m) * running_var[c] + m * f.var * (M / (M - 1.f));
+  if (running_mean) running_mean[c] = (1.f - m) * rm + m * mean;
+  if (running_var) running_var[c] = (1.f - m) * rv + m * f.var * (M / (M - 1.f));
+}
+__device__ __forceinline__ void bn_fwd_write(const BnFwdFinal& f, float shift, int64_t C, int c,
+                                             float M, float* stats, float* running_mean,
+                                             float* running_var, float momentum) {
+  bn_fwd_write_from(f, shift, C, c, M, stats, running_mean, running_var, momentum,
+                    running_mean ? running_mean[c] : 0.f, running_var ? running_var[c] : 0.f);
 }
 
 struct BnBwdFinal {

@@ -233,22 +233,24 @@ struct ApplyArgs {
 };
 
 // Warp 0 computes (shift, mean - shift, scale, beta) for channel c; in
-// training mode this is the forward finalize, and block j = 0 also writes
-// the stats rows and the running-statistics update.
-__device__ __noinline__ void apply_prologue(const BnGeom& g, const ApplyArgs& a, int c, int j,
-                                               float shift_x, float* fin) {
+// training mode this is the forward finalize, returned so that block j = 0
+// can write the stats rows and the running-statistics update after its
+// outputs (nothing in this launch reads them).  shift_x, gamma and beta are
+// the channel's inputs that the stats grid does not write: the caller loads
+// them before it waits for that grid, so that only the partials are read
+// after the wait.
+__device__ __noinline__ BnFwdFinal apply_prologue(const BnGeom& g, const ApplyArgs& a, int c,
+                                                  float shift_x, float gamma, float beta,
+                                                  float* fin) {
   float shift, mean_d, scale;
-  const float beta = a.beta ? a.beta[c] : 0.f;
+  BnFwdFinal f{};
   if (a.mode == kApplyTrain) {
     DF s1, s2;
     reduce_partials(a.part, g, c, s1, s2);
-    const BnFwdFinal f = bn_fwd_final(s1, s2, g.Mh, g.Ml, a.gamma ? a.gamma[c] : 1.f, a.eps);
+    f = bn_fwd_final(s1, s2, g.Mh, g.Ml, gamma, a.eps);
     shift = shift_x;
     mean_d = f.md.hi;
     scale = f.scale;
-    if (j == 0 && threadIdx.x == 0)
-      bn_fwd_write(f, shift, g.C, c, g.Mh + g.Ml, a.stats, a.running_mean, a.running_var,
-                   a.momentum);
   } else if (a.mode == kApplyStats) {
     const int64_t C = g.C;
     shift = a.stats[4 * C + c];
@@ -260,6 +262,7 @@ __device__ __noinline__ void apply_prologue(const BnGeom& g, const ApplyArgs& a,
     scale = a.scale[c];
   }
   if (threadIdx.x == 0) { fin[0] = shift; fin[1] = mean_d; fin[2] = scale; fin[3] = beta; }
+  return f;
 }
 
 template <typename T, int VEC, typename I>
@@ -271,6 +274,18 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   int32_t v0, cnt;
   slice(g, j, v0, cnt);
 
+  // The channel's own inputs first (ahead of the vector loads below): the
+  // finalize then waits on nothing but the stats grid's partials.
+  float shift_x = 0.f, gam = 1.f, bet = 0.f, rm_old = 0.f, rv_old = 0.f;
+  if (threadIdx.x < 32) {
+    shift_x = to_f32(x[(int64_t)c * g.P]);
+    if (a.gamma) gam = a.gamma[c];
+    if (a.beta) bet = a.beta[c];
+    if (a.mode == kApplyTrain && j == 0 && threadIdx.x == 0) {
+      if (a.running_mean) rm_old = a.running_mean[c];
+      if (a.running_var) rv_old = a.running_var[c];
+    }
+  }
   // Walk this thread's vectors backwards (the stats pass read the slice
   // tails last, so they are the likeliest to be in L2); load the first batch
   // before waiting on the stats grid (x is never written by it).
@@ -286,7 +301,8 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   }
 
   if (a.mode == kApplyTrain) pdl_wait();
-  if (threadIdx.x < 32) apply_prologue(g, a, c, j, to_f32(x[(int64_t)c * g.P]), fin);
+  BnFwdFinal fin_f{};
+  if (threadIdx.x < 32) fin_f = apply_prologue(g, a, c, shift_x, gam, bet, fin);
   __syncthreads();
   const float shift = fin[0], mean_d = fin[1], scale = fin[2], beta = fin[3];
   // 16-byte vectors without an activation: two elements per instruction
@@ -326,6 +342,9 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
       cursor_back(q, g);
     }
   }
+  if (a.mode == kApplyTrain && j == 0 && threadIdx.x == 0)
+    bn_fwd_write_from(fin_f, shift, g.C, c, g.Mh + g.Ml, a.stats, a.running_mean,
+                      a.running_var, a.momentum, rm_old, rv_old);
 }
 
 // --------------------------------------------------------- grad_sums --
@@ -443,19 +462,23 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
 
 // ---------------------------------------------------- finalize + dx --
 
+// The forward's per-channel values the backward finalize and dx need,
+// read from stats (written by the forward, before the grad-sums grid).
+struct DxChan {
+  float shift, mean_d, inv_std, scale, md_hi, md_lo, beta;
+};
+
 // Warp 0: the backward finalize for channel c (block j = 0 writes grads).
 // S = sum dy*(x - mean) = sum dy*(x - shift) - (mean - shift)*sum dy, in
-// double-fp32 with the forward's (mean - shift) pair.
-__device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
-                                         const float2* part, float* grads, int c, int j,
-                                         const float* beta, float* fin) {
+// double-fp32 with the forward's (mean - shift) pair.  ch was loaded before
+// the wait for the grad-sums grid, so only its partials are read after it.
+__device__ __noinline__ void dx_prologue(const BnGeom& g, const float2* part, float* grads,
+                                         int c, int j, const DxChan ch, float* fin) {
   DF p0, p1;
   reduce_partials(part, g, c, p0, p1);
   const int64_t C = g.C;
-  const float inv_std = stats[2 * C + c];
-  const float scale = stats[3 * C + c];
-  const DF md{stats[6 * C + c], stats[7 * C + c]};
-  const BnBwdFinal f = bn_bwd_final(p0, p1, md, inv_std, scale, g.Mh + g.Ml);
+  const DF md{ch.md_hi, ch.md_lo};
+  const BnBwdFinal f = bn_bwd_final(p0, p1, md, ch.inv_std, ch.scale, g.Mh + g.Ml);
   const float k1 = f.k1, k2 = f.k2;
   if (j == 0 && threadIdx.x == 0) {
     grads[c] = f.dgamma;
@@ -464,12 +487,12 @@ __device__ __noinline__ void dx_prologue(const BnGeom& g, const float* stats,
     grads[3 * C + c] = k2;
   }
   if (threadIdx.x == 0) {
-    fin[0] = stats[4 * C + c];
-    fin[1] = stats[5 * C + c];
-    fin[2] = scale;
+    fin[0] = ch.shift;
+    fin[1] = ch.mean_d;
+    fin[2] = ch.scale;
     fin[3] = k1;
     fin[4] = k2;
-    fin[5] = beta ? beta[c] : 0.f;
+    fin[5] = ch.beta;
   }
 }
 
@@ -485,6 +508,19 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   int32_t v0, cnt;
   slice(g, j, v0, cnt);
 
+  // The forward's values of this channel first (stats rows 2-7; beta for
+  // the activation gate), ahead of the vector loads below.
+  DxChan ch{0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (threadIdx.x < 32) {
+    const int64_t C = g.C;
+    ch.inv_std = stats[2 * C + c];
+    ch.scale = stats[3 * C + c];
+    ch.shift = stats[4 * C + c];
+    ch.mean_d = stats[5 * C + c];
+    ch.md_hi = stats[6 * C + c];
+    ch.md_lo = stats[7 * C + c];
+    ch.beta = beta ? beta[c] : 0.f;
+  }
   const int32_t vlast = v0 + (int32_t)threadIdx.x + (cnt > 0 ? cnt - 1 : 0) * kBnThreads;
   Cursor<I> q = cursor_at<I>(g, c, vlast);
   typename V::raw rx[kUDx], rd[kUDx];
@@ -500,7 +536,7 @@ __global__ void __launch_bounds__(kBnThreads, kBnBlocksPerSm)
   }
 
   pdl_wait();
-  if (threadIdx.x < 32) dx_prologue(g, stats, part, grads, c, j, beta, fin);
+  if (threadIdx.x < 32) dx_prologue(g, part, grads, c, j, ch, fin);
   __syncthreads();
   const float shift = fin[0], mean_d = fin[1], scale = fin[2], k1 = fin[3], k2 = fin[4];
   const float bta = fin[5];

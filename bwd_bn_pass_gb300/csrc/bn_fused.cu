@@ -219,6 +219,11 @@ __device__ __forceinline__ void store16_cs(bf16* p, const float (&e)[8]) {
 // own lane is 32*(w % 4) + t); the 16 consumer warps share each lane quarter
 // four ways, 128 of the 512 columns each.  Address: lane << 16 | column.
 
+// Vectors per consumer thread and input of a stage at the usual stage size
+// (227 KB of shared memory: 48 KB stages of x forward, 24 KB of x and dy
+// backward): the phase-1 early release keeps that many in registers.
+constexpr int kKVFwd = 6;
+constexpr int kKVBwd = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kTmemColsPerThread = kTmemCols / (kFConsumerWarps / 4);  // 128
 
@@ -790,6 +795,34 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
       if constexpr (kStageSum) {
         FwdStage f;
         fwd_stage_begin(f, smag);
+        if (KV == kKVFwd && i + NS < N1) {
+          // A stage that phase 1 refills: this thread's vectors into
+          // registers and the slot released before the copies to TMEM (for
+          // a TMEM stage) and the sums, so that the refill starts sooner.
+          uint4 rx[kKVFwd];
+#pragma unroll
+          for (int k = 0; k < kKVFwd; ++k)
+            rx[k] = *reinterpret_cast<const uint4*>(st + (size_t)(ct + k * kFConsumers) * 16);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.empty[slot]);
+          if (i >= sh.t_lo && i < sh.t_hi) {
+            uint32_t ta = tbase + (uint32_t)((i - sh.t_lo) * cps);
+#pragma unroll
+            for (int k = 0; k < kKVFwd; ++k, ta += 4u) tmem_st16(ta, rx[k]);
+          }
+#pragma unroll
+          for (int k = 0; k < kKVFwd; ++k)
+            if (ct + k * kFConsumers < len) fwd_stage_vec(f, rx[k], sh2);
+          df2_add(a0, f2_add(f.q0, f.q1));
+          if (span_ok && fwd_stage_exact(f, span7)) {
+            df2_add(a1[0], f2_add(f.s0, f.s1));
+          } else {
+#pragma unroll
+            for (int k = 0; k < kKVFwd; ++k)
+              if (ct + k * kFConsumers < len) fwd_sum_elems(rx[k], sh2, a1);
+          }
+          continue;
+        }
         if (i >= sh.t_lo && i < sh.t_hi) {
           // a TMEM stage (see below): every slot copied, the valid ones summed
           uint32_t ta = tbase + (uint32_t)((i - sh.t_lo) * cps);
@@ -810,6 +843,37 @@ __device__ void consumer_phase1(const FArgs& a, FShared& sh, const unsigned char
           for (int v = ct; v < len; v += kFConsumers)
             fwd_sum_elems(*reinterpret_cast<const uint4*>(st + (size_t)v * 16), sh2, a1);
         }
+      } else if (BWD && KV == kKVBwd && i + NS < N1) {
+        // Backward, a stage that phase 1 refills: as above, every vector
+        // pair of this thread into registers and the slot released first.
+        uint4 rx[kKVBwd], rd[kKVBwd];
+#pragma unroll
+        for (int k = 0; k < kKVBwd; ++k) {
+          const int v = ct + k * kFConsumers;
+          rx[k] = *reinterpret_cast<const uint4*>(st + (size_t)v * 16);
+          rd[k] = *reinterpret_cast<const uint4*>(st + in_bytes + (size_t)v * 16);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.empty[slot]);
+        if (i >= sh.t_lo && i < sh.t_hi) {
+          uint32_t ta = tbase + (uint32_t)((i - sh.t_lo) * cps);
+#pragma unroll
+          for (int k = 0; k < kKVBwd; ++k, ta += 8u) {
+            tmem_st16(ta, rx[k]);
+            tmem_st16(ta + 4u, rd[k]);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < kKVBwd; ++k) {
+          if (ct + k * kFConsumers >= len) continue;
+          if (a.act == GBN_ACT_NONE)
+            bwd_acc<T, GBN_ACT_NONE>(rx[k], rd[k], sh2, nsh2, ap, a0, a1);
+          else if (a.act == GBN_ACT_RELU)
+            bwd_acc<T, GBN_ACT_RELU>(rx[k], rd[k], sh2, nsh2, ap, a0, a1);
+          else
+            bwd_acc<T, GBN_ACT_LEAKY_RELU>(rx[k], rd[k], sh2, nsh2, ap, a0, a1);
+        }
+        continue;
       } else if (i >= sh.t_lo && i < sh.t_hi) {
         // A TMEM stage: every lane copies all its vector slots of the stage
         // (the tcgen05 copies are warp-wide; a slot past len holds stale

@@ -524,7 +524,7 @@ def run_ours(args, rank, world, local_rank):
 
     graph = run_graph(ops, stream, dev, args.steps, world, flush_l2)
     latency = None if args.ops else run_latency(build_ops(LATENCY_OPS, dev), stream, dev,
-                                                max(args.steps, 20), flush_l2)
+                                                max(args.steps, 200), flush_l2)
 
     e2e = None
     if not args.no_e2e:
@@ -567,7 +567,10 @@ def run_ours(args, rank, world, local_rank):
 def run_latency(ops, stream, dev, steps, flush_l2):
     """Microseconds per call of latency-bound ops: each call timed alone with
     CUDA events after an L2 flush, eagerly and as a replay of a CUDA graph
-    that holds just that call (the launch overhead a graph removes)."""
+    that holds just that call (the launch overhead a graph removes).  The
+    event timer advances in steps of about 2 us on this device, so a single
+    sample, and hence the median and the minimum, snap to a step; the mean
+    over many calls resolves finer differences."""
     import torch
     out = {}
     for op in ops:
@@ -605,8 +608,10 @@ def run_latency(ops, stream, dev, steps, flush_l2):
         out[op.name] = {
             "desc": op.desc, "launches": op.launches,
             "us_median": round(statistics.median(eager), 2), "us_min": round(min(eager), 2),
+            "us_mean": round(statistics.mean(eager), 2), "samples": len(eager),
             "us_graph_median": round(statistics.median(graph), 2) if graph else None,
             "us_graph_min": round(min(graph), 2) if graph else None,
+            "us_graph_mean": round(statistics.mean(graph), 2) if graph else None,
         }
     return out
 

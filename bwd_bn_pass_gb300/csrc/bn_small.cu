@@ -63,6 +63,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   __shared__ float2 red[64];
   const int c = blockIdx.x, t = threadIdx.x, M = B * P;
   const float shift = to_f32(x[(int64_t)c * P]);  // x[0, c, 0, 0]
+  // The channel's parameters and running statistics are read now, with x:
+  // after the block's reduction each would be one more memory round trip.
+  const float gam = gamma ? gamma[c] : 1.f, b = beta ? beta[c] : 0.f;
+  float rm = 0.f, rv = 0.f;
+  if (t == 0) {
+    rm = running_mean ? running_mean[c] : 0.f;
+    rv = running_var ? running_var[c] : 0.f;
+  }
   DF s1{0.f, 0.f}, s2{0.f, 0.f};
   for (int m0 = t; m0 < M; m0 += kSmallBatch * kSmallThreads) {
     float v[kSmallBatch];
@@ -85,13 +93,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
   }
   block_sum2_df(s1, s2, red);  // contains __syncthreads: vals is complete
-  const BnFwdFinal f = bn_fwd_final(s1, s2, Mh, Ml, gamma ? gamma[c] : 1.f, eps);
-  if (t == 0)
-    bn_fwd_write(f, shift, C, c, Mh + Ml, stats, running_mean, running_var, momentum);
-  const float b = beta ? beta[c] : 0.f, mean_d = f.md.hi, scale = f.scale;
+  const BnFwdFinal f = bn_fwd_final(s1, s2, Mh, Ml, gam, eps);
+  const float mean_d = f.md.hi, scale = f.scale;
   for (int m = t; m < M; m += kSmallThreads)
     y[elem_offset(m, C, c, P, pd)] =
         from_f32<T>(act_out(fmaf((vals[m] - shift) - mean_d, scale, b), act, slope));
+  if (t == 0)
+    bn_fwd_write_from(f, shift, C, c, Mh + Ml, stats, running_mean, running_var, momentum, rm,
+                      rv);
 }
 
 template <typename T>

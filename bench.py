@@ -233,15 +233,16 @@ def build_ops(names, dev):
                     + (" channels-last" if nhwc else ""))
             key = "bn_forward_train" if name.endswith("fwd") else "bn_backward"
             # NCHW: one launch of the persistent kernel from the library's size
-            # threshold on, or of the small-channel kernel for channels of at
-            # most bn_small_max_elems() elements, else stats + apply (grad
-            # sums + dx); NHWC: three.
+            # threshold on, or of the small-channel kernels where the library
+            # takes them (a block or a cluster of up to 8 blocks per channel,
+            # one resident wave), else stats + apply (grad sums + dx); NHWC:
+            # three.
             in_bytes = T * (1 if name.endswith("fwd") else 2)
             M = x.numel() // C
             if nhwc:
                 launches = 3
-            elif in_bytes >= G.bn_persistent_min_bytes() or M <= G.bn_small_max_elems():
-                launches = 1  # the persistent kernel, or the small-channel kernel
+            elif in_bytes >= G.bn_persistent_min_bytes() or G.bn_small_blocks_per_channel(x.shape):
+                launches = 1  # the persistent kernel, or a small-channel kernel
             else:
                 launches = 2
             pin = lambda t: torch.empty_like(t, device="cpu").pin_memory()  # noqa: E731

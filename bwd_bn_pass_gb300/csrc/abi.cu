@@ -234,9 +234,10 @@ static int bn_finalize_apply_impl(const void* x, int dtype, int64_t B, int64_t C
     return to_status(bn_fused_forward(fp, dtype, x, y, gamma, beta, stats, running_mean,
                                       running_var, momentum, eps, act, slope,
                                       const_cast<void*>(ws), dev->status, st));
-  if (with_stats_pass && M <= g_small_max_m.load())
+  const int K = with_stats_pass ? bn_small_blocks(M, C, g_small_max_m.load(), *dev) : 0;
+  if (K > 0)
     return to_status(bn_small_forward(dtype, x, y, B, C, HW, gamma, beta, stats, running_mean,
-                                      running_var, momentum, eps, act, slope, st));
+                                      running_var, momentum, eps, act, slope, K, st));
   if (with_stats_pass) {
     cudaError_t e = bn_launch_stats(x, dtype, p, part, st);
     if (e != cudaSuccess) return GBN_ECUDA;
@@ -289,6 +290,17 @@ int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes) {
 int64_t gbn_bn_persistent_min_bytes(void) { return g_fused_min_bytes.load(); }
 
 int64_t gbn_bn_small_max_elems(void) { return g_small_max_m.load(); }
+
+int gbn_bn_small_blocks_per_channel(int64_t B, int64_t C, int64_t HW) {
+  int64_t M;
+  if (bn_check(GBN_F32, B, C, HW, false, &M) != GBN_OK) return 0;
+  const DevInfo* dev = device_info(-1);
+  if (dev == nullptr) {
+    cudaGetLastError();
+    return 0;
+  }
+  return bn_small_blocks(M, C, g_small_max_m.load(), *dev);
+}
 
 int64_t gbn_bn_set_small_max_elems(int64_t m) {
   if (m < 0) m = 0;
@@ -389,9 +401,10 @@ static int bn_backward_impl(const void* x, const void* dy, int dtype, int64_t B,
       ws_bytes >= fp.ws_bytes)
     return to_status(bn_fused_backward(fp, dtype, x, dy, dx, stats, beta, act, slope, grads,
                                        const_cast<void*>(ws), dev->status, st));
-  if (sums && finalize && M <= g_small_max_m.load())
+  const int K = sums && finalize ? bn_small_blocks(M, C, g_small_max_m.load(), *dev) : 0;
+  if (K > 0)
     return to_status(bn_small_backward(dtype, x, dy, dx, B, C, HW, stats, beta, act, slope,
-                                       grads, st));
+                                       grads, K, st));
   if (sums) {
     cudaError_t e = bn_launch_grad_sums(x, dy, dtype, p, stats, part, beta, act, slope, st);
     if (e != cudaSuccess) return GBN_ECUDA;

@@ -89,15 +89,29 @@ cudaError_t bn_launch_dx(const void* x, const void* dy, void* dx, int dtype, con
                          int act, float slope, cudaStream_t st, bool pdl);
 
 // Single-launch BatchNorm for small channels (bn_small.cu): one block per
-// channel holds the channel's M <= kBnSmallMaxM elements in registers.
+// channel stages the channel's M <= lim elements in shared memory; up to
+// kBnClusterMax * lim elements, a cluster of up to kBnClusterMax blocks per
+// channel, each staging a share of at most lim (lim <= kBnSmallMaxM).
 constexpr int64_t kBnSmallMaxM = 2048;
+constexpr int kBnClusterMax = 8;
+// Resident 256-thread blocks per SM the small-channel kernels are sized for
+// (at most 64 registers a thread).
+constexpr int kBnSmallBlocksPerSm = 4;
+// Blocks per channel K (1, 2, 4 or 8) with which the small-channel kernels
+// take a shape: the smallest K whose shares hold at most lim elements, and
+// only while the grid is one latency chain per block (load, reduce,
+// finalize, store) with no second wave: one block per channel while the C
+// blocks fit kBnSmallBlocksPerSm per SM; a cluster while the C*K blocks fit
+// one per SM (measured: 148 blocks beat the two-launch kernels by ~0.5 us,
+// 256 tie, 608 lose by ~3 us).  0: not eligible.
+int bn_small_blocks(int64_t M, int64_t C, int64_t lim, const DevInfo& dev);
 cudaError_t bn_small_forward(int dtype, const void* x, void* y, int64_t B, int64_t C,
                              int64_t HW, const float* gamma, const float* beta, float* stats,
                              float* running_mean, float* running_var, float momentum, float eps,
-                             int act, float slope, cudaStream_t st);
+                             int act, float slope, int K, cudaStream_t st);
 cudaError_t bn_small_backward(int dtype, const void* x, const void* dy, void* dx, int64_t B,
                               int64_t C, int64_t HW, const float* stats, const float* beta,
-                              int act, float slope, float* grads, cudaStream_t st);
+                              int act, float slope, float* grads, int K, cudaStream_t st);
 
 // Persistent single-launch BatchNorm (bn_fused.cu): one CTA per SM owns a
 // contiguous range of the channel-major view; see that file.

@@ -31,9 +31,9 @@ namespace {
 // The single-launch persistent kernel also needs its per-CTA flags (16 bytes
 // per SM) and its own partials; it runs whenever those fit the array too
 // (and the call's size threshold selects it), otherwise the two-launch
-// kernels do.  Channels of at most 2048 elements run the single-launch
-// small-channel kernels, which use no scratch (the size check above still
-// applies to them).
+// kernels do.  Channels of at most 8 x 2048 elements run the single-launch
+// small-channel kernels (a block or a cluster of blocks per channel), which
+// use no scratch (the size check above still applies to them).
 constexpr size_t kNoAllocScratchBytes = 64 * 1024;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];

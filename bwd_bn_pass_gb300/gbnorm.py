@@ -63,6 +63,7 @@ _SIGNATURES = {
     "gbn_bn_set_persistent_min_bytes": (_I64, [_I64]),
     "gbn_bn_set_small_max_elems": (_I64, [_I64]),
     "gbn_bn_small_max_elems": (_I64, []),
+    "gbn_bn_small_blocks_per_channel": (_INT, [_I64, _I64, _I64]),
     "gbn_bn_persistent_min_bytes": (_I64, []),
     "gbn_bn_set_wide_offsets": (_INT, [_INT]),
     "gbn_bn_set_persistent_tmem": (_INT, [_INT]),
@@ -214,9 +215,11 @@ def bn_set_persistent_min_bytes(nbytes):
 
 
 def bn_set_small_max_elems(m):
-    """Per-channel element count up to which the composite BatchNorm calls
-    run the single-launch small-channel kernels (default and maximum 2048;
-    0 disables them).  Returns the previous value."""
+    """Per-block element limit of the composite BatchNorm calls'
+    single-launch small-channel kernels (default and maximum 2048; 0
+    disables them): a channel of at most m elements takes one block, one of
+    at most 8*m a thread-block cluster of 2, 4 or 8 blocks.  Returns the
+    previous value."""
     return lib().gbn_bn_set_small_max_elems(int(m))
 
 
@@ -226,6 +229,18 @@ def bn_persistent_min_bytes():
 
 def bn_small_max_elems():
     return lib().gbn_bn_small_max_elems()
+
+
+def bn_small_blocks_per_channel(shape):
+    """Blocks per channel (1, 2, 4 or 8) with which the composite BatchNorm
+    calls run an NCHW shape in the single-launch small-channel kernels on
+    the current device (below the persistent kernel's threshold), or 0 for
+    the two-launch kernels."""
+    B, C = shape[0], shape[1]
+    HW = 1
+    for d in shape[2:]:
+        HW *= d
+    return lib().gbn_bn_small_blocks_per_channel(int(B), int(C), int(HW))
 
 
 def bn_set_persistent_tmem(enable):

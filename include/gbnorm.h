@@ -167,16 +167,30 @@ GBN_API int64_t gbn_bn_set_persistent_min_bytes(int64_t bytes);
 GBN_API int64_t gbn_bn_persistent_min_bytes(void);
 
 /* Below the persistent kernel's threshold, the composite calls run channels
- * of at most this many elements (M = B*HW per channel) in ONE launch: a
- * block per channel stages the channel in shared memory as it reads it
- * once, reduces, finalizes and writes the outputs ([P4]'s stats / finalize
- * / apply, or grad_sums / finalize / dx, fused for latency-bound shapes).  Default and maximum
- * 2048; 0 sends every shape to the two-launch kernels.  Results are within
- * the parity tolerance of the other paths.  Process-wide; returns the
- * previous value.  The pages have no counterpart: a tuning knob.           */
+ * of at most 8 * m elements (M = B*HW per channel), m this limit, in ONE
+ * launch while the grid is a single wave (gbn_bn_small_blocks_per_channel) ([P4]'s stats / finalize / apply, or grad_sums / finalize / dx,
+ * fused for latency-bound shapes): a channel of at most m elements takes a
+ * block that stages it in shared memory as it reads it once, reduces,
+ * finalizes and writes the outputs; a larger one a thread-block cluster of
+ * K = 2, 4 or 8 blocks (the smallest K whose shares hold at most m
+ * elements), whose partial sums meet in distributed shared memory behind
+ * the cluster barrier.  Default and maximum 2048; 0 sends every shape to
+ * the two-launch kernels.  Results are within the parity tolerance of the
+ * other paths.  Process-wide; returns the previous value.  The pages have
+ * no counterpart: a tuning knob.                                           */
 GBN_API int64_t gbn_bn_set_small_max_elems(int64_t m);
 /* The current limit (elements per channel).                               */
 GBN_API int64_t gbn_bn_small_max_elems(void);
+/* Blocks per channel (1, 2, 4 or 8) with which the composite calls, below
+ * the persistent kernel's threshold, run an NCHW [B, C, HW] shape in the
+ * single-launch small-channel kernels on the current device, or 0 when they
+ * run the two-launch kernels: eligible are channels of at most 8 * m
+ * elements (m the limit above) whose blocks run as one latency chain each
+ * with no second wave -- one block per channel (K = 1) while C is at most 4
+ * blocks per SM, a cluster (K > 1) while C * K is at most the SM count;
+ * beyond that the two-launch kernels are faster.  Host arithmetic and a
+ * cached device query only; 0 also for invalid dimensions.                */
+GBN_API int gbn_bn_small_blocks_per_channel(int64_t B, int64_t C, int64_t HW);
 
 /* The persistent BatchNorm kernel keeps a few stages per SM in tensor
  * memory (TMEM) between its reduction and output passes, instead of loading

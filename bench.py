@@ -39,6 +39,7 @@ bounded sample of the same workload on the host cores (rank 0 only).
 """
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -445,11 +446,21 @@ def run_ours(args, rank, world, local_rank):
                 evs.append(e)
             record.append((op, evs))
 
-    for _ in range(args.warmup):
-        one_step([])
-    barrier()
+    # The events bracket device work only, but a call's host-side cost
+    # (~25 us for a BatchNorm call) overlaps the L2 flush only as long as the
+    # host does not stall; a garbage-collector pause longer than the flush
+    # would land inside an operation's events.  As timeit does, the
+    # collector stays off while the GPU legs are timed.
+    gc.collect()
+    gc.disable()
     rec = []
     with ClockSampler(local_rank) as clk:
+        # the warm-up runs after the sampler has started (it waits 0.3 s for
+        # nvidia-smi): a GPU left idle that long takes its first call of the
+        # timed region several times slower (measured: 100 us for a 23 us
+        # call), so the idle gap belongs before the warm-up, not after it
+        for _ in range(args.warmup):
+            one_step([])
         barrier()
         t0 = time.perf_counter()
         for _ in range(args.steps):
@@ -530,6 +541,7 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(ops, stream, dev, args.steps, world)
+    gc.enable()
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -541,7 +553,8 @@ def run_ours(args, rank, world, local_rank):
             "ops": names,
             "l2": "before every operation: 256 MB write + 256 MB read of another buffer "
                   "(outside the timed events; L2 left clean)",
-            "timing": "CUDA events per operation on the launching stream; sum over ops",
+            "timing": "CUDA events per operation on the launching stream; sum over ops; "
+                      "Python's garbage collector off while the GPU legs are timed",
             "warm_l2": "ops.*.us_warm_l2: the same calls back to back without the flush "
                        "(labelled, not used in value)",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
